@@ -1,0 +1,361 @@
+/*
+ * moe_oracle.c -- plain, slow CPU oracle for one mixture-of-experts layer
+ * forward pass: route -> dispatch -> expert compute -> combine.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference legs of bench.py may load this file.  It shares no
+ * code, header, table or helper with the CUDA library in
+ * expert_dispatch_top_b300/csrc, and the CUDA library never calls it.
+ *
+ * The four steps follow the Ultralytics glossary page "Expert Parallelism",
+ * section "How Tokens Move Between GPUs" (steps 1-4: Route, Dispatch,
+ * Compute, Combine), and the ai360xpert page "Expert Parallelism", section
+ * "The All-to-All Bottleneck" (Routing, Scatter, Compute, Gather).  On one
+ * device both all-to-all exchanges become an on-device permutation into an
+ * expert-major buffer whose contiguous expert blocks are the virtual
+ * expert-parallel ranks (mbrenndoerfer.com "Expert Parallelism > Summary":
+ * uniform placement; Ultralytics snippet: experts 0-1 on GPU 0, 2-3 on GPU 1).
+ *
+ * Arithmetic: every sum is an fp64 sum taken in index order, with no FMA
+ * contraction (built with -ffp-contract=off) and no reassociation.  Where a
+ * floating-point value decides an integer (the top-k selection), the value is
+ * first brought to fp32, the precision the device path decides in:
+ *   logit  L = fp32( sum_i x_i * w_i )  [+ fp32 logit bias, one fp32 add]
+ *   softmax routers select on L (softmax is monotone in L);
+ *   sigmoid routers select on fp32( 1 / (1 + exp(-L)) ) [+ selection bias,
+ *   one fp32 add].
+ * Inputs on the dyadic grid (x multiples of 1/8, weights multiples of 1/512,
+ * d <= 8192) make every partial sum exact, so L does not depend on the order.
+ *
+ * Readings taken where the pages are silent (all listed in the design doc):
+ *   - ties in the selection key go to the lower expert index;
+ *   - capacity C = ceil(cf * T * k / E) (Ultralytics "Load Balancing and
+ *     Capacity": a fixed number of tokens per expert, e.g. 1.25x the even
+ *     share), or an explicit C; overflow is decided per (token, expert)
+ *     assignment in token order; surviving gates of a partly dropped token
+ *     are not renormalised;
+ *   - a dropped assignment contributes nothing to the MoE output; with the
+ *     residual added, a fully dropped token leaves the layer as it came in
+ *     (ai360xpert "Load Balancing and Dropped Tokens", capacity limits;
+ *     Ultralytics "Load Balancing and Capacity": skipped tokens ride the
+ *     residual path);
+ *   - source rank of token t is t / ceil(T/R); expert e lives on rank
+ *     e / (E/R);
+ *   - expert FFNs have no biases; GELU is the exact erf form; SwiGLU is
+ *     silu(gate) * up followed by the down projection.
+ *
+ * Parallelism: OpenMP over independent tokens / rows only; nothing in the
+ * arithmetic of one token depends on the thread count.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_F32 = 0, OR_BF16 = 1 };
+enum { OR_SOFTMAX = 0, OR_SIGMOID = 1 };
+enum { OR_GELU = 0, OR_SWIGLU = 1, OR_IDENTITY = 2 };
+
+/* Exact widening of one stored element to double. */
+static double elem(const void* base, int dtype, int64_t i) {
+    if (dtype == OR_BF16) {
+        uint16_t h = ((const uint16_t*)base)[i];
+        uint32_t bits = ((uint32_t)h) << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float*)base)[i];
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 1: Route (Ultralytics, How Tokens Move Between GPUs, step 1): each   */
+/* token gets a score per expert and the k best experts are kept.  The       */
+/* selection-only bias is DeepSeek-V3's per-expert bias that changes which   */
+/* experts win but not the weights (Ultralytics, Load Balancing and          */
+/* Capacity, bias-based balancing); it is supported for sigmoid scores.      */
+/* ------------------------------------------------------------------------ */
+
+/* The fp32 logit of token t against expert e. */
+static float logit32(const void* x, const void* w, int dtype, int64_t t, int e,
+                     int d, const float* logit_bias) {
+    double acc = 0.0;
+    for (int i = 0; i < d; ++i)
+        acc += elem(x, dtype, t * (int64_t)d + i) * elem(w, dtype, (int64_t)e * d + i);
+    float L = (float)acc;
+    if (logit_bias) L = L + logit_bias[e];
+    return L;
+}
+
+/* The fp32 sigmoid score used for selection and for sigmoid gates. */
+float oracle_sigmoid32(float L) {
+    return (float)(1.0 / (1.0 + exp(-(double)L)));
+}
+
+/*
+ * x [T,d], w_router [E,d] (row-major, dtype), logit_bias [E] or NULL,
+ * sel_bias [E] or NULL (sigmoid only).
+ * Outputs: topk_idx [T,k] in selection order (descending key, ties to the
+ * lower index), topk_gate [T,k], logits [T,E] (fp32, may be NULL).
+ * Returns 0, or -1 for an unsupported combination.
+ */
+int oracle_route(int64_t T, int d, int E, int k, int dtype, int score, int renorm,
+                 const void* x, const void* w_router, const float* logit_bias,
+                 const float* sel_bias, int32_t* topk_idx, float* topk_gate,
+                 float* logits_out) {
+    if (k < 1 || k > E) return -1;
+    if (score == OR_SOFTMAX && sel_bias) return -1;
+    int bad = 0;
+#pragma omp parallel
+    {
+        float* L = (float*)malloc(sizeof(float) * E);
+        float* key = (float*)malloc(sizeof(float) * E);
+        float* s = (float*)malloc(sizeof(float) * E);
+        char* taken = (char*)malloc(E);
+        if (!L || !key || !s || !taken) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (int64_t t = 0; t < T; ++t) {
+                for (int e = 0; e < E; ++e) {
+                    L[e] = logit32(x, w_router, dtype, t, e, d, logit_bias);
+                    if (score == OR_SIGMOID) {
+                        s[e] = oracle_sigmoid32(L[e]);
+                        key[e] = sel_bias ? s[e] + sel_bias[e] : s[e];
+                    } else {
+                        key[e] = L[e];
+                    }
+                    taken[e] = 0;
+                    if (logits_out) logits_out[t * E + e] = L[e];
+                }
+                /* k rounds: the largest key not yet taken; ascending scan and a
+                   strict comparison give ties to the lower index. */
+                int32_t* idx = topk_idx + t * k;
+                for (int j = 0; j < k; ++j) {
+                    int best = -1;
+                    for (int e = 0; e < E; ++e) {
+                        if (taken[e]) continue;
+                        if (best < 0 || key[e] > key[best]) best = e;
+                    }
+                    taken[best] = 1;
+                    idx[j] = best;
+                }
+                /* Gates: the router weights applied in step 4, Combine. */
+                float* g = topk_gate + t * k;
+                if (score == OR_SOFTMAX) {
+                    double m = -INFINITY;
+                    if (renorm) {
+                        for (int j = 0; j < k; ++j) m = fmax(m, (double)L[idx[j]]);
+                    } else {
+                        for (int e = 0; e < E; ++e) m = fmax(m, (double)L[e]);
+                    }
+                    double z = 0.0;
+                    if (renorm) {
+                        for (int j = 0; j < k; ++j) z += exp((double)L[idx[j]] - m);
+                    } else {
+                        for (int e = 0; e < E; ++e) z += exp((double)L[e] - m);
+                    }
+                    for (int j = 0; j < k; ++j) g[j] = (float)(exp((double)L[idx[j]] - m) / z);
+                } else {
+                    if (renorm) {
+                        double z = 0.0;
+                        for (int j = 0; j < k; ++j) z += (double)s[idx[j]];
+                        for (int j = 0; j < k; ++j) g[j] = (float)((double)s[idx[j]] / z);
+                    } else {
+                        for (int j = 0; j < k; ++j) g[j] = s[idx[j]];
+                    }
+                }
+            }
+        }
+        free(L);
+        free(key);
+        free(s);
+        free(taken);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 2: Dispatch, as counts, capacity and an on-device layout.           */
+/* ------------------------------------------------------------------------ */
+
+/* Capacity per expert: an explicit value, else ceil(cf*T*k/E) evaluated left
+   to right in double, else -1 (no limit). */
+int64_t oracle_capacity(int64_t T, int k, int E, double cf, int64_t explicit_cap) {
+    if (explicit_cap > 0) return explicit_cap;
+    if (!(cf > 0.0)) return -1;
+    return (int64_t)ceil(cf * (double)T * (double)k / (double)E);
+}
+
+/*
+ * topk_idx [T,k] -> per-expert load (pre-drop), expert-major row offsets of
+ * the kept rows [E+1], kept rows per virtual rank [R], the would-be
+ * all-to-all send counts [R,R] (source rank of the token, destination rank of
+ * the expert), slot_row [T,k] (row in the expert-major buffer, -1 if dropped),
+ * row_token [rows] (row -> token) and the number of dropped assignments.
+ * Token order is kept inside every expert segment (mbrenndoerfer.com
+ * Summary: the buffers must keep the tokens' order through dispatch, compute
+ * and combine).  Returns the number of kept rows.
+ */
+int64_t oracle_dispatch(int64_t T, int E, int k, int R, int64_t C, const int32_t* topk_idx,
+                        int32_t* expert_counts, int32_t* expert_offsets, int32_t* rank_counts,
+                        int32_t* rank_splits, int32_t* slot_row, int32_t* row_token,
+                        int64_t* n_dropped) {
+    int64_t* seen = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    int64_t* pos = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T * k > 0 ? T * k : 1));
+    if (!seen || !pos) {
+        free(seen);
+        free(pos);
+        return -1;
+    }
+    /* Position of each assignment among the assignments of the same expert,
+       counted in token order. */
+    for (int64_t t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            int e = topk_idx[t * k + j];
+            pos[t * k + j] = seen[e]++;
+        }
+    for (int e = 0; e < E; ++e) expert_counts[e] = (int32_t)seen[e];
+    /* Kept rows per expert and the exclusive prefix over experts. */
+    expert_offsets[0] = 0;
+    for (int e = 0; e < E; ++e) {
+        int64_t kept = seen[e];
+        if (C >= 0 && kept > C) kept = C;
+        expert_offsets[e + 1] = expert_offsets[e] + (int32_t)kept;
+    }
+    int per_rank = E / R;
+    int64_t tok_per_src = (T + R - 1) / R;
+    for (int r = 0; r < R; ++r) rank_counts[r] = 0;
+    for (int i = 0; i < R * R; ++i) rank_splits[i] = 0;
+    int64_t dropped = 0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            int e = topk_idx[t * k + j];
+            int64_t p = pos[t * k + j];
+            if (C >= 0 && p >= C) {
+                slot_row[t * k + j] = -1;
+                ++dropped;
+                continue;
+            }
+            int32_t row = expert_offsets[e] + (int32_t)p;
+            slot_row[t * k + j] = row;
+            row_token[row] = (int32_t)t;
+            int dst = e / per_rank;
+            int src = (int)(t / tok_per_src);
+            rank_counts[dst] += 1;
+            rank_splits[src * R + dst] += 1;
+        }
+    *n_dropped = dropped;
+    int64_t rows = expert_offsets[E];
+    free(seen);
+    free(pos);
+    return rows;
+}
+
+/* The permutation itself: each token's hidden state is written to the row of
+   every expert that kept it.  Elements are moved as raw bytes. */
+void oracle_permute(int64_t T, int k, int64_t row_bytes, const void* x, const int32_t* slot_row,
+                    void* xp) {
+    for (int64_t t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            int32_t row = slot_row[t * k + j];
+            if (row < 0) continue;
+            memcpy((char*)xp + (int64_t)row * row_bytes, (const char*)x + t * row_bytes,
+                   (size_t)row_bytes);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 3: Compute (step 3): every expert processes the rows dispatched to  */
+/* it.  One expert FFN applied to n_rows rows.                               */
+/* ------------------------------------------------------------------------ */
+
+static double gelu_exact(double v) { return 0.5 * v * (1.0 + erf(v / sqrt(2.0))); }
+static double silu(double v) { return v / (1.0 + exp(-v)); }
+
+/*
+ * rows [n_rows,d] (dtype), w_up [f,d] (GELU) or [2f,d] with gate rows first
+ * then up rows (SwiGLU), w_down [d,f]; out [n_rows,d] fp64, no intermediate
+ * rounding.  Identity: out = rows.
+ */
+void oracle_expert_ffn(int64_t n_rows, int d, int f, int act, int dtype, const void* rows,
+                       const void* w_up, const void* w_down, double* out) {
+    if (act == OR_IDENTITY) {
+        for (int64_t r = 0; r < n_rows; ++r)
+            for (int c = 0; c < d; ++c) out[r * d + c] = elem(rows, dtype, r * d + c);
+        return;
+    }
+#pragma omp parallel
+    {
+        double* xr = (double*)malloc(sizeof(double) * d);
+        double* h = (double*)malloc(sizeof(double) * f);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            for (int i = 0; i < d; ++i) xr[i] = elem(rows, dtype, r * d + i);
+            for (int n = 0; n < f; ++n) {
+                double a = 0.0;
+                for (int i = 0; i < d; ++i) a += xr[i] * elem(w_up, dtype, (int64_t)n * d + i);
+                if (act == OR_GELU) {
+                    h[n] = gelu_exact(a);
+                } else {
+                    double u = 0.0;
+                    for (int i = 0; i < d; ++i)
+                        u += xr[i] * elem(w_up, dtype, (int64_t)(f + n) * d + i);
+                    h[n] = silu(a) * u;
+                }
+            }
+            for (int c = 0; c < d; ++c) {
+                double a = 0.0;
+                for (int n = 0; n < f; ++n) a += h[n] * elem(w_down, dtype, (int64_t)c * f + n);
+                out[r * d + c] = a;
+            }
+        }
+        free(xr);
+        free(h);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 4: Combine (step 4): expert outputs come back to token order and    */
+/* are summed with the router gates as weights.                             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Tokens toks[0..n_tok) are produced into y [n_tok,d].  The expert-major
+ * buffer is addressed through slot_row: the output of row r is
+ * yp_rows[row_map[r] * d ...] (row_map lets a caller hold only the rows that
+ * the listed tokens use).  shared [n_tok,d] fp64 or NULL (always-on shared
+ * expert, gate 1); resid [T,d] (dtype) or NULL (the residual connection).
+ */
+void oracle_combine(int64_t n_tok, const int64_t* toks, int d, int k, const double* yp_rows,
+                    const int32_t* row_map, const int32_t* slot_row, const float* topk_gate,
+                    const double* shared, int dtype, const void* resid, double* y) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n_tok; ++i) {
+        int64_t t = toks[i];
+        double* yt = y + i * d;
+        for (int c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int32_t row = slot_row[t * k + j];
+                if (row < 0) continue;
+                acc += (double)topk_gate[t * k + j] * yp_rows[(int64_t)row_map[row] * d + c];
+            }
+            if (shared) acc += shared[i * d + c];
+            if (resid) acc += elem(resid, dtype, t * d + c);
+            yt[c] = acc;
+        }
+    }
+}
