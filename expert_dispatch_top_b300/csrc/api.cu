@@ -1,0 +1,395 @@
+// api.cu -- the C ABI declared in include/moe.h: argument checks, workspace
+// layout and the launch sequence of each step.  Host code only; every step of
+// the layer runs in the library's own kernels on the caller's stream.
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxRanks = 32;
+
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+inline int elem_bytes(const moe_config* c) { return c->act_dtype == MOE_DTYPE_F32 ? 4 : 2; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
+
+int64_t capacity_of(const moe_config* c) {
+    if (c->capacity > 0) return c->capacity;
+    if (c->capacity_factor > 0.f)
+        return (int64_t)ceil((double)c->capacity_factor * (double)c->T * (double)c->k / (double)c->E);
+    return -1;
+}
+
+int64_t max_rows_of(const moe_config* c) {
+    const int64_t tk = (int64_t)c->T * c->k;
+    const int64_t C = capacity_of(c);
+    if (C < 0) return tk;
+    const int64_t ec = (int64_t)c->E * C;
+    return ec < tk ? ec : tk;
+}
+
+// Byte offsets of every workspace section.
+struct Layout {
+    size_t status = 0, ticket = 4, done = 8;
+    size_t counts, desc, splits_acc;
+    size_t topk_idx, topk_gate, slot_row, row_token, expert_counts, offsets, rank_counts,
+        rank_splits, n_dropped;
+    size_t clear_bytes;  // bytes [4, clear_bytes) are zeroed before dispatch
+    size_t total;
+};
+
+Layout layout_of(const moe_config* c) {
+    Layout L;
+    size_t o = kAlign;
+    L.counts = o;
+    o = align_up(o + (size_t)c->E * 4);
+    L.clear_bytes = o;
+    L.desc = o;
+    o = align_up(o + (size_t)dispatch_blocks(c->T) * c->E * 8);
+    L.splits_acc = o;
+    o = align_up(o + (size_t)c->R * c->R * 4);
+    const size_t tk = (size_t)c->T * c->k;
+    L.topk_idx = o;
+    o = align_up(o + tk * 4);
+    L.topk_gate = o;
+    o = align_up(o + tk * 4);
+    L.slot_row = o;
+    o = align_up(o + tk * 4);
+    L.row_token = o;
+    o = align_up(o + (size_t)max_rows_of(c) * 4);
+    L.expert_counts = o;
+    o = align_up(o + (size_t)c->E * 4);
+    L.offsets = o;
+    o = align_up(o + (size_t)(c->E + 1) * 4);
+    L.rank_counts = o;
+    o = align_up(o + (size_t)c->R * 4);
+    L.rank_splits = o;
+    o = align_up(o + (size_t)c->R * c->R * 4);
+    L.n_dropped = o;
+    o = align_up(o + 4);
+    L.total = o;
+    return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status check_ffn_config(const moe_config* c) {
+    if (c->act == MOE_ACT_IDENTITY) return c->n_shared == 0 ? MOE_OK : MOE_ERR_INVALID_ARG;
+    if (c->d_ff < 1 || ((int64_t)c->d_ff * elem_bytes(c)) % 16 != 0) return MOE_ERR_INVALID_ARG;
+    if (c->act_dtype == MOE_DTYPE_BF16 && (c->d % 64 != 0 || c->d_ff % 64 != 0))
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status route_impl(const moe_config* c, const void* x, const void* w, const float* lb,
+                      const float* sb, int32_t* idx, float* gate, cudaStream_t s) {
+    if (c->T == 0) return MOE_OK;
+    if (!x || !w || !idx || !gate) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned4(idx) || !aligned4(gate) || !aligned4(lb) ||
+        !aligned4(sb))
+        return MOE_ERR_INVALID_ARG;
+    if (sb && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_UNSUPPORTED;
+    RouteArgs a;
+    a.x = x;
+    a.w = w;
+    a.logit_bias = lb;
+    a.sel_bias = sb;
+    a.idx = idx;
+    a.gate = gate;
+    a.T = c->T;
+    a.d = c->d;
+    a.E = c->E;
+    a.k = c->k;
+    a.score = c->score;
+    a.renorm = c->renorm;
+    a.dtype = c->act_dtype;
+    return cuda_status(launch_route(a, s));
+}
+
+moe_status dispatch_impl(const moe_config* c, const void* x, const int32_t* idx, void* xp,
+                         int32_t* row_token, int32_t* slot_row, int32_t* counts, int32_t* offsets,
+                         int32_t* rank_counts, int32_t* rank_splits, int32_t* n_dropped, void* ws,
+                         cudaStream_t s) {
+    if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    if (!counts || !offsets || !rank_counts || !n_dropped) return MOE_ERR_INVALID_ARG;
+    if (c->T > 0 && (!x || !idx || !xp || !row_token || !slot_row)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xp) || !aligned4(idx) || !aligned4(row_token) ||
+        !aligned4(slot_row) || !aligned4(counts) || !aligned4(offsets) || !aligned4(rank_counts) ||
+        !aligned4(rank_splits) || !aligned4(n_dropped))
+        return MOE_ERR_INVALID_ARG;
+    const Layout L = layout_of(c);
+    cudaError_t e = cudaMemsetAsync(at<char>(ws, 4), 0, L.clear_bytes - 4, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    DispatchArgs a;
+    a.x = x;
+    a.idx = idx;
+    a.xp = xp;
+    a.row_token = row_token;
+    a.slot_row = slot_row;
+    a.expert_counts = counts;
+    a.expert_offsets = offsets;
+    a.rank_counts = rank_counts;
+    a.rank_splits = rank_splits;
+    a.n_dropped = n_dropped;
+    a.status = at<uint32_t>(ws, L.status);
+    a.ticket = at<uint32_t>(ws, L.ticket);
+    a.done = at<uint32_t>(ws, L.done);
+    a.counts = at<int32_t>(ws, L.counts);
+    a.desc = at<uint64_t>(ws, L.desc);
+    a.splits_acc = at<int32_t>(ws, L.splits_acc);
+    a.T = c->T;
+    a.d = c->d;
+    a.E = c->E;
+    a.k = c->k;
+    a.R = c->R;
+    a.dtype = c->act_dtype;
+    a.C = capacity_of(c);
+    return cuda_status(launch_dispatch(a, s));
+}
+
+moe_status ffn_impl(const moe_config* c, const void* xp, const int32_t* offsets, const void* w_up,
+                    const void* w_down, void* h, void* yp, const void* shared_x,
+                    const void* shared_up, const void* shared_down, void* shared_h,
+                    void* shared_out, void* ws, cudaStream_t s) {
+    if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    const int64_t rows = max_rows_of(c);
+    const int eb = elem_bytes(c);
+    if (c->act == MOE_ACT_IDENTITY) {
+        if (!xp || !yp) return rows == 0 ? MOE_OK : MOE_ERR_INVALID_ARG;
+        if (xp == yp || rows == 0) return MOE_OK;
+        return cuda_status(cudaMemcpyAsync(yp, xp, (size_t)rows * c->d * eb,
+                                           cudaMemcpyDeviceToDevice, s));
+    }
+    if (!offsets || !w_up || !w_down || !aligned4(offsets) || !aligned16(w_up) || !aligned16(w_down))
+        return MOE_ERR_INVALID_ARG;
+    if (rows > 0 && (!xp || !h || !yp || !aligned16(xp) || !aligned16(h) || !aligned16(yp)))
+        return MOE_ERR_INVALID_ARG;
+    if (c->n_shared == 1 && c->T > 0) {
+        if (!shared_x || !shared_up || !shared_down || !shared_h || !shared_out ||
+            !aligned16(shared_x) || !aligned16(shared_up) || !aligned16(shared_down) ||
+            !aligned16(shared_h) || !aligned16(shared_out))
+            return MOE_ERR_INVALID_ARG;
+    }
+    const Layout L = layout_of(c);
+    uint32_t* status = at<uint32_t>(ws, L.status);
+    const bool tc = c->act_dtype == MOE_DTYPE_BF16;
+    auto run = [&](const GemmArgs& g) -> cudaError_t {
+        return tc ? launch_gemm_tc(g, s) : launch_gemm_simt(g, s);
+    };
+    // One pass per expert group set: routed experts (device offsets), then the
+    // shared expert over all T rows of shared_x.
+    for (int pass = 0; pass < 1 + (c->n_shared == 1 ? 1 : 0); ++pass) {
+        const bool shared = pass == 1;
+        GemmArgs up;
+        up.A = shared ? shared_x : xp;
+        up.B = shared ? shared_up : w_up;
+        up.out = shared ? shared_h : h;
+        up.offsets = shared ? nullptr : offsets;
+        up.rows_cap = shared ? c->T : rows;
+        up.m_rows = shared ? c->T : 0;
+        up.G = shared ? 1 : c->E;
+        up.N = c->d_ff;
+        up.K = c->d;
+        up.epi = c->act == MOE_ACT_SWIGLU ? EPI_SWIGLU : EPI_GELU;
+        up.dtype = c->act_dtype;
+        up.status = status;
+        GemmArgs down = up;
+        down.A = shared ? shared_h : h;
+        down.B = shared ? shared_down : w_down;
+        down.out = shared ? shared_out : yp;
+        down.N = c->d;
+        down.K = c->d_ff;
+        down.epi = EPI_NONE;
+        if (up.rows_cap == 0) continue;
+        if (tc && (gemm_tc_supported(up) != 0 || gemm_tc_supported(down) != 0))
+            return MOE_ERR_UNSUPPORTED;
+        cudaError_t e = run(up);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        e = run(down);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+moe_status combine_impl(const moe_config* c, const void* yp, const int32_t* slot_row,
+                        const float* gate, const void* shared_out, const void* resid, void* y,
+                        cudaStream_t s) {
+    if (c->T == 0) return MOE_OK;
+    if (!yp || !slot_row || !gate || !y) return MOE_ERR_INVALID_ARG;
+    if (c->add_residual && !resid) return MOE_ERR_INVALID_ARG;
+    if (c->n_shared == 1 && !shared_out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(yp) || !aligned16(y) || !aligned16(shared_out) || !aligned16(resid) ||
+        !aligned4(slot_row) || !aligned4(gate))
+        return MOE_ERR_INVALID_ARG;
+    CombineArgs a;
+    a.yp = yp;
+    a.slot_row = slot_row;
+    a.gate = gate;
+    a.shared = c->n_shared == 1 ? shared_out : nullptr;
+    a.resid = c->add_residual ? resid : nullptr;
+    a.y = y;
+    a.T = c->T;
+    a.d = c->d;
+    a.k = c->k;
+    a.dtype = c->act_dtype;
+    return cuda_status(launch_combine(a, s));
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: unsupported combination";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA call or launch failed";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded device wait gave up";
+        case MOE_ERR_NONFINITE: return "MOE_ERR_NONFINITE: non-finite input";
+        case MOE_ERR_BOUNDS: return "MOE_ERR_BOUNDS: index out of range";
+    }
+    return "unknown moe_status";
+}
+
+moe_status moe_check_config(const moe_config* c) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->T < 0 || c->d < 1 || c->d > 16384 || c->E < 1 || c->E > 256 || c->k < 1 || c->k > 8 ||
+        c->k > c->E || c->R < 1 || c->R > kMaxRanks || c->E % c->R != 0)
+        return MOE_ERR_INVALID_ARG;
+    if ((int64_t)c->T * c->k >= (1ll << 30)) return MOE_ERR_INVALID_ARG;
+    if (c->act_dtype != MOE_DTYPE_F32 && c->act_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+    if (c->act != MOE_ACT_GELU && c->act != MOE_ACT_SWIGLU && c->act != MOE_ACT_IDENTITY)
+        return MOE_ERR_INVALID_ARG;
+    if ((c->renorm != 0 && c->renorm != 1) || (c->add_residual != 0 && c->add_residual != 1))
+        return MOE_ERR_INVALID_ARG;
+    if (c->n_shared < 0 || c->n_shared > 1) return MOE_ERR_INVALID_ARG;
+    if (c->capacity < 0 || !(c->capacity_factor == c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+    if (((int64_t)c->d * elem_bytes(c)) % 16 != 0) return MOE_ERR_INVALID_ARG;
+    return check_ffn_config(c);
+}
+
+size_t moe_workspace_size(const moe_config* cfg) {
+    if (moe_check_config(cfg) != MOE_OK) return 0;
+    return layout_of(cfg).total;
+}
+
+int64_t moe_capacity(const moe_config* cfg) {
+    if (moe_check_config(cfg) != MOE_OK) return -1;
+    return capacity_of(cfg);
+}
+
+int64_t moe_max_rows(const moe_config* cfg) {
+    if (moe_check_config(cfg) != MOE_OK) return -1;
+    return max_rows_of(cfg);
+}
+
+moe_status moe_route(const moe_config* cfg, const void* x, const void* w_router,
+                     const float* logit_bias, const float* sel_bias, int32_t* topk_idx,
+                     float* topk_gate, void* ws, moe_stream_t stream) {
+    moe_status st = moe_check_config(cfg);
+    if (st != MOE_OK) return st;
+    (void)ws;
+    return route_impl(cfg, x, w_router, logit_bias, sel_bias, topk_idx, topk_gate,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, void* xp,
+                        int32_t* row_token, int32_t* slot_row, int32_t* expert_counts,
+                        int32_t* expert_offsets, int32_t* rank_counts, int32_t* rank_splits,
+                        int32_t* n_dropped, void* ws, moe_stream_t stream) {
+    moe_status st = moe_check_config(cfg);
+    if (st != MOE_OK) return st;
+    return dispatch_impl(cfg, x, topk_idx, xp, row_token, slot_row, expert_counts, expert_offsets,
+                         rank_counts, rank_splits, n_dropped, ws,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* expert_offsets,
+                          const void* w_up, const void* w_down, void* h, void* yp,
+                          const void* shared_x, const void* shared_up, const void* shared_down,
+                          void* shared_h, void* shared_out, void* ws, moe_stream_t stream) {
+    moe_status st = moe_check_config(cfg);
+    if (st != MOE_OK) return st;
+    return ffn_impl(cfg, xp, expert_offsets, w_up, w_down, h, yp, shared_x, shared_up, shared_down,
+                    shared_h, shared_out, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slot_row,
+                       const float* topk_gate, const void* shared_out, const void* x_residual,
+                       void* y, moe_stream_t stream) {
+    moe_status st = moe_check_config(cfg);
+    if (st != MOE_OK) return st;
+    return combine_impl(cfg, yp, slot_row, topk_gate, shared_out, x_residual, y,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router,
+                             const float* logit_bias, const float* sel_bias, const void* w_up,
+                             const void* w_down, const void* shared_up, const void* shared_down,
+                             const moe_buffers* buf, void* y, void* ws, moe_stream_t stream) {
+    moe_status st = moe_check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!buf || !ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const Layout L = layout_of(cfg);
+    int32_t* idx = buf->topk_idx ? buf->topk_idx : at<int32_t>(ws, L.topk_idx);
+    float* gate = buf->topk_gate ? buf->topk_gate : at<float>(ws, L.topk_gate);
+    int32_t* slot_row = buf->slot_row ? buf->slot_row : at<int32_t>(ws, L.slot_row);
+    int32_t* row_token = buf->row_token ? buf->row_token : at<int32_t>(ws, L.row_token);
+    int32_t* counts = buf->expert_counts ? buf->expert_counts : at<int32_t>(ws, L.expert_counts);
+    int32_t* offsets = buf->expert_offsets ? buf->expert_offsets : at<int32_t>(ws, L.offsets);
+    int32_t* rank_counts = buf->rank_counts ? buf->rank_counts : at<int32_t>(ws, L.rank_counts);
+    int32_t* rank_splits = buf->rank_splits ? buf->rank_splits : at<int32_t>(ws, L.rank_splits);
+    int32_t* n_dropped = buf->n_dropped ? buf->n_dropped : at<int32_t>(ws, L.n_dropped);
+    const bool identity = cfg->act == MOE_ACT_IDENTITY;
+    if (!buf->xp || (!identity && (!buf->h || !buf->yp))) return MOE_ERR_INVALID_ARG;
+    if (cfg->n_shared == 1 && (!shared_up || !shared_down || !buf->shared_h || !buf->shared_out))
+        return MOE_ERR_INVALID_ARG;
+    if (!y || (cfg->T > 0 && !x)) return MOE_ERR_INVALID_ARG;
+
+    st = route_impl(cfg, x, w_router, logit_bias, sel_bias, idx, gate, s);
+    if (st != MOE_OK) return st;
+    st = dispatch_impl(cfg, x, idx, buf->xp, row_token, slot_row, counts, offsets, rank_counts,
+                       rank_splits, n_dropped, ws, s);
+    if (st != MOE_OK) return st;
+    const void* yp = buf->xp;
+    if (!identity) {
+        st = ffn_impl(cfg, buf->xp, offsets, w_up, w_down, buf->h, buf->yp, x, shared_up, shared_down,
+                      buf->shared_h, buf->shared_out, ws, s);
+        if (st != MOE_OK) return st;
+        yp = buf->yp;
+    }
+    return combine_impl(cfg, yp, slot_row, gate, buf->shared_out, x, y, s);
+}
+
+moe_status moe_read_device_status(const void* ws, uint32_t* out, moe_stream_t stream) {
+    if (!ws || !out) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, ws, 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(const_cast<void*>(ws), 0, 4, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    *out = v;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+// combine.cu -- Step 4, Combine: gate-weighted un-permute back to token order.
+//
+// Ultralytics glossary "Expert Parallelism", "How Tokens Move Between GPUs",
+// step 4 (outputs return to their token and are summed with the router
+// gates as weights); ai360xpert "The All-to-All Bottleneck" (Gather).  A
+// dropped assignment (slot_row < 0) contributes nothing; the optional
+// residual carries a fully dropped token through unchanged (ai360xpert "Load
+// Balancing and Dropped Tokens"; Ultralytics "Load Balancing and Capacity").
+//
+// One warp per token, grid-stride; each lane moves 16-byte vectors.  The
+// k expert rows of a token are independent loads issued back to back, fp32
+// accumulation in slot order, one rounding to the output type.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+template <typename T>
+__global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
+    constexpr int V = Elem<T>::kPerVec;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int nvec = a.d / V;
+    const int64_t row_bytes = (int64_t)a.d * sizeof(T);
+    const char* yp = static_cast<const char*>(a.yp);
+    const char* sh = static_cast<const char*>(a.shared);
+    const char* rs = static_cast<const char*>(a.resid);
+    char* y = static_cast<char*>(a.y);
+    for (int64_t t = warp0; t < a.T; t += nwarps) {
+        int r_l = -1;
+        float g_l = 0.f;
+        if (lane < a.k) {
+            r_l = a.slot_row[t * a.k + lane];
+            g_l = a.gate[t * a.k + lane];
+        }
+        int r[8];
+        float g[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            r[j] = __shfl_sync(0xffffffffu, r_l, j);
+            g[j] = __shfl_sync(0xffffffffu, g_l, j);
+            if (j >= a.k) r[j] = -1;
+        }
+        for (int c = lane; c < nvec; c += 32) {
+            float acc[V];
+#pragma unroll
+            for (int q = 0; q < V; ++q) acc[q] = 0.f;
+            uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (r[j] >= 0) v[j] = ld_nc_v4(yp + (int64_t)r[j] * row_bytes + (int64_t)c * 16);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (r[j] >= 0) {
+                    float f[V];
+                    Elem<T>::unpack(v[j], f);
+#pragma unroll
+                    for (int q = 0; q < V; ++q) acc[q] = fmaf(g[j], f[q], acc[q]);
+                }
+            if (sh) {
+                float f[V];
+                Elem<T>::unpack(ld_nc_v4(sh + t * row_bytes + (int64_t)c * 16), f);
+#pragma unroll
+                for (int q = 0; q < V; ++q) acc[q] += f[q];
+            }
+            if (rs) {
+                float f[V];
+                Elem<T>::unpack(ld_nc_v4(rs + t * row_bytes + (int64_t)c * 16), f);
+#pragma unroll
+                for (int q = 0; q < V; ++q) acc[q] += f[q];
+            }
+            st_cs_v4(y + t * row_bytes + (int64_t)c * 16, Elem<T>::pack(acc));
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
+    if (a.T == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int64_t blocks = (a.T + 7) / 8;  // 8 warps (tokens) per block
+    const int64_t cap = (int64_t)sms * 16;
+    if (blocks > cap) blocks = cap;
+    if (a.dtype == MOE_DTYPE_F32)
+        combine_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(a);
+    else
+        combine_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,553 @@
+// ffn_tc.cu -- Step 3, Compute, for bf16 experts: a tcgen05 grouped GEMM.
+//
+// Ultralytics glossary "Expert Parallelism", "How Tokens Move Between GPUs",
+// step 3: every expert processes the rows dispatched to it.  The expert FFN
+// is the only dense contraction of the layer, so it runs on the 5th-gen
+// tensor cores:
+//
+//   out[rows of group g, :] = epi( A[rows, :K] . B[g]^T )
+//
+// with bf16 operands, fp32 accumulation in tensor memory (TMEM) and a fused
+// epilogue (GELU, SwiGLU = silu(gate) * up, or none) that rounds to bf16 once.
+//
+// Persistent, warp-specialised kernel, one CTA per SM (192 threads):
+//   warp 0     TMA producer: A tile 128 x 64 and B tile 256 x 64 (bf16,
+//              128-byte swizzle) per stage into a 4-stage shared-memory ring;
+//   warp 1     allocates 512 TMEM columns; one lane issues tcgen05.mma
+//              (M=128, N=256, K=16, kind::f16) into one of two 256-column
+//              accumulators and commits each stage back to the producer;
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (each warp owns the
+//              32 TMEM lanes its warp index allows), activation, bf16 pack,
+//              a padded shared-memory transpose and coalesced 128-byte row
+//              stores masked to the group's rows.  With two accumulators the
+//              epilogue of tile i overlaps the MMAs of tile i+1.
+//
+// Ragged groups: tiles are enumerated from the device-side row offsets, group
+// by group, n-tile by n-tile, m-tile fastest (the 148 concurrent tiles share
+// one group's A rows and a few of its weight tiles through L2).  A tile that
+// runs past its group's last row reads the next group's rows (or TMA's zero
+// fill past the buffer); those output rows are computed and never stored.
+// SwiGLU weights are [G, 2N, K] with the gate rows first: one B stage holds
+// 128 gate rows and the matching 128 up rows, so the accumulator holds gate
+// and up side by side and the epilogue writes 128 output columns per tile.
+//
+// Every mbarrier wait is bounded by %globaltimer: on timeout the kernel sets
+// MOE_DEV_GEMM_TIMEOUT, raises an abort flag seen by the other roles, drains
+// its own MMAs (bounded) and frees TMEM before returning.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;  // 16 KB
+constexpr int B_STAGE = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int EPI_WARPS = 4;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int STG_PITCH = 144;  // staged row: 128 data bytes + 16 pad (conflict-free)
+constexpr int STG_BYTES = EPI_WARPS * 32 * STG_PITCH;
+constexpr int MAX_GROUPS = 256;
+constexpr int TABLE_BYTES = 128 + 4 * MAX_GROUPS * 4;  // barriers + flags, then 4 int tables
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_BYTES + TABLE_BYTES;
+constexpr uint32_t TMEM_COLS = 512;
+
+// tcgen05 instruction descriptor, kind::f16: D fp32, A and B bf16, both
+// K-major, N = 256 (bits 17-22, N>>3), M = 128 (bits 24-28, M>>4).
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+struct TcParams {
+    const int32_t* offsets;
+    int64_t m_rows;
+    int G, N, K, epi;
+    int num_kb;
+    int n_tiles;
+    int out_cols;  // output columns per tile (128 SwiGLU, 256 otherwise)
+    __nv_bfloat16* out;
+    uint32_t* status;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of parity `parity`.  False on timeout or abort.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* status) {
+#pragma unroll 1
+    for (int i = 0; i < 128; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            atomicOr(status, MOE_DEV_GEMM_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                            int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, rows of 128 bytes,
+// 128-byte swizzle, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;            // leading byte offset (unused with this swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;            // descriptor version
+    d |= (uint64_t)2 << 61;            // SWIZZLE_128B
+    return d;
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accum)
+        : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns; waits for completion before the
+// registers are used.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ float gelu_f(float v) {
+    return 0.5f * v * (1.f + erff(v * 0.70710678118654752440f));
+}
+__device__ __forceinline__ float silu_f(float v) { return v / (1.f + __expf(-v)); }
+
+// Tile -> (group, n-tile, m-tile) from the per-group tile table.
+struct TileInfo {
+    int g, m_tile, n_tile, row0, rows;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int tile, int G, const int* tstart, const int* mt,
+                                                const int* rowoff, const int* grows, int n_tiles) {
+    int lo = 0, hi = G - 1;  // last g with tstart[g] <= tile
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tstart[mid] <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    TileInfo ti;
+    ti.g = lo;
+    const int local = tile - tstart[lo];
+    ti.n_tile = local / mt[lo];
+    ti.m_tile = local - ti.n_tile * mt[lo];
+    ti.row0 = rowoff[lo] + ti.m_tile * BM;
+    ti.rows = grows[lo] - ti.m_tile * BM;
+    if (ti.rows > BM) ti.rows = BM;
+    (void)n_tiles;
+    return ti;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* stg = smem + STAGES * STAGE_BYTES;
+    uint8_t* tbl = stg + STG_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(tbl);  // full[4] empty[4] accf[2] acce[2] drain
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tbl + 112);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tbl + 116);
+    int* total_s = reinterpret_cast<int*>(tbl + 120);
+    int* tstart = reinterpret_cast<int*>(tbl + 128);           // [MAX_GROUPS]
+    int* mt = tstart + MAX_GROUPS;                              // [MAX_GROUPS]
+    int* rowoff = mt + MAX_GROUPS;                              // [MAX_GROUPS]
+    int* grows = rowoff + MAX_GROUPS;                           // [MAX_GROUPS]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+    const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
+    const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(acce0 + 8 * b, EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp == 2) {
+        // Per-group tile table: lane l covers groups [8l, 8l+8).
+        int cnt[8];
+        int sum = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int g = lane * 8 + q;
+            cnt[q] = 0;
+            if (g < p.G) {
+                const int lo = p.offsets ? p.offsets[g] : 0;
+                const int hi = p.offsets ? p.offsets[g + 1] : (int)p.m_rows;
+                const int m = (hi - lo + BM - 1) / BM;
+                mt[g] = m > 0 ? m : 1;
+                rowoff[g] = lo;
+                grows[g] = hi - lo;
+                cnt[q] = m * p.n_tiles;
+                sum += cnt[q];
+            }
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int g = lane * 8 + q;
+            if (g < p.G) tstart[g] = run;
+            run += cnt[q];
+        }
+        if (lane == 31) *total_s = incl;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = *total_s;
+    const int n_tiles = p.n_tiles;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+                const TileInfo ti = decode_tile(tile, p.G, tstart, mt, rowoff, grows, n_tiles);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status)) break;
+                    const uint32_t fb = full0 + 8 * stage;
+                    mbar_expect_tx(fb, STAGE_BYTES);
+                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_STAGE;
+                    const int k0 = kb * BK;
+                    tma_load_2d(sa, &tmA, k0, ti.row0, fb);
+                    if (p.epi == EPI_SWIGLU) {
+                        tma_load_3d(sb, &tmB, k0, ti.n_tile * 128, ti.g, fb);
+                        tma_load_3d(sb + B_STAGE / 2, &tmB, k0, p.N + ti.n_tile * 128, ti.g, fb);
+                    } else {
+                        tma_load_3d(sb, &tmB, k0, ti.n_tile * BN, ti.g, fb);
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_STAGE;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        tc_mma(d_tmem, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32),
+                               (kb | kk) != 0 ? 1u : 0u);
+                    tc_commit(empty0 + 8 * stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(accf0 + 8 * acc);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            if (!ok) {
+                // drain this thread's MMAs before TMEM is released (bounded)
+                tc_commit(drain);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        uint8_t* my_stg = stg + (warp - 2) * (32 * STG_PITCH);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            const TileInfo ti = decode_tile(tile, p.G, tstart, mt, rowoff, grows, n_tiles);
+            // every lane waits, then the warp agrees, so the .sync.aligned TMEM loads
+            // below always run converged
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(accf0 + 8 * acc, acc_phase, abort_flag, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            const int col0 = ti.n_tile * p.out_cols;
+            for (int c64 = 0; c64 < p.out_cols / 64; ++c64) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int col = c64 * 64 + h * 32;
+                    float v[32];
+                    tmem_ld32(tbase + (uint32_t)col, v);
+                    if (p.epi == EPI_SWIGLU) {
+                        float u[32];
+                        tmem_ld32(tbase + (uint32_t)(128 + col), u);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i]) * u[i];
+                    } else if (p.epi == EPI_GELU) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
+                    }
+                    uint8_t* dst = my_stg + lane * STG_PITCH + h * 64;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 w;
+                        w.x = Elem<__nv_bfloat16>::pack2(v[8 * i + 0], v[8 * i + 1]);
+                        w.y = Elem<__nv_bfloat16>::pack2(v[8 * i + 2], v[8 * i + 3]);
+                        w.z = Elem<__nv_bfloat16>::pack2(v[8 * i + 4], v[8 * i + 5]);
+                        w.w = Elem<__nv_bfloat16>::pack2(v[8 * i + 6], v[8 * i + 7]);
+                        *reinterpret_cast<uint4*>(dst + 16 * i) = w;
+                    }
+                }
+                __syncwarp();
+                // 32 rows x 128 bytes: 8 lanes per row, 4 rows per pass
+                const int gc = col0 + c64 * 64 + (lane & 7) * 8;
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int r = it * 4 + (lane >> 3);
+                    const int lr = q * 32 + r;  // row inside the tile
+                    if (lr < ti.rows && gc < p.N) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(my_stg + r * STG_PITCH +
+                                                                        (lane & 7) * 16);
+                        st_v4(p.out + (int64_t)(ti.row0 + q * 32 + r) * p.N + gc, w);
+                    }
+                }
+                __syncwarp();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+}  // namespace
+
+int gemm_tc_supported(const GemmArgs& a) {
+    if (a.dtype != MOE_DTYPE_BF16) return 1;
+    if (a.K % BK != 0 || a.N % 64 != 0) return 2;
+    if (a.G < 1 || a.G > MAX_GROUPS) return 3;
+    if (a.rows_cap >= (1ll << 31) || a.K > (1 << 20)) return 4;
+    if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B) |
+         reinterpret_cast<uintptr_t>(a.out)) & 15)
+        return 5;
+    return 0;
+}
+
+cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
+    if (gemm_tc_supported(a) != 0) return cudaErrorInvalidValue;
+    const int64_t rows_cap = a.offsets ? a.rows_cap : a.m_rows;
+    if (rows_cap <= 0) return cudaSuccess;
+    auto encode = get_encode();
+    if (!encode) return cudaErrorNotSupported;
+
+    const bool gated = a.epi == EPI_SWIGLU;
+    const int b_rows = gated ? 2 * a.N : a.N;
+    CUtensorMap tmA, tmB;
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)rows_cap};
+        cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
+        cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+        cuuint32_t es[2] = {1, 1};
+        CUresult r = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.A), dims,
+                            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)a.K, (cuuint64_t)b_rows, (cuuint64_t)a.G};
+        cuuint64_t strides[2] = {(cuuint64_t)a.K * 2, (cuuint64_t)b_rows * a.K * 2};
+        cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)(gated ? 128 : BN), 1};
+        cuuint32_t es[3] = {1, 1, 1};
+        CUresult r = encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.B), dims,
+                            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    TcParams p;
+    p.offsets = a.offsets;
+    p.m_rows = a.m_rows;
+    p.G = a.offsets ? a.G : 1;
+    p.N = a.N;
+    p.K = a.K;
+    p.epi = a.epi;
+    p.num_kb = a.K / BK;
+    p.out_cols = gated ? 128 : BN;
+    p.n_tiles = (a.N + p.out_cols - 1) / p.out_cols;
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.status = a.status;
+
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t tiles_bound = ((rows_cap + BM - 1) / BM + p.G) * p.n_tiles;
+    int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
+    if (grid < 1) grid = 1;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e =
+            cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    tc_gemm_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

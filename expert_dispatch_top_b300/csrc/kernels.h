@@ -1,0 +1,77 @@
+// kernels.h -- host-side launchers of the library's kernels (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+struct RouteArgs {
+    const void* x;
+    const void* w;
+    const float* logit_bias;
+    const float* sel_bias;
+    int32_t* idx;
+    float* gate;
+    int64_t T;
+    int d, E, k, score, renorm, dtype;
+};
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+
+struct DispatchArgs {
+    const void* x;
+    const int32_t* idx;
+    void* xp;
+    int32_t* row_token;
+    int32_t* slot_row;
+    int32_t* expert_counts;
+    int32_t* expert_offsets;
+    int32_t* rank_counts;
+    int32_t* rank_splits;  // may be null
+    int32_t* n_dropped;
+    // workspace pieces
+    uint32_t* status;
+    uint32_t* ticket;
+    uint32_t* done;
+    int32_t* counts;     // [E] accumulation
+    uint64_t* desc;      // [n_blk, E] lookback descriptors
+    int32_t* splits_acc; // [R*R] accumulation (used when rank_splits is null)
+    int64_t T;
+    int d, E, k, R, dtype;
+    int64_t C;           // < 0: no limit
+};
+// Header bytes of the workspace that dispatch clears before it runs.
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
+int64_t dispatch_blocks(int64_t T);
+
+struct CombineArgs {
+    const void* yp;
+    const int32_t* slot_row;
+    const float* gate;
+    const void* shared;
+    const void* resid;
+    void* y;
+    int64_t T;
+    int d, k, dtype;
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+
+// Epilogue of one grouped GEMM: out = epi(A . B^T).
+enum Epilogue { EPI_NONE = 0, EPI_GELU = 1, EPI_SWIGLU = 2 };
+
+struct GemmArgs {
+    const void* A;          // [rows_cap, K] row-major
+    const void* B;          // [G, b_rows, K] row-major (b_rows = N, or 2N for SwiGLU)
+    void* out;              // [rows_cap, N]
+    const int32_t* offsets; // [G+1] device row offsets, or null: one group of m_rows rows
+    int64_t rows_cap;       // rows the A/out buffers hold
+    int64_t m_rows;         // rows of the single group when offsets is null
+    int G, N, K, epi, dtype;
+    uint32_t* status;
+};
+cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s);
+// Returns 0 if the tensor-core grouped GEMM supports the shape, else non-zero.
+int gemm_tc_supported(const GemmArgs& a);
+
+}  // namespace moe

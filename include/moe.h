@@ -1,0 +1,241 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) mixture-of-experts layer hot path.
+ *
+ * One MoE layer forward pass in the four steps of the Ultralytics glossary
+ * page "Expert Parallelism", section "How Tokens Move Between GPUs": Route,
+ * Dispatch, Compute, Combine.  On one GPU the two all-to-all exchanges of
+ * that section become on-device permutations: dispatch writes an
+ * expert-major buffer whose contiguous expert blocks are the virtual
+ * expert-parallel ranks (expert e lives on rank e / (E/R), the uniform
+ * placement of mbrenndoerfer.com "Expert Parallelism > Summary"), and
+ * combine gathers it back into token order.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All pointers are DEVICE pointers on the current CUDA device unless a
+ *    parameter says otherwise; the caller owns every buffer.  The library
+ *    never allocates or frees device memory and keeps no global state.
+ *  - Every pointer must be 16-byte aligned; tensors are dense and row-major.
+ *  - Activations and expert/router weights share one storage type,
+ *    cfg->act_dtype (fp32 or bf16).  Router logits, gates and every
+ *    accumulation are fp32.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream).  No entry point synchronises the stream, except
+ *    moe_read_device_status.
+ *  - Argument errors are returned synchronously before anything is
+ *    enqueued.  A failed launch returns MOE_ERR_CUDA.  Errors found on the
+ *    device (a bounded wait that timed out, an index out of range) are
+ *    recorded in the status word at the start of the workspace and read with
+ *    moe_read_device_status.  No entry point traps, aborts or throws.
+ *  - Calls on different streams need separate workspaces.
+ *
+ * Limits: 1 <= T, T*k < 2^30; 1 <= k <= min(E, 8); 1 <= E <= 256; R >= 1 and
+ * E % R == 0; d and d_ff multiples of 64 for bf16 (4 for fp32); d <= 16384.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (binary-compatible typedef; no CUDA header needed). */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or limit */
+    MOE_ERR_UNSUPPORTED = 2,  /* a valid combination this build does not run */
+    MOE_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    MOE_ERR_TIMEOUT = 4,      /* a bounded device wait gave up (status word) */
+    MOE_ERR_NONFINITE = 5,    /* reserved: non-finite input detected */
+    MOE_ERR_BOUNDS = 6        /* an index left its range (status word) */
+} moe_status;
+
+enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 };
+enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
+enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1, MOE_ACT_IDENTITY = 2 };
+
+/* Bits of the device status word (first 4 bytes of the workspace). */
+#define MOE_DEV_LOOKBACK_TIMEOUT 0x1u /* dispatch scan waited too long on a predecessor */
+#define MOE_DEV_GEMM_TIMEOUT 0x2u     /* expert GEMM pipeline wait gave up */
+#define MOE_DEV_BAD_INDEX 0x4u        /* an expert index outside [0, E) reached dispatch */
+
+/*
+ * Layer shape and method switches.
+ *   T tokens, d = d_model, E routed experts, k experts per token, R virtual
+ *   expert-parallel ranks (contiguous blocks of E/R experts), d_ff expert
+ *   hidden size, n_shared always-on shared experts (0 or 1; gate 1, run on
+ *   every token -- DeepSeek-V3-style).
+ *   score: softmax or sigmoid router scores.  renorm: gates normalised over
+ *   the chosen k; otherwise a gate is the full softmax probability or the
+ *   plain sigmoid score.
+ *   capacity: > 0 is an explicit per-expert capacity C; otherwise
+ *   capacity_factor > 0 gives C = ceil(capacity_factor * T * k / E)
+ *   (Ultralytics "Load Balancing and Capacity": at most a fixed number of
+ *   tokens per expert, e.g. 1.25x the even share); otherwise no limit.
+ *   Overflow is decided per (token, expert) assignment in token order.
+ *   act: expert FFN form (GELU: down(gelu(up x)); SWIGLU: down(silu(gate x)
+ *   * (up x)); IDENTITY: the expert returns its input).  No biases.
+ *   add_residual: combine adds x to the MoE output, so a fully dropped token
+ *   leaves the layer unchanged.
+ */
+typedef struct moe_config {
+    int32_t T;
+    int32_t d;
+    int32_t E;
+    int32_t k;
+    int32_t R;
+    int32_t d_ff;
+    int32_t n_shared;
+    int32_t act_dtype;      /* MOE_DTYPE_* */
+    int32_t score;          /* MOE_SCORE_* */
+    int32_t renorm;         /* 0 or 1 */
+    float capacity_factor;  /* <= 0: none (unless capacity > 0) */
+    int32_t capacity;       /* > 0: explicit per-expert capacity */
+    int32_t act;            /* MOE_ACT_* */
+    int32_t add_residual;   /* 0 or 1 */
+} moe_config;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* moe_status_string(moe_status s);
+
+/* Checks cfg against the limits above; MOE_OK or the reason it fails. */
+moe_status moe_check_config(const moe_config* cfg);
+
+/* Workspace bytes for cfg (0 if cfg is invalid).  The workspace holds the
+   device status word, the dispatch scan state and the default metadata
+   arrays of moe_layer_forward.  Caller-allocated, 256-byte aligned; it need
+   not be initialised, except that the status word should be zeroed once
+   (moe_read_device_status does this). */
+size_t moe_workspace_size(const moe_config* cfg);
+
+/* Per-expert capacity C in force for cfg (-1: no limit). */
+int64_t moe_capacity(const moe_config* cfg);
+
+/* Rows the expert-major buffers (xp, h, yp) must hold: min(T*k, E*C), or
+   T*k without a capacity limit. */
+int64_t moe_max_rows(const moe_config* cfg);
+
+/*
+ * Step 1, Route (Ultralytics "How Tokens Move Between GPUs", step 1): every
+ * token is scored against every expert and the k best experts are kept.
+ *   x [T,d], w_router [E,d] (act dtype).  logit_bias [E] fp32 or NULL is
+ *   added to each logit (it moves both the selection and the gates).
+ *   sel_bias [E] fp32 or NULL is DeepSeek-V3's selection-only bias
+ *   (Ultralytics "Load Balancing and Capacity", bias-based balancing):
+ *   added to the fp32 sigmoid score for the selection only; sigmoid scores
+ *   only (MOE_ERR_UNSUPPORTED with softmax).
+ *   logit L[t,e] = fp32 sum_i x[t,i] * w_router[e,i] (+ logit_bias[e]).
+ *   Selection key: L (softmax) or fp32(1/(1+exp(-L))) (+ sel_bias) (sigmoid).
+ * Outputs: topk_idx [T,k] int32, experts in descending key order with ties
+ * to the lower expert index; topk_gate [T,k] fp32.  ws: workspace.
+ */
+moe_status moe_route(const moe_config* cfg, const void* x, const void* w_router,
+                     const float* logit_bias, const float* sel_bias, int32_t* topk_idx,
+                     float* topk_gate, void* ws, moe_stream_t stream);
+
+/*
+ * Step 2, Dispatch (Ultralytics step 2; ai360xpert "The All-to-All
+ * Bottleneck", Scatter) as one on-device permutation.
+ *   x [T,d]; topk_idx [T,k] (any valid choices, e.g. from moe_route).
+ * Outputs:
+ *   expert_counts [E]: assignments per expert before drops;
+ *   expert_offsets [E+1]: exclusive prefix over experts of the kept counts
+ *     min(count, C); expert e's kept rows are [offsets[e], offsets[e+1]);
+ *   rank_counts [R]: kept rows per virtual rank (its receive count);
+ *   rank_splits [R,R] or NULL: kept rows sent from source rank s (token t
+ *     belongs to rank t / ceil(T/R)) to destination rank r, i.e. the send
+ *     counts the all-to-all would use;
+ *   slot_row [T,k]: row of assignment (t,j) in the expert-major buffer, or
+ *     -1 if it overflowed its expert's capacity (in token order);
+ *   row_token [max_rows]: token of each kept row (entries past
+ *     offsets[E] are left untouched);
+ *   xp [max_rows, d]: xp[slot_row[t,j]] = x[t], bit for bit; token order is
+ *     kept inside every expert block;
+ *   n_dropped [1]: T*k - offsets[E].
+ * Device-side: an expert index outside [0,E) sets MOE_DEV_BAD_INDEX and the
+ * assignment is treated as dropped.
+ */
+moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, void* xp,
+                        int32_t* row_token, int32_t* slot_row, int32_t* expert_counts,
+                        int32_t* expert_offsets, int32_t* rank_counts, int32_t* rank_splits,
+                        int32_t* n_dropped, void* ws, moe_stream_t stream);
+
+/*
+ * Step 3, Compute (Ultralytics step 3): each expert's FFN on its rows of xp.
+ *   xp [max_rows, d]; expert_offsets [E+1] (device; read on the device, no
+ *   host synchronisation).  w_up [E, d_ff, d] (GELU) or [E, 2*d_ff, d]
+ *   (SwiGLU: the d_ff gate rows first, then the d_ff up rows); w_down
+ *   [E, d, d_ff].  All weights are [out, in] row-major.
+ *   h [max_rows, d_ff]: scratch for the hidden activations (act dtype).
+ *   yp [max_rows, d]: expert outputs, same row layout as xp.  Rows past
+ *   offsets[E] are left untouched.
+ *   Shared expert (cfg->n_shared == 1): shared_x [T,d] (normally x),
+ *   shared_up / shared_down shaped like one expert's weights, shared_h
+ *   [T, d_ff] scratch and shared_out [T,d] output; all NULL when
+ *   n_shared == 0.
+ * bf16 runs on the tensor cores (tcgen05, fp32 accumulation in tensor
+ * memory, h rounded to bf16 once); fp32 runs as an fp32 FFMA grouped GEMM.
+ * IDENTITY copies xp to yp (nothing if they are the same buffer).
+ */
+moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* expert_offsets,
+                          const void* w_up, const void* w_down, void* h, void* yp,
+                          const void* shared_x, const void* shared_up, const void* shared_down,
+                          void* shared_h, void* shared_out, void* ws, moe_stream_t stream);
+
+/*
+ * Step 4, Combine (Ultralytics step 4; ai360xpert Gather): back to token
+ * order, weighted by the gates and summed.
+ *   y[t] = sum over kept j, in slot order, of topk_gate[t,j] *
+ *   yp[slot_row[t,j]] (+ shared_out[t]) (+ x_residual[t] if
+ *   cfg->add_residual), accumulated in fp32 and rounded once to the act
+ *   dtype.  A token with every slot dropped gets exactly 0 (or exactly x).
+ *   shared_out [T,d] or NULL; x_residual [T,d] (required iff add_residual).
+ */
+moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slot_row,
+                       const float* topk_gate, const void* shared_out, const void* x_residual,
+                       void* y, moe_stream_t stream);
+
+/*
+ * Buffers of moe_layer_forward.  xp, yp, h (and shared_h, shared_out when
+ * n_shared == 1) are required.  Any metadata pointer may be NULL; the
+ * library then keeps that array in the workspace.  For IDENTITY experts,
+ * yp and h may be NULL (combine reads xp).
+ */
+typedef struct moe_buffers {
+    int32_t* topk_idx;       /* [T,k] */
+    float* topk_gate;        /* [T,k] */
+    int32_t* slot_row;       /* [T,k] */
+    int32_t* row_token;      /* [max_rows] */
+    int32_t* expert_counts;  /* [E] */
+    int32_t* expert_offsets; /* [E+1] */
+    int32_t* rank_counts;    /* [R] */
+    int32_t* rank_splits;    /* [R,R] */
+    int32_t* n_dropped;      /* [1] */
+    void* xp;                /* [max_rows, d] */
+    void* h;                 /* [max_rows, d_ff] */
+    void* yp;                /* [max_rows, d] */
+    void* shared_h;          /* [T, d_ff] */
+    void* shared_out;        /* [T, d] */
+} moe_buffers;
+
+/* The whole layer: route, dispatch, expert compute, combine, enqueued on
+   one stream with no host synchronisation.  y [T,d] (act dtype). */
+moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router,
+                             const float* logit_bias, const float* sel_bias, const void* w_up,
+                             const void* w_down, const void* shared_up, const void* shared_down,
+                             const moe_buffers* buf, void* y, void* ws, moe_stream_t stream);
+
+/* Copies the device status word of `ws` to *out (HOST pointer), waiting for
+   `stream`, then clears it.  MOE_OK with *out == 0 means no device error. */
+moe_status moe_read_device_status(const void* ws, uint32_t* out, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -1,0 +1,150 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/moe.h declares, and its host-side logic (validation, capacity,
+workspace sizing, status strings) behaves as documented.  No compute call is
+made here."""
+import ctypes
+import math
+import os
+import re
+import subprocess
+
+import pytest
+
+import expert_dispatch_top_b300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(moe_[a-z_]+)\s*\(", src,
+                       flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ["moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_layer_forward",
+              "moe_workspace_size", "moe_status_string", "moe_read_device_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = moe.library()
+    for n in _declared_functions():
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", moe.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = set(re.findall(r" T (moe_[a-z_]+)$", out, flags=re.M))
+    assert set(_declared_functions()) <= exported
+
+
+def test_status_strings():
+    for s in range(7):
+        assert moe.status_string(s).startswith("MOE_")
+    assert "unknown" in moe.status_string(99)
+
+
+def _cfg(**kw):
+    base = dict(T=4096, d=512, E=8, k=2, R=4, d_ff=1024, dtype="f32", score="softmax",
+                act="gelu")
+    base.update(kw)
+    return moe.make_config(**base)
+
+
+def test_struct_layout_matches_header():
+    assert ctypes.sizeof(moe.moe_config) == 14 * 4
+    assert ctypes.sizeof(moe.moe_buffers) == 14 * 8
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(), moe.MOE_OK),
+    (dict(k=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(k=9, E=16, R=4), moe.MOE_ERR_INVALID_ARG),
+    (dict(k=5, E=4, R=4), moe.MOE_ERR_INVALID_ARG),
+    (dict(E=257, R=1), moe.MOE_ERR_INVALID_ARG),
+    (dict(E=12, R=8), moe.MOE_ERR_INVALID_ARG),
+    (dict(R=64, E=256), moe.MOE_ERR_INVALID_ARG),
+    (dict(d=6), moe.MOE_ERR_INVALID_ARG),                 # fp32 row not 16-byte multiple
+    (dict(d=520, dtype="bf16"), moe.MOE_ERR_UNSUPPORTED),  # tensor-core path wants d % 64
+    (dict(d=516), moe.MOE_OK),                             # fp32 path takes d % 4
+    (dict(d_ff=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(d_ff=0, act="identity"), moe.MOE_OK),
+    (dict(n_shared=1, act="identity", d_ff=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(n_shared=2), moe.MOE_ERR_INVALID_ARG),
+    (dict(T=0), moe.MOE_OK),
+    (dict(T=-1), moe.MOE_ERR_INVALID_ARG),
+    (dict(T=1 << 28, k=4, E=8), moe.MOE_ERR_INVALID_ARG),  # T*k >= 2^30
+    (dict(capacity=-1), moe.MOE_ERR_INVALID_ARG),
+])
+def test_check_config(kw, status):
+    assert moe.moe_check_config(_cfg(**kw)) == status
+
+
+def test_capacity_and_max_rows():
+    # explicit capacity, factor, none
+    assert moe.moe_capacity(_cfg(capacity=100)) == 100
+    assert moe.moe_capacity(_cfg(capacity_factor=1.25)) == math.ceil(1.25 * 4096 * 2 / 8)
+    assert moe.moe_capacity(_cfg()) == -1
+    assert moe.moe_max_rows(_cfg()) == 4096 * 2
+    assert moe.moe_max_rows(_cfg(capacity=100)) == 8 * 100
+    assert moe.moe_max_rows(_cfg(capacity=5000)) == 4096 * 2
+    sw = moe.make_config(32768, 1024, 64, 1, 8, 4096, dtype="bf16", act="gelu",
+                         capacity_factor=1.25, renorm=False)
+    assert moe.moe_capacity(sw) == 640
+    assert moe.moe_max_rows(sw) == min(32768, 64 * 640)
+    tight = moe.make_config(32768, 1024, 64, 1, 8, 4096, dtype="bf16", act="gelu", capacity=300)
+    assert moe.moe_max_rows(tight) == 64 * 300
+
+
+def test_workspace_size():
+    c = _cfg()
+    n = moe.moe_workspace_size(c)
+    assert n > 0 and n % 256 == 0
+    # metadata arrays of the whole-layer call fit inside
+    assert n >= 3 * 4096 * 2 * 4 + 4096 * 2 * 4
+    assert moe.moe_workspace_size(_cfg(k=0)) == 0
+    big = moe.make_config(131072, 7168, 256, 8, 8, 0, act="identity", score="sigmoid")
+    assert moe.moe_workspace_size(big) > 131072 // 32 * 256 * 8
+
+
+def test_invalid_calls_fail_before_any_launch():
+    """Argument errors come back synchronously, with no GPU touched."""
+    c = _cfg()
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_route(c, None, None, None, None, None, None, None, stream=0)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_route(_cfg(k=0), None, None, None, None, None, None, None, stream=0)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+    # misaligned pointer
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_route(c, 0x1008 + 4, 0x2000, None, None, 0x3000, 0x4000, None, stream=0)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+    # selection-only bias needs sigmoid scores
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_route(c, 0x1000, 0x2000, None, 0x5000, 0x3000, 0x4000, None, stream=0)
+    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_dispatch(c, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, None, 0x7000, 0x8000, None,
+                         0x9000, 0xa000, stream=0)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_combine(_cfg(add_residual=True), 0x1000, 0x2000, 0x3000, None, None, 0x4000,
+                        stream=0)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_layer_forward(c, 0x1000, 0x2000, None, None, 0x3000, 0x4000, None, None,
+                              moe.moe_buffers(), 0x5000, 0x6000, stream=0)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_read_device_status(None, stream=0)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_noop():
+    c = _cfg(T=0)
+    moe.moe_route(c, None, None, None, None, None, None, None, stream=0)
+    moe.moe_combine(c, None, None, None, None, None, None, stream=0)

@@ -1,0 +1,139 @@
+"""GPU parity of Step 1 (Route) against the oracle: bit-exact expert choices
+and tie-breaks, gates within the fp32 bound."""
+import json
+import os
+
+import pytest
+import torch
+
+import expert_dispatch_top_b300 as moe
+import moe_workloads as W
+import oracle
+from gpu_util import DEV, assert_gates_close, cfg_for, run_dispatch, run_route, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_route(w, inp_cpu, T=None):
+    cfg = cfg_for(w, T=inp_cpu["x"].shape[0])
+    idx, gate = run_route(cfg, to_dev(inp_cpu))
+    ridx, rgate = oracle.route(inp_cpu["x"], inp_cpu["w_router"], w.k, w.score, w.renorm,
+                               inp_cpu["logit_bias"], inp_cpu["sel_bias"])
+    assert torch.equal(idx, ridx), f"{int((idx != ridx).any(1).sum())} tokens differ"
+    n_terms = w.k if w.renorm or w.score == "sigmoid" else w.E
+    assert_gates_close(gate, rgate, n_terms)
+
+
+@pytest.mark.parametrize("name", ["toy", "mixtral", "switch", "deepseek"])
+@pytest.mark.parametrize("T", [1, 33, 517])
+def test_route_workloads_small_T(name, T):
+    w = W.WORKLOADS[name]
+    _check_route(w, W.make_inputs(w, ffn=False, T=T))
+
+
+@pytest.mark.parametrize("s", [0.0, 1.5])
+def test_route_sweep_skew(s):
+    w = W.sweep(4096, s)
+    _check_route(w, W.make_inputs(w, ffn=False, T=300))
+
+
+@pytest.mark.parametrize("E,k,score,renorm", [(4, 2, "softmax", True), (8, 8, "sigmoid", False),
+                                               (16, 3, "softmax", False), (32, 4, "sigmoid", True),
+                                               (48, 5, "softmax", True), (64, 1, "softmax", False),
+                                               (128, 6, "sigmoid", True), (256, 8, "sigmoid", True),
+                                               (200, 7, "softmax", True)])
+def test_route_ties_and_shapes(E, k, score, renorm):
+    """A coarse weight grid makes exact ties common: the lower index must win."""
+    T, d = 257, 64
+    g = W._gen(E * 100 + k, "cpu")
+    x = W._grid_int((T, d), -8, 8, 8.0, g, "cpu").to(torch.bfloat16)
+    wr = W._grid_int((E, d), -1, 1, 512.0, g, "cpu").to(torch.bfloat16)
+    sel = (W._grid_int((E,), -1, 1, 4096.0, g, "cpu") if score == "sigmoid" else None)
+    lb = W._grid_int((E,), 0, 1, 4096.0, g, "cpu")
+    w = W.Workload("tie", T, d, E, 1, k, 64, "identity", "bf16", score, renorm, 0.0, 0, 0,
+                   "normal512")
+    inp = dict(x=x, w_router=wr, logit_bias=lb, sel_bias=sel)
+    _, _, L = oracle.route(x, wr, k, score, renorm, lb, sel, return_logits=True)
+    assert sum(len(set(r.tolist())) < E for r in L) > T // 4
+    _check_route(w, inp)
+
+
+@pytest.mark.parametrize("name", ["switch", "deepseek"])
+def test_route_full_size_sampled(name):
+    """The full workload through the bench's launch; the oracle scores a
+    seeded sample of tokens (routing is per token)."""
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w, ffn=False)
+    cfg = cfg_for(w)
+    idx, gate = run_route(cfg, to_dev(inp))
+    samp = torch.randperm(w.T, generator=torch.Generator().manual_seed(7))[:384]
+    samp = torch.cat([samp, torch.tensor([0, w.T - 1])])
+    ridx, rgate = oracle.route(inp["x"][samp], inp["w_router"], w.k, w.score, w.renorm,
+                               inp["logit_bias"], inp["sel_bias"])
+    assert torch.equal(idx[samp], ridx)
+    assert_gates_close(gate[samp], rgate, w.k if (w.renorm or w.score == "sigmoid") else w.E)
+
+
+def test_route_sigmoid_every_grid_logit():
+    """Every logit on the 1/4096 grid in [-16, 16] (131073 values) gets the
+    oracle's fp32 sigmoid, bit for bit.  Tokens hit base values v/4096 with
+    v = m0 + 8*m1 + 64*(sum of the rest); experts add a logit bias of 4e."""
+    E, k, d = 8, 8, 256
+    T = 16385
+    base = torch.arange(T, dtype=torch.int64) - 65536          # v in [-65536, -49152]
+    q, r = torch.div(base, 64, rounding_mode="floor"), base % 64
+    x = torch.zeros((T, d), dtype=torch.float32)
+    x[:, 0] = (r % 8).float() / 8
+    x[:, 1] = (r // 8).float() / 8
+    rest = q.abs()
+    sign = torch.sign(q).float()
+    for i in range(2, d):
+        take = torch.clamp(rest, max=8)
+        x[:, i] = sign * take.float() / 8
+        rest = rest - take
+    assert int(rest.abs().max()) == 0
+    wr = torch.full((E, d), 64.0 / 512)
+    wr[:, 0] = 1.0 / 512
+    wr[:, 1] = 8.0 / 512
+    lb = torch.arange(E, dtype=torch.float32) * 4.0
+    x, wr = x.to(torch.bfloat16), wr.to(torch.bfloat16)
+    _, _, L = oracle.route(x, wr, k, "sigmoid", False, lb, None, return_logits=True)
+    grid = torch.unique(L.double() * 4096)
+    assert grid.numel() == 131073 and int(grid.min()) == -65536 and int(grid.max()) == 65536
+    w = W.Workload("sig", T, d, E, 1, k, 64, "identity", "bf16", "sigmoid", False, 0.0, 0, 0,
+                   "normal512")
+    _check_route(w, dict(x=x, w_router=wr, logit_bias=lb, sel_bias=None))
+    cfg = cfg_for(w)
+    _, gate = run_route(cfg, to_dev(dict(x=x, w_router=wr, logit_bias=lb, sel_bias=None)))
+    _, rgate = oracle.route(x, wr, k, "sigmoid", False, lb, None)
+    assert torch.equal(gate, rgate)   # no-renorm sigmoid gates are the scores themselves
+
+
+def test_route_snippet_loads_on_gpu():
+    """The Ultralytics routing snippet through the GPU route and dispatch:
+    per-expert loads 948..1087 and per-GPU loads 1968..2139."""
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                    "snippet_router_loads.json")))
+    torch.manual_seed(g["seed"])
+    hidden = torch.randn(g["tokens"], g["d_model"])
+    layer = torch.nn.Linear(g["d_model"], g["experts"])
+    w = W.Workload("snippet", g["tokens"], g["d_model"], g["experts"], g["gpus"], g["top_k"], 0,
+                   "identity", "f32", "softmax", True, 0.0, 0, 0, "uniform64")
+    inp = dict(x=hidden, w_router=layer.weight.detach(), logit_bias=layer.bias.detach(),
+               sel_bias=None)
+    cfg = cfg_for(w)
+    idx, _ = run_route(cfg, to_dev(inp))
+    out = run_dispatch(cfg, hidden.to(DEV), idx)
+    ec, rc = out["expert_counts"].cpu(), out["rank_counts"].cpu()
+    assert int(ec.sum()) == g["assignments"]
+    assert (int(ec.min()), int(ec.max())) == (g["expert_load_min"], g["expert_load_max"])
+    assert (int(rc.min()), int(rc.max())) == (g["gpu_load_min"], g["gpu_load_max"])
+
+
+def test_route_deterministic():
+    w = W.WORKLOADS["deepseek"]
+    inp = to_dev(W.make_inputs(w, ffn=False, T=1024))
+    cfg = cfg_for(w, T=1024)
+    a = run_route(cfg, inp)
+    b = run_route(cfg, inp)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
