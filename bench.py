@@ -426,6 +426,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="mixtral")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (small profiling cases)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-route-tokens", type=int, default=256)
@@ -433,6 +434,8 @@ def main():
     args = ap.parse_args()
     import moe_workloads as W
     w = W.get(args.workload)
+    if args.tokens:
+        w = w.replace(T=args.tokens)
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -33,7 +33,6 @@ def _run_ffn(counts, d, f, act, dtype, seed, rows_cap=None, shared=False):
     cfg = moe.make_config(T, d, E, 1, 1, f, 1 if shared else 0,
                           "bf16" if dtype == torch.bfloat16 else "f32", "softmax", True, 0.0,
                           0, act)
-    assert moe.moe_max_rows(cfg) >= rows_cap or rows_cap == max(N, 1)
     h = torch.zeros((rows_cap, f), dtype=dtype, device=DEV)
     yp = torch.full((rows_cap, d), 7.0, dtype=dtype, device=DEV)
     ws = moe.alloc_workspace(cfg)

@@ -44,7 +44,8 @@ def test_route_sweep_skew(s):
                                                (200, 7, "softmax", True)])
 def test_route_ties_and_shapes(E, k, score, renorm):
     """A coarse weight grid makes exact ties common: the lower index must win."""
-    T, d = 257, 64
+    T = 257
+    d = 8 if E <= 8 else 64       # short rows keep exact ties frequent for small E
     g = W._gen(E * 100 + k, "cpu")
     x = W._grid_int((T, d), -8, 8, 8.0, g, "cpu").to(torch.bfloat16)
     wr = W._grid_int((E, d), -1, 1, 512.0, g, "cpu").to(torch.bfloat16)
@@ -54,7 +55,7 @@ def test_route_ties_and_shapes(E, k, score, renorm):
                    "normal512")
     inp = dict(x=x, w_router=wr, logit_bias=lb, sel_bias=sel)
     _, _, L = oracle.route(x, wr, k, score, renorm, lb, sel, return_logits=True)
-    assert sum(len(set(r.tolist())) < E for r in L) > T // 4
+    assert sum(len(set(r.tolist())) < E for r in L) > T // 8
     _check_route(w, inp)
 
 
