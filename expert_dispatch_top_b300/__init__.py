@@ -83,6 +83,8 @@ def _load():
     lib.moe_route.restype = i32
     lib.moe_dispatch.argtypes = [cfgp] + [vp] * 12
     lib.moe_dispatch.restype = i32
+    lib.moe_dispatch_noalloc.argtypes = [cfgp] + [vp] * 12
+    lib.moe_dispatch_noalloc.restype = i32
     lib.moe_expert_ffn.argtypes = [cfgp] + [vp] * 13
     lib.moe_expert_ffn.restype = i32
     lib.moe_combine.argtypes = [cfgp] + [vp] * 7
@@ -174,6 +176,17 @@ def moe_dispatch(cfg, x, topk_idx, xp, row_token, slot_row, expert_counts, exper
                                 _p(slot_row), _p(expert_counts), _p(expert_offsets),
                                 _p(rank_counts), _p(rank_splits), _p(n_dropped), _p(ws),
                                 _stream(stream)), "moe_dispatch")
+
+
+def moe_dispatch_noalloc(cfg, x, topk_idx, xp, row_token, slot_row, expert_counts, expert_offsets,
+                         rank_counts, rank_splits, n_dropped, device_status=None, stream=None):
+    """moe_dispatch with its scratch in the library's fixed device array (no
+    workspace argument, nothing allocated); for callers that cannot allocate."""
+    _check(_load().moe_dispatch_noalloc(ctypes.byref(cfg), _p(x), _p(topk_idx), _p(xp),
+                                        _p(row_token), _p(slot_row), _p(expert_counts),
+                                        _p(expert_offsets), _p(rank_counts), _p(rank_splits),
+                                        _p(n_dropped), _p(device_status), _stream(stream)),
+           "moe_dispatch_noalloc")
 
 
 def moe_expert_ffn(cfg, xp, expert_offsets, w_up, w_down, h, yp, shared_x=None, shared_up=None,

@@ -1,0 +1,130 @@
+// dispatch_noalloc.cu -- moe_dispatch_noalloc: the dispatch step with its
+// scratch state kept in a fixed-size array inside the library.
+//
+// Some callers cannot call cudaMalloc: a plugin inside an inference engine
+// that is handed only its input and output pointers, or a serving loop whose
+// device memory was all reserved by another allocator at start-up.  They have
+// no way to provide the workspace moe_dispatch needs.  This entry point runs
+// the very same dispatch kernels, but points their scratch state (status
+// word, block ticket, finish counter, per-expert counts, look-back
+// descriptors, send-count accumulator) at the file-scope device array below.
+//
+// The array is a static __device__ object: every GPU that loads the library
+// holds kScratchBytes of it until the process exits.  Host code cannot use
+// the array's name as a device address (in host code it names a host-side
+// stand-in), so the first call on each device, with that device current,
+// looks the address up with cudaGetSymbolAddress and caches it.  Every call
+// shares the one array and finds the previous call's contents in it; each
+// call clears the parts that must start at zero before its kernels run.
+// Calls that overlap on the GPU (different streams, or several host threads
+// without ordering) race on the array.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kScratchBytes = size_t(4) << 20;  // 4 MiB per device
+constexpr size_t kAlignNA = 256;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_dispatch_scratch[kScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+inline size_t up256(size_t v) { return (v + kAlignNA - 1) / kAlignNA * kAlignNA; }
+
+// Device address of the scratch array on the current device (set up once).
+cudaError_t scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+// Scratch layout: status, ticket, finish counter | counts [E] | look-back
+// descriptors [ceil(T/32), E] | send-count accumulator [R, R].
+struct NoAllocLayout {
+    size_t counts, desc, splits, clear, total;
+};
+
+NoAllocLayout noalloc_layout(const moe_config* c) {
+    NoAllocLayout L;
+    L.counts = kAlignNA;
+    L.desc = up256(L.counts + (size_t)c->E * 4);
+    L.clear = L.desc;
+    L.splits = up256(L.desc + (size_t)dispatch_blocks(c->T) * c->E * 8);
+    L.total = up256(L.splits + (size_t)c->R * c->R * 4);
+    return L;
+}
+
+inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+inline bool a4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x,
+                                           const int32_t* topk_idx, void* xp, int32_t* row_token,
+                                           int32_t* slot_row, int32_t* expert_counts,
+                                           int32_t* expert_offsets, int32_t* rank_counts,
+                                           int32_t* rank_splits, int32_t* n_dropped,
+                                           uint32_t* device_status, moe_stream_t stream) {
+    moe_status st = moe_check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!expert_counts || !expert_offsets || !rank_counts || !n_dropped) return MOE_ERR_INVALID_ARG;
+    if (cfg->T > 0 && (!x || !topk_idx || !xp || !row_token || !slot_row)) return MOE_ERR_INVALID_ARG;
+    if (!a16(x) || !a16(xp) || !a4(topk_idx) || !a4(row_token) || !a4(slot_row) ||
+        !a4(expert_counts) || !a4(expert_offsets) || !a4(rank_counts) || !a4(rank_splits) ||
+        !a4(n_dropped) || !a4(device_status))
+        return MOE_ERR_INVALID_ARG;
+    const NoAllocLayout L = noalloc_layout(cfg);
+    if (L.total > kScratchBytes) return MOE_ERR_INVALID_ARG;  // beyond the fixed scratch size
+
+    void* base = nullptr;
+    if (scratch_address(&base) != cudaSuccess) return MOE_ERR_CUDA;
+    char* s = static_cast<char*>(base);
+    cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
+    // status word, ticket, finish counter and per-expert counts start at zero
+    if (cudaMemsetAsync(s, 0, L.clear, strm) != cudaSuccess) return MOE_ERR_CUDA;
+
+    DispatchArgs a;
+    a.x = x;
+    a.idx = topk_idx;
+    a.xp = xp;
+    a.row_token = row_token;
+    a.slot_row = slot_row;
+    a.expert_counts = expert_counts;
+    a.expert_offsets = expert_offsets;
+    a.rank_counts = rank_counts;
+    a.rank_splits = rank_splits;
+    a.n_dropped = n_dropped;
+    a.status = device_status ? device_status : reinterpret_cast<uint32_t*>(s);
+    a.ticket = reinterpret_cast<uint32_t*>(s + 4);
+    a.done = reinterpret_cast<uint32_t*>(s + 8);
+    a.counts = reinterpret_cast<int32_t*>(s + L.counts);
+    a.desc = reinterpret_cast<uint64_t*>(s + L.desc);
+    a.splits_acc = reinterpret_cast<int32_t*>(s + L.splits);
+    a.T = cfg->T;
+    a.d = cfg->d;
+    a.E = cfg->E;
+    a.k = cfg->k;
+    a.R = cfg->R;
+    a.dtype = cfg->act_dtype;
+    a.C = moe_capacity(cfg);
+    return launch_dispatch(a, strm) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -14,7 +14,8 @@
  * ---------------------------------------
  *  - All pointers are DEVICE pointers on the current CUDA device unless a
  *    parameter says otherwise; the caller owns every buffer.  The library
- *    never allocates or frees device memory and keeps no global state.
+ *    never allocates or frees device memory and keeps no global state,
+ *    except the fixed scratch array that moe_dispatch_noalloc uses.
  *  - Every pointer must be 16-byte aligned; tensors are dense and row-major.
  *  - Activations and expert/router weights share one storage type,
  *    cfg->act_dtype (fp32 or bf16).  Router logits, gates and every
@@ -164,6 +165,33 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
                         int32_t* row_token, int32_t* slot_row, int32_t* expert_counts,
                         int32_t* expert_offsets, int32_t* rank_counts, int32_t* rank_splits,
                         int32_t* n_dropped, void* ws, moe_stream_t stream);
+
+/*
+ * moe_dispatch without a workspace, for callers that cannot allocate device
+ * memory (a plugin handed only its input and output pointers; a serving loop
+ * whose memory was all reserved by another allocator).  The pages have no
+ * counterpart: this is a deployment variant of moe_dispatch, not a step of
+ * the method.
+ *   Arguments and outputs are those of moe_dispatch, minus ws; results are
+ *   identical to moe_dispatch's.  device_status (DEVICE pointer, nullable):
+ *   the kernels OR their MOE_DEV_* bits into it; the caller zeroes it.
+ *   Scratch state lives in one fixed 4 MiB device array inside the library
+ *   (allocated when the library loads, on every GPU that loads it, until the
+ *   process exits).  Limit: 256 + 4*E + 8*E*ceil(T/32) + 4*R*R bytes, each
+ *   term rounded up to 256, must fit in 4 MiB (T*E <= ~16.7 million, e.g.
+ *   T = 65536 with E = 128); larger shapes return MOE_ERR_INVALID_ARG before
+ *   anything is enqueued.
+ *   The first call on a device (with that device current) looks up the
+ *   array's device address; make that first call before any stream capture.
+ *   Every call shares the array and clears what must start at zero itself;
+ *   calls that overlap on the GPU (other streams, unordered host threads)
+ *   race on it.  Allocates nothing: no cudaMalloc, no cudaFree.
+ */
+moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                                void* xp, int32_t* row_token, int32_t* slot_row,
+                                int32_t* expert_counts, int32_t* expert_offsets,
+                                int32_t* rank_counts, int32_t* rank_splits, int32_t* n_dropped,
+                                uint32_t* device_status, moe_stream_t stream);
 
 /*
  * Step 3, Compute (Ultralytics step 3): each expert's FFN on its rows of xp.
