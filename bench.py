@@ -59,8 +59,13 @@ def _peaks():
         with open(p) as f:
             d = json.load(f)
         return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
-                    src="measured")
-    return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, src="fallback")
+                    src="measured", sm_mhz=d.get("sm_max_mhz", 2032.0))
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, src="fallback", sm_mhz=2032.0)
+
+
+def fp32_ffma_peak_tflops(sm_count, sm_mhz):
+    """FP32 FFMA roofline: SMs x 128 FP32 lanes x 2 flops x clock."""
+    return sm_count * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
 class ClockSampler:
@@ -368,26 +373,39 @@ def run_ours(args, w):
     }
     for kname in ("dispatch", "combine"):
         kernels[kname]["frac_hbm"] = kernels[kname]["GB/s"] / peaks["hbm"]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     if not ident:
         kernels["ffn"] = {"ms": ffn_ms, "TFLOP/s": work["ffn_flops"] / (ffn_ms * 1e-3) / 1e12,
                           "launches_per_step": 2 * (1 + w.n_shared)}
         achieved = kernels["ffn"]["TFLOP/s"]
-        tr = TRAFFIC.get(w.name)
-        traffic = None
-        if tr and tr["src_hash"] == _src_hash(os.path.join(ROOT, "expert_dispatch_top_b300",
-                                                           "csrc", "ffn_tc.cu")):
-            traffic = tr["bytes"]
-        roofline = {"kernel": "tc_gemm_kernel (expert FFN, up+down per step)", "bound": "tensor",
-                    "achieved": achieved, "peak": peaks["bf16_sus"], "unit": "TFLOP/s",
-                    "frac": achieved / peaks["bf16_sus"], "traffic": traffic,
-                    "peak_kind": f"bf16 sustained ({peaks['src']})",
-                    "frac_of_burst": achieved / peaks["bf16"],
-                    "algorithmic_flops_per_step": work["ffn_flops"]}
+        if w.dtype == "bf16":
+            tr = TRAFFIC.get(w.name)
+            traffic = None
+            if tr and tr["src_hash"] == _src_hash(os.path.join(ROOT, "expert_dispatch_top_b300",
+                                                               "csrc", "ffn_tc.cu")):
+                traffic = tr["bytes"]
+            roofline = {"kernel": "tc_gemm_kernel (expert FFN, up+down per step)",
+                        "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sus"],
+                        "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sus"],
+                        "traffic": traffic, "peak_kind": f"bf16 sustained ({peaks['src']})",
+                        "frac_of_burst": achieved / peaks["bf16"],
+                        "algorithmic_flops_per_step": work["ffn_flops"]}
+        else:
+            pk = fp32_ffma_peak_tflops(sms, peaks["sm_mhz"])
+            roofline = {"kernel": "gemm_simt_kernel (fp32 expert FFN, up+down per step)",
+                        "bound": "alu", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
+                        "frac": achieved / pk, "traffic": None,
+                        "peak_kind": f"FP32 FFMA: {sms} SMs x 128 lanes x 2 x {peaks['sm_mhz']:.0f} MHz",
+                        "algorithmic_flops_per_step": work["ffn_flops"]}
     else:
         gbs = kernels["dispatch"]["GB/s"]
         roofline = {"kernel": "place_kernel (permute)", "bound": "hbm", "achieved": gbs,
                     "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
-                    "traffic": None, "peak_kind": f"HBM copy ({peaks['src']})"}
+                    "traffic": None, "peak_kind": f"HBM copy ({peaks['src']})",
+                    "algorithmic_bytes_per_step": work["permute_bytes"]}
+    kernels["route"]["frac_fp32_ffma"] = kernels["route"]["TFLOP/s_fp32"] / \
+        fp32_ffma_peak_tflops(sms, peaks["sm_mhz"])
+    kernels["route"]["frac_hbm"] = kernels["route"]["GB/s"] / peaks["hbm"]
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -423,7 +441,7 @@ def run_ours(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="mixtral")
     ap.add_argument("--tokens", type=int, default=0, help="override T (small profiling cases)")
