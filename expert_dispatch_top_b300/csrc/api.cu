@@ -94,9 +94,9 @@ moe_status check_ffn_config(const moe_config* c) {
 }
 
 moe_status route_impl(const moe_config* c, const void* x, const void* w, const float* lb,
-                      const float* sb, int32_t* idx, float* gate, cudaStream_t s) {
+                      const float* sb, int32_t* idx, float* gate, void* ws, cudaStream_t s) {
     if (c->T == 0) return MOE_OK;
-    if (!x || !w || !idx || !gate) return MOE_ERR_INVALID_ARG;
+    if (!x || !w || !idx || !gate || !ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w) || !aligned4(idx) || !aligned4(gate) || !aligned4(lb) ||
         !aligned4(sb))
         return MOE_ERR_INVALID_ARG;
@@ -108,6 +108,7 @@ moe_status route_impl(const moe_config* c, const void* x, const void* w, const f
     a.sel_bias = sb;
     a.idx = idx;
     a.gate = gate;
+    a.status = at<uint32_t>(ws, layout_of(c).status);
     a.T = c->T;
     a.d = c->d;
     a.E = c->E;
@@ -305,8 +306,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* w_router,
                      float* topk_gate, void* ws, moe_stream_t stream) {
     moe_status st = moe_check_config(cfg);
     if (st != MOE_OK) return st;
-    (void)ws;
-    return route_impl(cfg, x, w_router, logit_bias, sel_bias, topk_idx, topk_gate,
+    return route_impl(cfg, x, w_router, logit_bias, sel_bias, topk_idx, topk_gate, ws,
                       reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -364,7 +364,7 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w
         return MOE_ERR_INVALID_ARG;
     if (!y || (cfg->T > 0 && !x)) return MOE_ERR_INVALID_ARG;
 
-    st = route_impl(cfg, x, w_router, logit_bias, sel_bias, idx, gate, s);
+    st = route_impl(cfg, x, w_router, logit_bias, sel_bias, idx, gate, ws, s);
     if (st != MOE_OK) return st;
     st = dispatch_impl(cfg, x, idx, buf->xp, row_token, slot_row, counts, offsets, rank_counts,
                        rank_splits, n_dropped, ws, s);

@@ -34,14 +34,13 @@
 // Every mbarrier wait is bounded by %globaltimer: on timeout the kernel sets
 // MOE_DEV_GEMM_TIMEOUT, raises an abort flag seen by the other roles, drains
 // its own MMAs (bounded) and frees TMEM before returning.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace moe {
 namespace {
+
+using namespace tc;
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
@@ -56,10 +55,7 @@ constexpr int TABLE_BYTES = 128 + 4 * MAX_GROUPS * 4;  // barriers + flags, then
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_BYTES + TABLE_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
 
-// tcgen05 instruction descriptor, kind::f16: D fp32, A and B bf16, both
-// K-major, N = 256 (bits 17-22, N>>3), M = 128 (bits 24-28, M>>4).
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
 
 struct TcParams {
     const int32_t* offsets;
@@ -71,127 +67,6 @@ struct TcParams {
     __nv_bfloat16* out;
     uint32_t* status;
 };
-
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.b32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the phase of parity `parity`.  False on timeout or abort.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* status) {
-#pragma unroll 1
-    for (int i = 0; i < 128; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-#pragma unroll 1
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-            atomicOr(status, MOE_DEV_GEMM_TIMEOUT);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
-                                            int c2, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, rows of 128 bytes,
-// 128-byte swizzle, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;            // leading byte offset (unused with this swizzle)
-    d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: 8 rows x 128 B
-    d |= (uint64_t)1 << 46;            // descriptor version
-    d |= (uint64_t)2 << 61;            // SWIZZLE_128B
-    return d;
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accum)
-        : "memory");
-}
-
-// 32 lanes x 32 consecutive fp32 columns; waits for completion before the
-// registers are used.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 __device__ __forceinline__ float gelu_f(float v) {
     return 0.5f * v * (1.f + erff(v * 0.70710678118654752440f));
@@ -256,18 +131,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_fence_init();
     }
     if (warp == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(tmem_slot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     }
     if (warp == 2) {
         // Per-group tile table: lane l covers groups [8l, 8l+8).
@@ -303,9 +174,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (lane == 31) *total_s = incl;
     }
-    tc_fence_before();
+    fence_before();
     __syncthreads();
-    tc_fence_after();
+    fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total = *total_s;
     const int n_tiles = p.n_tiles;
@@ -318,7 +189,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
                 const TileInfo ti = decode_tile(tile, p.G, tstart, mt, rowoff, grows, n_tiles);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status)) break;
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT)) break;
                     const uint32_t fb = full0 + 8 * stage;
                     mbar_expect_tx(fb, STAGE_BYTES);
                     const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
@@ -347,38 +218,38 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status)) {
+                if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
+                fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
+                    fence_after();
                     const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
                     const uint32_t sb = sa + A_STAGE;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        tc_mma(d_tmem, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32),
-                               (kb | kk) != 0 ? 1u : 0u);
-                    tc_commit(empty0 + 8 * stage);
+                        mma_bf16(d_tmem, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), kIdesc,
+                                 (kb | kk) != 0 ? 1u : 0u);
+                    commit(empty0 + 8 * stage);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                tc_commit(accf0 + 8 * acc);
+                commit(accf0 + 8 * acc);
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1;
             }
             if (!ok) {
                 // drain this thread's MMAs before TMEM is released (bounded)
-                tc_commit(drain);
+                commit(drain);
                 const uint64_t t0 = globaltimer_ns();
                 while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
                 }
@@ -394,9 +265,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             const TileInfo ti = decode_tile(tile, p.G, tstart, mt, rowoff, grows, n_tiles);
             // every lane waits, then the warp agrees, so the .sync.aligned TMEM loads
             // below always run converged
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(accf0 + 8 * acc, acc_phase, abort_flag, p.status));
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(accf0 + 8 * acc, acc_phase, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT));
             if (!ok) break;
-            tc_fence_after();
+            fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             const int col0 = ti.n_tile * p.out_cols;
             for (int c64 = 0; c64 < p.out_cols / 64; ++c64) {
@@ -440,41 +311,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 __syncwarp();
             }
-            tc_fence_before();
+            fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce0 + 8 * acc);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
     }
-    tc_fence_before();
+    fence_before();
     __syncthreads();
-    tc_fence_after();
+    fence_after();
     if (warp == 1) {
         __syncwarp();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(TMEM_COLS)
-                     : "memory");
+        tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
 }  // namespace
 
 int gemm_tc_supported(const GemmArgs& a) {
@@ -492,34 +347,14 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
     if (gemm_tc_supported(a) != 0) return cudaErrorInvalidValue;
     const int64_t rows_cap = a.offsets ? a.rows_cap : a.m_rows;
     if (rows_cap <= 0) return cudaSuccess;
-    auto encode = get_encode();
-    if (!encode) return cudaErrorNotSupported;
-
     const bool gated = a.epi == EPI_SWIGLU;
     const int b_rows = gated ? 2 * a.N : a.N;
     CUtensorMap tmA, tmB;
-    {
-        cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)rows_cap};
-        cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
-        cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
-        cuuint32_t es[2] = {1, 1};
-        CUresult r = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.A), dims,
-                            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    }
-    {
-        cuuint64_t dims[3] = {(cuuint64_t)a.K, (cuuint64_t)b_rows, (cuuint64_t)a.G};
-        cuuint64_t strides[2] = {(cuuint64_t)a.K * 2, (cuuint64_t)b_rows * a.K * 2};
-        cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)(gated ? 128 : BN), 1};
-        cuuint32_t es[3] = {1, 1, 1};
-        CUresult r = encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.B), dims,
-                            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    }
+    // A is read with 2-D loads, the stacked weights with 3-D loads (group index).
+    if (!make_tmap_bf16(&tmA, a.A, (uint64_t)a.K, (uint64_t)rows_cap, 1, BM, 2) ||
+        !make_tmap_bf16(&tmB, a.B, (uint64_t)a.K, (uint64_t)b_rows, (uint64_t)a.G, gated ? 128 : BN,
+                        3))
+        return cudaErrorInvalidValue;
     TcParams p;
     p.offsets = a.offsets;
     p.m_rows = a.m_rows;

@@ -13,10 +13,14 @@ struct RouteArgs {
     const float* sel_bias;
     int32_t* idx;
     float* gate;
+    uint32_t* status;  // device status word (bounded-wait timeouts)
     int64_t T;
     int d, E, k, score, renorm, dtype;
 };
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+// Tensor-core router (bf16, E <= 256): 0 if supported.
+int route_tc_supported(const RouteArgs& a);
+cudaError_t launch_route_tc(const RouteArgs& a, cudaStream_t s);
 
 struct DispatchArgs {
     const void* x;

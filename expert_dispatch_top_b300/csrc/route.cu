@@ -1,4 +1,5 @@
 // route.cu -- Step 1, Route: router logits (fp32 FFMA), score, top-k, gates.
+// fp32 routers run here; bf16 routers run on the tensor cores (route_tc.cu).
 //
 // Ultralytics glossary "Expert Parallelism", section "How Tokens Move Between
 // GPUs", step 1: every token gets a score for every expert and keeps the k
@@ -364,6 +365,7 @@ cudaError_t launch_typed(const RouteArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
+    if (route_tc_supported(a) == 0) return launch_route_tc(a, s);
     if (a.dtype == MOE_DTYPE_F32) return launch_typed<float>(a, s);
     return launch_typed<__nv_bfloat16>(a, s);
 }

@@ -1,0 +1,441 @@
+// route_tc.cu -- Step 1, Route, for bf16 routers (1 <= E <= 256): the
+// router GEMM on the tensor cores with the score, top-k and gates fused into
+// the epilogue (Ultralytics glossary "Expert Parallelism", "How Tokens Move
+// Between GPUs", step 1; DeepSeek-V3 selection-only bias from "Load Balancing
+// and Capacity").
+//
+// logits[T, E] = x[T, d] . Wr[E, d]^T with bf16 operands and fp32
+// accumulation in tensor memory.  Every product of two bf16 values is exact
+// in fp32; on inputs whose partial sums stay representable (the dyadic test
+// grid: multiples of 2^-12 below 2^10) the accumulation is exact too, so the
+// logits -- and every routing decision -- equal the FFMA kernels' bit for bit.
+//
+// Persistent kernel, one CTA per SM (192 threads, ~192 KB of shared memory so
+// that exactly one CTA holds the SM's 512 TMEM columns):
+//   warp 0     TMA: a 128-token x 64 tile of x and the E x 64 tile of Wr
+//              (rows past E zero-filled) per stage;
+//   warp 1     TMEM allocation; one lane issues tcgen05.mma (M=128, N=Np,
+//              Np = E rounded up to a multiple of 16, at least 16) into one of
+//              two accumulators;
+//   warps 2-5  epilogue: each thread owns one token (one TMEM lane), reads
+//              its E logits 32 at a time and keeps a sorted top-k in registers
+//              (ties to the lower expert index), then computes the gates and
+//              writes topk_idx / topk_gate.
+// Sigmoid routers: the exact score fp32(1/(1+exp(-L))) needs double
+// precision, which is slow on this part.  The epilogue first ranks all
+// experts by an approximation a = 1/2 + tanh(L/2)/2 (+ bias), using the
+// hardware tanh whose documented maximum relative error is 2^-11 (so
+// |a - key| < 2.5e-4), finds the k-th largest approximation A_k, and
+// evaluates the exact score only for experts with a >= A_k - 2*delta, with
+// delta = 2^-8 (16x the bound).  Any expert of the exact top-k has key >=
+// (k-th exact key) >= A_k - delta and hence a >= A_k - 2*delta, so the exact
+// top-k over these candidates is the exact top-k over all experts, ties
+// included.
+//
+// Epilogue layout: per 32-logit chunk, one compact unrolled pass stashes the
+// logits in shared memory (one padded row per thread) and builds a 32-bit
+// mask of the values that beat the current k-th key; only those are inserted
+// (sorted insertion, ties to the lower index), so the insertion code exists
+// once and runs rarely.
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int RM = 128, RK = 64;
+constexpr int STASH_PITCH = 33;  // floats per epilogue thread (32 logits + pad: conflict-free)
+constexpr int STASH_BYTES = 128 * STASH_PITCH * 4;
+constexpr int R_THREADS = 192;
+constexpr int R_MAX_STAGES = 8;
+constexpr uint32_t R_TMEM_COLS = 512;
+constexpr int R_SMEM_TILES = 196608;  // bytes of stage ring
+constexpr int R_SMEM_EXTRA = 1024 /*align*/ + 256 /*barriers*/ + 2 * 256 * 4 /*biases*/ + STASH_BYTES;
+constexpr float kApproxDelta = 1.0f / 256.0f;
+
+struct RtParams {
+    int64_t T;
+    int d, E, Np, k, score, renorm;
+    const float* logit_bias;
+    const float* sel_bias;
+    int32_t* idx;
+    float* gate;
+    uint32_t* status;
+    int num_kb, m_tiles, stages, stage_bytes;
+};
+
+__device__ __forceinline__ float sigmoid_exact(float L) {
+    return (float)(1.0 / (1.0 + exp(-(double)L)));
+}
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float sigmoid_approx(float L) {
+    return fmaf(0.5f, tanh_approx(0.5f * L), 0.5f);
+}
+
+// Sorted top-k (k <= 8) in registers: key, a payload value and the index.
+struct TopK {
+    float key[8], val[8];
+    int idx[8];
+    float kth_key;
+    int kth_idx;
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            key[j] = -INFINITY;
+            val[j] = 0.f;
+            idx[j] = 0x7fffffff;
+        }
+        kth_key = -INFINITY;
+        kth_idx = 0x7fffffff;
+    }
+    __device__ __forceinline__ void insert(float kv, float v, int e, int k) {
+        if (!key_better(kv, e, kth_key, kth_idx)) return;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < k && key_better(kv, e, key[j], idx[j])) {
+                const float tk = key[j], tv = val[j];
+                const int ti = idx[j];
+                key[j] = kv;
+                val[j] = v;
+                idx[j] = e;
+                kv = tk;
+                v = tv;
+                e = ti;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j == k - 1) {
+                kth_key = key[j];
+                kth_idx = idx[j];
+            }
+    }
+};
+
+// First K block of a tile.  Every tile reads the same router weights; if all
+// CTAs walked K in the same order they would all hit the few L2 slices that
+// hold the current weight block at once.  Rotating the start per tile spreads
+// them over the whole matrix.  (The summation order then differs between
+// tiles; on inputs whose sums are exact in fp32 this changes nothing.)
+__device__ __forceinline__ int k_start(int tile, int num_kb) { return (int)(((unsigned)tile * 37u) % (unsigned)num_kb); }
+
+__global__ void __launch_bounds__(R_THREADS, 1)
+    route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                    const RtParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* extra = smem + p.stages * p.stage_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(extra);  // full[8] empty[8] accf[2] acce[2] drain
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(extra + 192);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(extra + 196);
+    float* lb_s = reinterpret_cast<float*>(extra + 256);
+    float* sb_s = lb_s + 256;
+    float* stash_all = sb_s + 256;  // [128][STASH_PITCH]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + R_MAX_STAGES);
+    const uint32_t accf0 = smem_u32(bars + 2 * R_MAX_STAGES);
+    const uint32_t acce0 = smem_u32(bars + 2 * R_MAX_STAGES + 2);
+    const uint32_t drain = smem_u32(bars + 2 * R_MAX_STAGES + 4);
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(acce0 + 8 * b, 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), R_TMEM_COLS);
+    if (warp >= 2) {
+        for (int e = threadIdx.x - 64; e < 256; e += 128) {
+            lb_s[e] = (p.logit_bias && e < p.E) ? p.logit_bias[e] : 0.f;
+            sb_s[e] = (p.sel_bias && e < p.E) ? p.sel_bias[e] : 0.f;
+        }
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int tile = blockIdx.x; tile < p.m_tiles && !*abort_flag; tile += gridDim.x) {
+                const int kb0 = k_start(tile, p.num_kb);
+                for (int i = 0; i < p.num_kb; ++i) {
+                    int kb = kb0 + i;
+                    if (kb >= p.num_kb) kb -= p.num_kb;
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status,
+                                   MOE_DEV_GEMM_TIMEOUT))
+                        break;
+                    const uint32_t fb = full0 + 8 * stage;
+                    mbar_expect_tx(fb, p.stage_bytes);
+                    const uint32_t sa = smem_u32(smem + stage * p.stage_bytes);
+                    tma_load_2d(sa, &tmX, kb * RK, tile * RM, fb);
+                    tma_load_2d(sa + RM * RK * 2, &tmW, kb * RK, 0, fb);
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(RM, p.Np);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < p.m_tiles && ok; tile += gridDim.x) {
+                if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status,
+                               MOE_DEV_GEMM_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+                for (int i = 0; i < p.num_kb; ++i) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status,
+                                   MOE_DEV_GEMM_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * p.stage_bytes);
+                    const uint32_t sb = sa + RM * RK * 2;
+#pragma unroll
+                    for (int kk = 0; kk < RK / 16; ++kk)
+                        mma_bf16(d_tmem, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), idesc,
+                                 (i | kk) != 0 ? 1u : 0u);
+                    commit(empty0 + 8 * stage);
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                commit(accf0 + 8 * acc);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            if (!ok) {
+                // drain this thread's MMAs before TMEM is released (bounded)
+                commit(drain);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue: one token per thread ----------------
+        const int q = warp & 3;
+        const int nchunks = (p.E + 31) / 32;
+        const bool sigmoid = p.score == MOE_SCORE_SIGMOID;
+        const bool has_lb = p.logit_bias != nullptr;
+        const bool has_sb = p.sel_bias != nullptr;
+        float* stash = stash_all + (threadIdx.x - 64) * STASH_PITCH;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < p.m_tiles; tile += gridDim.x) {
+            const bool ok =
+                __all_sync(0xffffffffu, mbar_wait(accf0 + 8 * acc, acc_phase, abort_flag, p.status,
+                                                  MOE_DEV_GEMM_TIMEOUT));
+            if (!ok) break;
+            fence_after();
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256);
+            const int64_t t = (int64_t)tile * RM + q * 32 + lane;
+            TopK top;
+            top.init();
+            float v[32];
+            if (!sigmoid) {
+                for (int c = 0; c < nchunks; ++c) {
+                    tmem_ld32(tb + (uint32_t)(c * 32), v);
+                    const float thr = top.kth_key;
+                    uint32_t mask = 0;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = c * 32 + i;
+                        const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
+                        stash[i] = L;
+                        if (e < p.E && L > thr) mask |= 1u << i;
+                    }
+                    while (mask) {
+                        const int i = __ffs(mask) - 1;
+                        mask &= mask - 1;
+                        const float L = stash[i];
+                        top.insert(L, L, c * 32 + i, p.k);
+                    }
+                }
+            } else {
+                TopK approx;
+                approx.init();
+                for (int c = 0; c < nchunks; ++c) {
+                    tmem_ld32(tb + (uint32_t)(c * 32), v);
+                    const float thr = approx.kth_key;
+                    uint32_t mask = 0;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = c * 32 + i;
+                        const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
+                        stash[i] = L;
+                        const float a = __fadd_rn(sigmoid_approx(L), sb_s[e & 255]);
+                        if (e < p.E && a > thr) mask |= 1u << i;
+                    }
+                    while (mask) {
+                        const int i = __ffs(mask) - 1;
+                        mask &= mask - 1;
+                        const int e = c * 32 + i;
+                        const float a = __fadd_rn(sigmoid_approx(stash[i]), sb_s[e]);
+                        approx.insert(a, 0.f, e, p.k);
+                    }
+                }
+                const float thresh = approx.kth_key - 2.f * kApproxDelta;
+                for (int c = 0; c < nchunks; ++c) {
+                    tmem_ld32(tb + (uint32_t)(c * 32), v);
+                    uint32_t mask = 0;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = c * 32 + i;
+                        const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
+                        stash[i] = L;
+                        const float a = __fadd_rn(sigmoid_approx(L), sb_s[e & 255]);
+                        if (e < p.E && a >= thresh) mask |= 1u << i;
+                    }
+                    while (mask) {
+                        const int i = __ffs(mask) - 1;
+                        mask &= mask - 1;
+                        const int e = c * 32 + i;
+                        const float s = sigmoid_exact(stash[i]);
+                        const float key = has_sb ? __fadd_rn(s, sb_s[e]) : s;
+                        top.insert(key, s, e, p.k);
+                    }
+                }
+            }
+            // gates
+            float g[8];
+            if (!sigmoid) {
+                const float m = top.val[0];
+                float z = 0.f;
+                if (p.renorm) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (j < p.k) z += expf(top.val[j] - m);
+                } else {
+                    for (int c = 0; c < nchunks; ++c) {
+                        tmem_ld32(tb + (uint32_t)(c * 32), v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int e = c * 32 + i;
+                            if (e < p.E) {
+                                const float L = has_lb ? __fadd_rn(v[i], lb_s[e]) : v[i];
+                                z += expf(L - m);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) g[j] = expf(top.val[j] - m) / z;
+            } else {
+                float z = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < p.k) z += top.val[j];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) g[j] = p.renorm ? top.val[j] / z : top.val[j];
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+            if (t < p.T) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < p.k) {
+                        p.idx[t * p.k + j] = top.idx[j];
+                        p.gate[t * p.k + j] = g[j];
+                    }
+            }
+        }
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, R_TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+int route_tc_supported(const RouteArgs& a) {
+    if (a.dtype != MOE_DTYPE_BF16) return 1;
+    if (a.E < 1 || a.E > 256) return 2;
+    if (a.d % 8 != 0) return 3;
+    if ((reinterpret_cast<uintptr_t>(a.x) | reinterpret_cast<uintptr_t>(a.w)) & 15) return 4;
+    return 0;
+}
+
+cudaError_t launch_route_tc(const RouteArgs& a, cudaStream_t s) {
+    if (route_tc_supported(a) != 0) return cudaErrorInvalidValue;
+    if (a.T == 0) return cudaSuccess;
+    RtParams p;
+    p.T = a.T;
+    p.d = a.d;
+    p.E = a.E;
+    p.Np = a.E <= 16 ? 16 : (a.E + 15) / 16 * 16;  // MMA N: a multiple of 16, at least 16
+    p.k = a.k;
+    p.score = a.score;
+    p.renorm = a.renorm;
+    p.logit_bias = a.logit_bias;
+    p.sel_bias = a.sel_bias;
+    p.idx = a.idx;
+    p.gate = a.gate;
+    p.status = a.status;
+    p.num_kb = (a.d + RK - 1) / RK;
+    p.m_tiles = (int)((a.T + RM - 1) / RM);
+    p.stage_bytes = RM * RK * 2 + p.Np * RK * 2;
+    p.stages = R_SMEM_TILES / p.stage_bytes;
+    if (p.stages > R_MAX_STAGES) p.stages = R_MAX_STAGES;
+    CUtensorMap tmX, tmW;
+    if (!make_tmap_bf16(&tmX, a.x, (uint64_t)a.d, (uint64_t)a.T, 1, RM, 2) ||
+        !make_tmap_bf16(&tmW, a.w, (uint64_t)a.d, (uint64_t)a.E, 1, (uint32_t)p.Np, 2))
+        return cudaErrorInvalidValue;
+    const int smem = p.stages * p.stage_bytes + R_SMEM_EXTRA;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    static int attr_bytes = 0;
+    if (attr_bytes < smem) {
+        cudaError_t e =
+            cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_bytes = smem;
+    }
+    const int grid = p.m_tiles < sms ? p.m_tiles : sms;
+    route_tc_kernel<<<grid, R_THREADS, smem, s>>>(tmX, tmW, p);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -125,8 +125,12 @@ def test_invalid_calls_fail_before_any_launch():
     assert e.value.status == moe.MOE_ERR_INVALID_ARG
     # selection-only bias needs sigmoid scores
     with pytest.raises(moe.MoeError) as e:
-        moe.moe_route(c, 0x1000, 0x2000, None, 0x5000, 0x3000, 0x4000, None, stream=0)
+        moe.moe_route(c, 0x1000, 0x2000, None, 0x5000, 0x3000, 0x4000, 0x6000, stream=0)
     assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+    # the route needs a workspace (its status word)
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_route(c, 0x1000, 0x2000, None, None, 0x3000, 0x4000, None, stream=0)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
     with pytest.raises(moe.MoeError) as e:
         moe.moe_dispatch(c, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, None, 0x7000, 0x8000, None,
                          0x9000, 0xa000, stream=0)
