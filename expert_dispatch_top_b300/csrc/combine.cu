@@ -7,16 +7,19 @@
 // residual carries a fully dropped token through unchanged (ai360xpert "Load
 // Balancing and Dropped Tokens"; Ultralytics "Load Balancing and Capacity").
 //
-// One warp per token, grid-stride; each lane moves 16-byte vectors.  The
-// k expert rows of a token are independent loads issued back to back, fp32
-// accumulation in slot order, one rounding to the output type.
+// One warp per token, grid-stride; each lane moves 16-byte vectors.  The k
+// expert rows of a token, for U column vectors at a time, are independent
+// loads issued back to back (8 in flight per lane); fp32 accumulation in slot
+// order, one rounding to the output type.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 namespace {
 
-template <typename T>
+// KMAX: compile-time bound on k; U: 16-byte column vectors per lane in flight.
+// U * KMAX = 8 keeps eight independent row loads in flight per lane.
+template <typename T, int KMAX, int U>
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     constexpr int V = Elem<T>::kPerVec;
     const int lane = threadIdx.x & 31;
@@ -35,45 +38,65 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
             r_l = a.slot_row[t * a.k + lane];
             g_l = a.gate[t * a.k + lane];
         }
-        int r[8];
-        float g[8];
+        int r[KMAX];
+        float g[KMAX];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < KMAX; ++j) {
             r[j] = __shfl_sync(0xffffffffu, r_l, j);
             g[j] = __shfl_sync(0xffffffffu, g_l, j);
             if (j >= a.k) r[j] = -1;
         }
-        for (int c = lane; c < nvec; c += 32) {
-            float acc[V];
+        for (int c0 = lane; c0 < nvec; c0 += 32 * U) {
+            uint4 v[U][KMAX];
 #pragma unroll
-            for (int q = 0; q < V; ++q) acc[q] = 0.f;
-            uint4 v[8];
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + 32 * u;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (r[j] >= 0) v[j] = ld_nc_v4(yp + (int64_t)r[j] * row_bytes + (int64_t)c * 16);
+                for (int j = 0; j < KMAX; ++j)
+                    if (c < nvec && r[j] >= 0)
+                        v[u][j] = ld_nc_v4(yp + (int64_t)r[j] * row_bytes + (int64_t)c * 16);
+            }
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (r[j] >= 0) {
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + 32 * u;
+                if (c >= nvec) break;
+                float acc[V];
+#pragma unroll
+                for (int q = 0; q < V; ++q) acc[q] = 0.f;
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j)
+                    if (r[j] >= 0) {
+                        float f[V];
+                        Elem<T>::unpack(v[u][j], f);
+#pragma unroll
+                        for (int q = 0; q < V; ++q) acc[q] = fmaf(g[j], f[q], acc[q]);
+                    }
+                if (sh) {
                     float f[V];
-                    Elem<T>::unpack(v[j], f);
+                    Elem<T>::unpack(ld_nc_v4(sh + t * row_bytes + (int64_t)c * 16), f);
 #pragma unroll
-                    for (int q = 0; q < V; ++q) acc[q] = fmaf(g[j], f[q], acc[q]);
+                    for (int q = 0; q < V; ++q) acc[q] += f[q];
                 }
-            if (sh) {
-                float f[V];
-                Elem<T>::unpack(ld_nc_v4(sh + t * row_bytes + (int64_t)c * 16), f);
+                if (rs) {
+                    float f[V];
+                    Elem<T>::unpack(ld_nc_v4(rs + t * row_bytes + (int64_t)c * 16), f);
 #pragma unroll
-                for (int q = 0; q < V; ++q) acc[q] += f[q];
+                    for (int q = 0; q < V; ++q) acc[q] += f[q];
+                }
+                st_cs_v4(y + t * row_bytes + (int64_t)c * 16, Elem<T>::pack(acc));
             }
-            if (rs) {
-                float f[V];
-                Elem<T>::unpack(ld_nc_v4(rs + t * row_bytes + (int64_t)c * 16), f);
-#pragma unroll
-                for (int q = 0; q < V; ++q) acc[q] += f[q];
-            }
-            st_cs_v4(y + t * row_bytes + (int64_t)c * 16, Elem<T>::pack(acc));
         }
     }
+}
+
+template <typename T>
+void launch_combine_typed(const CombineArgs& a, unsigned blocks, cudaStream_t s) {
+    if (a.k <= 2)
+        combine_kernel<T, 2, 4><<<blocks, 256, 0, s>>>(a);
+    else if (a.k <= 4)
+        combine_kernel<T, 4, 2><<<blocks, 256, 0, s>>>(a);
+    else
+        combine_kernel<T, 8, 1><<<blocks, 256, 0, s>>>(a);
 }
 
 }  // namespace
@@ -87,9 +110,9 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
     const int64_t cap = (int64_t)sms * 16;
     if (blocks > cap) blocks = cap;
     if (a.dtype == MOE_DTYPE_F32)
-        combine_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(a);
+        launch_combine_typed<float>(a, (unsigned)blocks, s);
     else
-        combine_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(a);
+        launch_combine_typed<__nv_bfloat16>(a, (unsigned)blocks, s);
     return cudaGetLastError();
 }
 

@@ -15,7 +15,7 @@
 //                    finish turns them into capacity-clipped counts and the
 //                    expert offsets.  It also clears the scan state used by
 //                    place_kernel.
-//   place_kernel  -- 32 tokens per block, blocks ordered by an atomic ticket.
+//   place_kernel  -- 32, 64 or 128 tokens per block, blocks ordered by an atomic ticket.
 //                    A per-expert decoupled look-back over the blocks gives
 //                    each assignment its position among the same expert's
 //                    assignments in token order; the position decides
@@ -29,7 +29,7 @@
 namespace moe {
 namespace {
 
-constexpr int kPlaceTokens = 32;  // tokens per place_kernel block (one warp's worth)
+constexpr int kPlaceTokens = 32;  // smallest place_kernel block: one warp's worth of tokens
 constexpr int kPlaceThreads = 256;
 constexpr int kMaxRanks = 32;     // virtual ranks supported by the send-count accumulator
 constexpr uint64_t kFlagAgg = 1ull << 32;   // descriptor holds the block's own count
@@ -120,36 +120,43 @@ __global__ void __launch_bounds__(256) count_kernel(DispatchArgs a, int64_t n_de
         a.rank_counts[r] = a.expert_offsets[(r + 1) * per] - a.expert_offsets[r * per];
 }
 
-template <typename T>
+// SUB sub-tiles of 32 tokens per block (TB = 32*SUB tokens): warp s < SUB
+// ranks sub-tile s with per-expert lane bitmaps; larger blocks amortise the
+// block's fixed costs (ticket, look-back, barriers) over more row copies.
+template <typename T, int SUB>
 __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
-    __shared__ uint32_t bits[256];      // per expert: lanes (tokens) of this block that chose it
-    __shared__ int prefix[256];         // per expert: assignments in earlier blocks
+    constexpr int TB = 32 * SUB;
+    __shared__ uint32_t bits[SUB][256];  // per sub-tile and expert: lanes (tokens) that chose it
+    __shared__ int wpre[SUB][256];       // per sub-tile and expert: assignments in earlier sub-tiles
+    __shared__ int prefix[256];          // per expert: assignments in earlier blocks
     __shared__ int offs[256];
-    __shared__ int rows[kPlaceTokens][8];
+    __shared__ int rows[TB][8];
     __shared__ int split_acc[kMaxRanks * kMaxRanks];  // [src][dst] kept rows of this block
     __shared__ uint32_t blk_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) blk_s = atomicAdd(a.ticket, 1u);
     for (int e = tid; e < a.E; e += kPlaceThreads) {
-        bits[e] = 0u;
+#pragma unroll
+        for (int sb = 0; sb < SUB; ++sb) bits[sb][e] = 0u;
         offs[e] = a.expert_offsets[e];
     }
     for (int i = tid; i < a.R * a.R; i += kPlaceThreads) split_acc[i] = 0;
     __syncthreads();
     const uint32_t blk = blk_s;
-    const int64_t t0 = (int64_t)blk * kPlaceTokens;
-    const int64_t t = t0 + lane;
-    const bool live = t < a.T;
+    const int64_t t0 = (int64_t)blk * TB;
+    const int64_t t = t0 + warp * 32 + lane;  // meaningful for warps < SUB
+    const bool live = warp < SUB && t < a.T;
     int my_e[8];
-    if (warp == 0) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) my_e[j] = -1;
+    if (warp < SUB) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            my_e[j] = -1;
             if (j < a.k && live) {
                 const int e = a.idx[t * a.k + j];
                 if ((unsigned)e < (unsigned)a.E) {
                     my_e[j] = e;
-                    atomicOr(&bits[e], 1u << lane);
+                    atomicOr(&bits[warp][e], 1u << lane);
                 }
             }
         }
@@ -158,7 +165,12 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
     // Per-expert decoupled look-back over the preceding blocks.
     uint64_t* desc = a.desc + (int64_t)blk * a.E;
     for (int e = tid; e < a.E; e += kPlaceThreads) {
-        const int own = __popc(bits[e]);
+        int own = 0;
+#pragma unroll
+        for (int sb = 0; sb < SUB; ++sb) {
+            wpre[sb][e] = own;
+            own += __popc(bits[sb][e]);
+        }
         if (blk == 0) {
             st_relaxed_u64(desc + e, kFlagIncl | (uint32_t)own);
             prefix[e] = 0;
@@ -190,7 +202,7 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
     }
     __syncthreads();
     // Positions, keep/drop, rows.
-    if (warp == 0) {
+    if (warp < SUB) {
         const int per = a.E / a.R;
         const int64_t src_size = (a.T + a.R - 1) / a.R;
         const int src = live ? (int)(t / src_size) : 0;
@@ -200,7 +212,7 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
             int row = -1;
             const int e = my_e[j];
             if (e >= 0) {
-                const int pos = prefix[e] + __popc(bits[e] & lanemask_lt());
+                const int pos = prefix[e] + wpre[warp][e] + __popc(bits[warp][e] & lanemask_lt());
                 if (a.C < 0 || pos < a.C) {
                     row = offs[e] + pos;
                     a.row_token[row] = (int32_t)t;
@@ -208,7 +220,7 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
                 }
             }
             if (live) a.slot_row[t * a.k + j] = row;
-            rows[lane][j] = row;
+            rows[warp * 32 + lane][j] = row;
         }
     }
     __syncthreads();
@@ -220,27 +232,68 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
             if (v) atomicAdd(&splits[i], v);
         }
     }
-    // Row copies: x[t] -> xp[row] for every kept row, 16-byte vectors.
+    // Row copies: x[t] -> xp[row] for every kept row, 16-byte vectors, eight
+    // loads in flight per thread.  Rows of >= 256 chunks (4 KB): one warp per
+    // token, lanes along the row.  Shorter rows: the block's 256 threads walk
+    // the (token, chunk) space of its TB rows together, each stepping its pair
+    // by 256 chunks, so short rows keep as many bytes in flight as long ones.
     const int nvec = a.d * (int)sizeof(T) / 16;
+    const int64_t row_bytes = (int64_t)a.d * sizeof(T);
     const char* x = static_cast<const char*>(a.x);
     char* xp = static_cast<char*>(a.xp);
-    for (int tok = warp; tok < kPlaceTokens; tok += kPlaceThreads / 32) {
-        const int64_t tt = t0 + tok;
-        if (tt >= a.T) break;
-        int r[8];
-        int nk = 0;
+    const int ntok = (int)((a.T - t0) < TB ? (a.T - t0) : TB);
+    if (nvec >= kPlaceThreads) {
+        for (int tok = warp; tok < ntok; tok += kPlaceThreads / 32) {
+            int r[8];
+            int nk = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            r[j] = (j < a.k) ? rows[tok][j] : -1;
-            nk += r[j] >= 0;
+            for (int j = 0; j < 8; ++j) {
+                r[j] = (j < a.k) ? rows[tok][j] : -1;
+                nk += r[j] >= 0;
+            }
+            if (nk == 0) continue;
+            const char* src = x + (t0 + tok) * row_bytes;
+            for (int c0 = lane; c0 < nvec; c0 += 256) {
+                uint4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (c0 + 32 * u < nvec) v[u] = ld_nc_v4(src + (int64_t)(c0 + 32 * u) * 16);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (c >= nvec) break;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (r[j] >= 0) st_v4(xp + (int64_t)r[j] * row_bytes + (int64_t)c * 16, v[u]);
+                }
+            }
         }
-        if (nk == 0) continue;
-        const char* src = x + tt * (int64_t)a.d * sizeof(T);
-        for (int c = lane; c < nvec; c += 32) {
-            const uint4 v = ld_nc_v4(src + (int64_t)c * 16);
+        return;
+    }
+    int tok = tid / nvec, c = tid - (tid / nvec) * nvec;
+    while (tok < ntok) {
+        uint4 v[8];
+        int vt[8], vc[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (r[j] >= 0) st_v4(xp + ((int64_t)r[j] * a.d * sizeof(T)) + (int64_t)c * 16, v);
+        for (int u = 0; u < 8; ++u) {
+            vt[u] = tok;
+            vc[u] = c;
+            if (tok < ntok) v[u] = ld_nc_v4(x + (t0 + tok) * row_bytes + (int64_t)c * 16);
+            c += kPlaceThreads;
+            while (c >= nvec) {
+                c -= nvec;
+                ++tok;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (vt[u] >= ntok) break;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j >= a.k) break;
+                const int r = rows[vt[u]][j];
+                if (r >= 0) st_v4(xp + (int64_t)r * row_bytes + (int64_t)vc[u] * 16, v[u]);
+            }
         }
     }
 }
@@ -249,8 +302,32 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
 
 int64_t dispatch_blocks(int64_t T) { return (T + kPlaceTokens - 1) / kPlaceTokens; }
 
+namespace {
+// Sub-tiles per place_kernel block: as large as keeps >= 2 blocks per SM.
+int place_sub(int64_t T) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t n32 = dispatch_blocks(T);
+    if (n32 >= 4 * 2 * (int64_t)sms) return 4;
+    if (n32 >= 2 * 2 * (int64_t)sms) return 2;
+    return 1;
+}
+
+template <typename T>
+void launch_place(const DispatchArgs& a, int sub, int64_t nblk, cudaStream_t s) {
+    if (sub == 4)
+        place_kernel<T, 4><<<(unsigned)nblk, kPlaceThreads, 0, s>>>(a);
+    else if (sub == 2)
+        place_kernel<T, 2><<<(unsigned)nblk, kPlaceThreads, 0, s>>>(a);
+    else
+        place_kernel<T, 1><<<(unsigned)nblk, kPlaceThreads, 0, s>>>(a);
+}
+}  // namespace
+
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
-    const int64_t nblk = dispatch_blocks(a.T);
+    const int sub = place_sub(a.T);
+    const int64_t nblk = (a.T + 32 * sub - 1) / (32 * sub);
     const int64_t n_desc = nblk * a.E;
     const int64_t n = a.T * a.k;
     int64_t cb = (n + 256 * 8 - 1) / (256 * 8);
@@ -262,9 +339,9 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || nblk == 0) return e;
     if (a.dtype == MOE_DTYPE_F32)
-        place_kernel<float><<<(unsigned)nblk, kPlaceThreads, 0, s>>>(a);
+        launch_place<float>(a, sub, nblk, s);
     else
-        place_kernel<__nv_bfloat16><<<(unsigned)nblk, kPlaceThreads, 0, s>>>(a);
+        launch_place<__nv_bfloat16>(a, sub, nblk, s);
     return cudaGetLastError();
 }
 
