@@ -91,6 +91,8 @@ def _load():
     lib.moe_combine.restype = i32
     lib.moe_layer_forward.argtypes = [cfgp] + [vp] * 8 + [ctypes.POINTER(moe_buffers), vp, vp, vp]
     lib.moe_layer_forward.restype = i32
+    lib.moe_update_sel_bias.argtypes = [cfgp, vp, vp, ctypes.c_float, vp]
+    lib.moe_update_sel_bias.restype = i32
     lib.moe_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.moe_read_device_status.restype = i32
     _lib = lib
@@ -209,6 +211,14 @@ def moe_layer_forward(cfg, x, w_router, logit_bias, sel_bias, w_up, w_down, shar
                                      _p(sel_bias), _p(w_up), _p(w_down), _p(shared_up),
                                      _p(shared_down), ctypes.byref(buffers), _p(y), _p(ws),
                                      _stream(stream)), "moe_layer_forward")
+
+
+def moe_update_sel_bias(cfg, expert_counts, sel_bias, gamma, stream=None):
+    """Bias-based balancing step on the device: sel_bias -= gamma for experts
+    above the even share T*k/E, += gamma below it (in place)."""
+    _check(_load().moe_update_sel_bias(ctypes.byref(cfg), _p(expert_counts), _p(sel_bias),
+                                       ctypes.c_float(gamma), _stream(stream)),
+           "moe_update_sel_bias")
 
 
 def moe_read_device_status(ws, stream=None) -> int:

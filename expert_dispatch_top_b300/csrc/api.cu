@@ -379,6 +379,17 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w
     return combine_impl(cfg, yp, slot_row, gate, buf->shared_out, x, y, s);
 }
 
+moe_status moe_update_sel_bias(const moe_config* cfg, const int32_t* expert_counts, float* sel_bias,
+                               float gamma, moe_stream_t stream) {
+    moe_status st = moe_check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!expert_counts || !sel_bias || !aligned4(expert_counts) || !aligned4(sel_bias))
+        return MOE_ERR_INVALID_ARG;
+    if (!(gamma >= 0.f) || gamma == INFINITY) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_update_sel_bias(expert_counts, sel_bias, cfg->E, cfg->T, cfg->k, gamma,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_read_device_status(const void* ws, uint32_t* out, moe_stream_t stream) {
     if (!ws || !out) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -78,4 +78,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s);
 // Returns 0 if the tensor-core grouped GEMM supports the shape, else non-zero.
 int gemm_tc_supported(const GemmArgs& a);
 
+cudaError_t launch_update_sel_bias(const int32_t* counts, float* bias, int E, int64_t T, int k,
+                                   float gamma, cudaStream_t s);
+
 }  // namespace moe

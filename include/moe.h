@@ -258,6 +258,19 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w
                              const void* w_down, const void* shared_up, const void* shared_down,
                              const moe_buffers* buf, void* y, void* ws, moe_stream_t stream);
 
+/*
+ * Bias-based balancing (Ultralytics "Load Balancing and Capacity": DeepSeek-V3
+ * lowers the selection bias of overloaded experts and raises it for idle ones
+ * after each step).  For each expert e: if expert_counts[e] * E > T * k (load
+ * above the even share) sel_bias[e] -= gamma; if below, sel_bias[e] += gamma;
+ * if equal, unchanged.  The comparison is exact (64-bit integers); the update
+ * is one fp32 add.  expert_counts [E] (device, e.g. moe_dispatch's output,
+ * counted before drops); sel_bias [E] fp32 (device, updated in place);
+ * gamma >= 0 and finite (the pages give no step size).  Enqueued on stream.
+ */
+moe_status moe_update_sel_bias(const moe_config* cfg, const int32_t* expert_counts, float* sel_bias,
+                               float gamma, moe_stream_t stream);
+
 /* Copies the device status word of `ws` to *out (HOST pointer), waiting for
    `stream`, then clears it.  MOE_OK with *out == 0 means no device error. */
 moe_status moe_read_device_status(const void* ws, uint32_t* out, moe_stream_t stream);

@@ -73,6 +73,8 @@ def _load():
         lib.oracle_expert_ffn.restype = None
         lib.oracle_combine.argtypes = [i64, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, vp]
         lib.oracle_combine.restype = None
+        lib.oracle_update_sel_bias.argtypes = [i64, i32, i32, vp, vp, ctypes.c_float]
+        lib.oracle_update_sel_bias.restype = None
         _lib = lib
     return _lib
 
@@ -200,6 +202,15 @@ def combine(tokens, yp_rows, row_map, slot_row, topk_gate, shared=None, resid=No
                            _ptr(g), _ptr(sh), _dtype_code(rs) if rs is not None else F32, _ptr(rs),
                            _ptr(y))
     return y
+
+
+def update_sel_bias(expert_counts, sel_bias, T, k, gamma):
+    """Bias-based balancing step: returns the updated fp32 selection bias."""
+    counts = _cpu(expert_counts, torch.int32)
+    out = _cpu(sel_bias, torch.float32).clone()
+    _load().oracle_update_sel_bias(int(T), int(k), counts.numel(), _ptr(counts), _ptr(out),
+                                   ctypes.c_float(gamma))
+    return out
 
 
 def layer_forward(x, w_router, *, k, E, R, d_ff, act, score="softmax", renorm=True,

@@ -359,3 +359,22 @@ void oracle_combine(int64_t n_tok, const int64_t* toks, int d, int k, const doub
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Bias-based balancing (Ultralytics, Load Balancing and Capacity: DeepSeek-V3 */
+/* lowers the selection bias of overloaded experts and raises it for idle     */
+/* ones after each step).  The step size gamma is not on the pages.  Reading: */
+/* an expert whose load is above the even share T*k/E is overloaded (bias -=  */
+/* gamma), one below it is underloaded (bias += gamma), one exactly at it is   */
+/* left alone; the comparison is exact (count*E against T*k in integers) and   */
+/* the update is one fp32 addition.                                            */
+/* ------------------------------------------------------------------------ */
+void oracle_update_sel_bias(int64_t T, int k, int E, const int32_t* counts, float* bias,
+                            float gamma) {
+    const int64_t even = T * (int64_t)k;
+    for (int e = 0; e < E; ++e) {
+        const int64_t load = (int64_t)counts[e] * E;
+        if (load > even) bias[e] = bias[e] - gamma;
+        else if (load < even) bias[e] = bias[e] + gamma;
+    }
+}

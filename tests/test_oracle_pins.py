@@ -418,3 +418,47 @@ def test_switch_workload_drop_fraction_in_band():
     d = oracle.dispatch(idx, w.E, w.R, C)
     frac = d["n_dropped"] / (w.T * w.k)
     assert 0.05 <= frac <= 0.20, frac
+
+
+# --------------------------------------------------------------------------
+# Bias-based balancing (Ultralytics "Load Balancing and Capacity", DeepSeek-V3)
+# --------------------------------------------------------------------------
+
+def _skewed_router(T=2048, E=16, k=2, d=64, seed=6):
+    w = W.WORKLOADS["deepseek"].replace(T=T, d=d, E=E, R=4, k=k, d_ff=64, act="identity",
+                                        n_shared=0, sel_skew=1.5, sel_bias_std=0.0)
+    return w, W.make_inputs(w, ffn=False)
+
+
+def test_balancing_step_direction():
+    """One step lowers the bias of every expert above the even share, raises
+    it for every expert below, and leaves exact-share experts alone."""
+    counts = torch.tensor([5, 1, 2, 0, 2], dtype=torch.int32)   # T*k = 10, E = 5: share 2
+    bias = torch.tensor([0.5, -0.25, 0.125, 0.0, 1.0])
+    out = oracle.update_sel_bias(counts, bias, T=5, k=2, gamma=0.0625)
+    assert out.tolist() == [0.4375, -0.1875, 0.125, 0.0625, 1.0]
+    # the even share need not be an integer: T*k/E = 7/3
+    out = oracle.update_sel_bias(torch.tensor([3, 2, 2], dtype=torch.int32),
+                                 torch.zeros(3), T=7, k=1, gamma=0.5)
+    assert out.tolist() == [-0.5, 0.5, 0.5]
+
+
+def test_balancing_reduces_load_imbalance():
+    """Iterating route -> count -> update on a skewed router evens out the
+    load without touching the gates' scores (the purpose the pages state)."""
+    w, inp = _skewed_router()
+    bias = inp["sel_bias"].clone()
+    T, k, E = w.T, w.k, w.E
+
+    def spread(b):
+        idx, _ = oracle.route(inp["x"], inp["w_router"], k, "sigmoid", True, None, b)
+        c = oracle.dispatch(idx, E, w.R, -1)["expert_counts"].double()
+        return c, float(c.max() / c.mean())
+
+    c0, s0 = spread(bias)
+    assert s0 > 1.6, s0
+    for _ in range(60):
+        c, _ = spread(bias)
+        bias = oracle.update_sel_bias(c.int(), bias, T, k, gamma=2.0 ** -8)
+    _, s1 = spread(bias)
+    assert s1 < 1.25 and s1 < s0, (s0, s1)
