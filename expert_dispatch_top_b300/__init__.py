@@ -47,7 +47,8 @@ class moe_config(ctypes.Structure):
                 ("n_shared", ctypes.c_int32), ("act_dtype", ctypes.c_int32),
                 ("score", ctypes.c_int32), ("renorm", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_float), ("capacity", ctypes.c_int32),
-                ("act", ctypes.c_int32), ("add_residual", ctypes.c_int32)]
+                ("act", ctypes.c_int32), ("add_residual", ctypes.c_int32),
+                ("max_ranks", ctypes.c_int32)]
 
 
 class moe_buffers(ctypes.Structure):
@@ -130,10 +131,11 @@ def _stream(stream):
 
 
 def make_config(T, d, E, k, R, d_ff=0, n_shared=0, dtype="bf16", score="softmax", renorm=True,
-                capacity_factor=0.0, capacity=0, act="swiglu", add_residual=False) -> moe_config:
+                capacity_factor=0.0, capacity=0, act="swiglu", add_residual=False,
+                max_ranks=0) -> moe_config:
     return moe_config(int(T), int(d), int(E), int(k), int(R), int(d_ff), int(n_shared),
                       _DTYPES[dtype], _SCORES[score], int(bool(renorm)), float(capacity_factor),
-                      int(capacity), _ACTS[act], int(bool(add_residual)))
+                      int(capacity), _ACTS[act], int(bool(add_residual)), int(max_ranks))
 
 
 def config_from_workload(w, T: Optional[int] = None, add_residual: Optional[bool] = None,
@@ -141,7 +143,8 @@ def config_from_workload(w, T: Optional[int] = None, add_residual: Optional[bool
     """moe_config of a workload description (any object with the Workload fields)."""
     return make_config(w.T if T is None else T, w.d, w.E, w.k, w.R, w.d_ff, w.n_shared, w.dtype,
                        w.score, w.renorm, w.capacity_factor, capacity, w.act,
-                       w.add_residual if add_residual is None else add_residual)
+                       w.add_residual if add_residual is None else add_residual,
+                       getattr(w, "max_ranks", 0))
 
 
 def moe_check_config(cfg: moe_config) -> int:

@@ -101,6 +101,8 @@ moe_status route_impl(const moe_config* c, const void* x, const void* w, const f
         !aligned4(sb))
         return MOE_ERR_INVALID_ARG;
     if (sb && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_UNSUPPORTED;
+    const bool limited = c->max_ranks > 0 && c->max_ranks < c->R;
+    if (limited && c->act_dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
     RouteArgs a;
     a.x = x;
     a.w = w;
@@ -116,6 +118,8 @@ moe_status route_impl(const moe_config* c, const void* x, const void* w, const f
     a.score = c->score;
     a.renorm = c->renorm;
     a.dtype = c->act_dtype;
+    a.R = c->R;
+    a.max_ranks = limited ? c->max_ranks : 0;
     return cuda_status(launch_route(a, s));
 }
 
@@ -282,6 +286,9 @@ moe_status moe_check_config(const moe_config* c) {
         return MOE_ERR_INVALID_ARG;
     if (c->n_shared < 0 || c->n_shared > 1) return MOE_ERR_INVALID_ARG;
     if (c->capacity < 0 || !(c->capacity_factor == c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+    if (c->max_ranks < 0 || c->max_ranks > c->R ||
+        (c->max_ranks > 0 && (int64_t)c->max_ranks * (c->E / c->R) < c->k))
+        return MOE_ERR_INVALID_ARG;
     if (((int64_t)c->d * elem_bytes(c)) % 16 != 0) return MOE_ERR_INVALID_ARG;
     return check_ffn_config(c);
 }

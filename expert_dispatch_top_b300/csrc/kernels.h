@@ -16,6 +16,7 @@ struct RouteArgs {
     uint32_t* status;  // device status word (bounded-wait timeouts)
     int64_t T;
     int d, E, k, score, renorm, dtype;
+    int R, max_ranks;  // rank-limited routing when 0 < max_ranks < R (tensor-core router)
 };
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 // Tensor-core router (bf16, E <= 256): 0 if supported.

@@ -46,18 +46,23 @@ namespace {
 using namespace tc;
 
 constexpr int RM = 128, RK = 64;
-constexpr int STASH_PITCH = 33;  // floats per epilogue thread (32 logits + pad: conflict-free)
-constexpr int STASH_BYTES = 128 * STASH_PITCH * 4;
+// Per epilogue thread: 32 stashed logits (+1 pad), and with rank limiting two
+// rows of 32 rank scores; odd pitches keep the per-thread rows conflict-free.
+constexpr int STASH_PITCH = 33;
+constexpr int STASH_PITCH_RANKS = 97;
 constexpr int R_THREADS = 192;
 constexpr int R_MAX_STAGES = 8;
 constexpr uint32_t R_TMEM_COLS = 512;
 constexpr int R_SMEM_TILES = 196608;  // bytes of stage ring
-constexpr int R_SMEM_EXTRA = 1024 /*align*/ + 256 /*barriers*/ + 2 * 256 * 4 /*biases*/ + STASH_BYTES;
+constexpr int R_SMEM_FIXED = 1024 /*align*/ + 256 /*barriers*/ + 2 * 256 * 4 /*biases*/;
+constexpr int R_SMEM_MAX = 232448;  // 227 KB per block
 constexpr float kApproxDelta = 1.0f / 256.0f;
 
 struct RtParams {
     int64_t T;
     int d, E, Np, k, score, renorm;
+    int R, max_ranks;   // rank-limited routing when max_ranks > 0
+    int stash_pitch;    // floats of shared memory per epilogue thread
     const float* logit_bias;
     const float* sel_bias;
     int32_t* idx;
@@ -118,6 +123,22 @@ struct TopK {
     }
 };
 
+// The best m of R scores s[0..R) by rounds of selection (ties to the lower
+// rank): returns the bit set of chosen ranks and, in *mth, the m-th score.
+__device__ __forceinline__ uint32_t pick_ranks(const float* sc, int R, int m, float* mth) {
+    uint32_t chosen = 0;
+    float last = -INFINITY;
+    for (int j = 0; j < m; ++j) {
+        int best = -1;
+        for (int r = 0; r < R; ++r)
+            if (!((chosen >> r) & 1u) && (best < 0 || sc[r] > sc[best])) best = r;
+        chosen |= 1u << best;
+        last = sc[best];
+    }
+    *mth = last;
+    return chosen;
+}
+
 // First K block of a tile.  Every tile reads the same router weights; if all
 // CTAs walked K in the same order they would all hit the few L2 slices that
 // hold the current weight block at once.  Rotating the start per tile spreads
@@ -137,7 +158,7 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(extra + 196);
     float* lb_s = reinterpret_cast<float*>(extra + 256);
     float* sb_s = lb_s + 256;
-    float* stash_all = sb_s + 256;  // [128][STASH_PITCH]
+    float* stash_all = sb_s + 256;  // [128][p.stash_pitch]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + R_MAX_STAGES);
@@ -253,7 +274,12 @@ __global__ void __launch_bounds__(R_THREADS, 1)
         const bool sigmoid = p.score == MOE_SCORE_SIGMOID;
         const bool has_lb = p.logit_bias != nullptr;
         const bool has_sb = p.sel_bias != nullptr;
-        float* stash = stash_all + (threadIdx.x - 64) * STASH_PITCH;
+        float* stash = stash_all + (threadIdx.x - 64) * p.stash_pitch;
+        float* rank_a = stash + 33;  // rank scores (rank-limited routing only)
+        float* rank_x = stash + 65;
+        const bool limited = p.max_ranks > 0;
+        const int per = p.E / p.R;
+        const float inv_per = 1.0f / (float)per;  // (e + 1/2) * inv_per truncates to e / per exactly
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < p.m_tiles; tile += gridDim.x) {
@@ -267,6 +293,65 @@ __global__ void __launch_bounds__(R_THREADS, 1)
             TopK top;
             top.init();
             float v[32];
+            // Rank-limited routing: rank score = best key among the rank's
+            // experts; keep the max_ranks best ranks (ties to the lower rank).
+            uint32_t allowed = 0xffffffffu;
+            if (limited) {
+                for (int r = 0; r < p.R; ++r) rank_a[r] = -INFINITY;
+                for (int c = 0; c < nchunks; ++c) {
+                    tmem_ld32(tb + (uint32_t)(c * 32), v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = c * 32 + i;
+                        if (e < p.E) {
+                            const float L = has_lb ? __fadd_rn(v[i], lb_s[e]) : v[i];
+                            const float key =
+                                sigmoid ? __fadd_rn(sigmoid_approx(L), sb_s[e]) : L;
+                            const int r = (int)(((float)e + 0.5f) * inv_per);
+                            if (key > rank_a[r]) rank_a[r] = key;
+                        }
+                    }
+                }
+                float mth;
+                if (!sigmoid) {
+                    allowed = pick_ranks(rank_a, p.R, p.max_ranks, &mth);
+                } else {
+                    // Approximate rank scores are within delta of the exact
+                    // ones: a rank of the exact best set has approximate score
+                    // >= (m-th approximate) - 2 delta, and its best expert has
+                    // approximate key >= its approximate score - 2 delta.
+                    pick_ranks(rank_a, p.R, p.max_ranks, &mth);
+                    const float rthr = mth - 2.f * kApproxDelta;
+                    for (int r = 0; r < p.R; ++r) rank_x[r] = -INFINITY;
+                    for (int c = 0; c < nchunks; ++c) {
+                        tmem_ld32(tb + (uint32_t)(c * 32), v);
+                        uint32_t mask = 0;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int e = c * 32 + i;
+                            const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
+                            stash[i] = L;
+                            if (e < p.E) {
+                                const float a = __fadd_rn(sigmoid_approx(L), sb_s[e]);
+                                const float ra = rank_a[(int)(((float)e + 0.5f) * inv_per)];
+                                if (ra >= rthr && a >= ra - 2.f * kApproxDelta) mask |= 1u << i;
+                            }
+                        }
+                        while (mask) {
+                            const int i = __ffs(mask) - 1;
+                            mask &= mask - 1;
+                            const int e = c * 32 + i;
+                            const float key = __fadd_rn(sigmoid_exact(stash[i]), sb_s[e]);
+                            const int r = (int)(((float)e + 0.5f) * inv_per);
+                            if (key > rank_x[r]) rank_x[r] = key;
+                        }
+                    }
+                    allowed = pick_ranks(rank_x, p.R, p.max_ranks, &mth);
+                }
+            }
+            auto rank_ok = [&](int e) -> bool {
+                return !limited || ((allowed >> (int)(((float)e + 0.5f) * inv_per)) & 1u);
+            };
             if (!sigmoid) {
                 for (int c = 0; c < nchunks; ++c) {
                     tmem_ld32(tb + (uint32_t)(c * 32), v);
@@ -277,7 +362,7 @@ __global__ void __launch_bounds__(R_THREADS, 1)
                         const int e = c * 32 + i;
                         const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
                         stash[i] = L;
-                        if (e < p.E && L > thr) mask |= 1u << i;
+                        if (e < p.E && L > thr && rank_ok(e)) mask |= 1u << i;
                     }
                     while (mask) {
                         const int i = __ffs(mask) - 1;
@@ -299,7 +384,7 @@ __global__ void __launch_bounds__(R_THREADS, 1)
                         const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
                         stash[i] = L;
                         const float a = __fadd_rn(sigmoid_approx(L), sb_s[e & 255]);
-                        if (e < p.E && a > thr) mask |= 1u << i;
+                        if (e < p.E && a > thr && rank_ok(e)) mask |= 1u << i;
                     }
                     while (mask) {
                         const int i = __ffs(mask) - 1;
@@ -319,7 +404,7 @@ __global__ void __launch_bounds__(R_THREADS, 1)
                         const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
                         stash[i] = L;
                         const float a = __fadd_rn(sigmoid_approx(L), sb_s[e & 255]);
-                        if (e < p.E && a >= thresh) mask |= 1u << i;
+                        if (e < p.E && a >= thresh && rank_ok(e)) mask |= 1u << i;
                     }
                     while (mask) {
                         const int i = __ffs(mask) - 1;
@@ -415,14 +500,19 @@ cudaError_t launch_route_tc(const RouteArgs& a, cudaStream_t s) {
     p.status = a.status;
     p.num_kb = (a.d + RK - 1) / RK;
     p.m_tiles = (int)((a.T + RM - 1) / RM);
+    p.R = a.R > 0 ? a.R : 1;
+    p.max_ranks = (a.max_ranks > 0 && a.max_ranks < p.R && p.R <= 32) ? a.max_ranks : 0;
+    p.stash_pitch = p.max_ranks > 0 ? STASH_PITCH_RANKS : STASH_PITCH;
+    const int extra = R_SMEM_FIXED + 128 * p.stash_pitch * 4;
+    const int ring = (R_SMEM_MAX - extra) < R_SMEM_TILES ? (R_SMEM_MAX - extra) : R_SMEM_TILES;
     p.stage_bytes = RM * RK * 2 + p.Np * RK * 2;
-    p.stages = R_SMEM_TILES / p.stage_bytes;
+    p.stages = ring / p.stage_bytes;
     if (p.stages > R_MAX_STAGES) p.stages = R_MAX_STAGES;
     CUtensorMap tmX, tmW;
     if (!make_tmap_bf16(&tmX, a.x, (uint64_t)a.d, (uint64_t)a.T, 1, RM, 2) ||
         !make_tmap_bf16(&tmW, a.w, (uint64_t)a.d, (uint64_t)a.E, 1, (uint32_t)p.Np, 2))
         return cudaErrorInvalidValue;
-    const int smem = p.stages * p.stage_bytes + R_SMEM_EXTRA;
+    const int smem = p.stages * p.stage_bytes + extra;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -83,6 +83,12 @@ enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1, MOE_ACT_IDENTITY = 2 };
  *   * (up x)); IDENTITY: the expert returns its input).  No biases.
  *   add_residual: combine adds x to the MoE output, so a fully dropped token
  *   leaves the layer unchanged.
+ *   max_ranks: rank-limited routing (Ultralytics "Load Balancing and
+ *   Capacity": DeepSeek-V3 sends each token to experts on at most 4 nodes).
+ *   A rank's score is the best selection key among its E/R experts; the
+ *   max_ranks best ranks are kept (ties to the lower rank) and the top-k is
+ *   taken among their experts.  Needs max_ranks <= R and max_ranks*(E/R) >= k;
+ *   bf16 routers only (MOE_ERR_UNSUPPORTED for fp32).
  */
 typedef struct moe_config {
     int32_t T;
@@ -99,6 +105,7 @@ typedef struct moe_config {
     int32_t capacity;       /* > 0: explicit per-expert capacity */
     int32_t act;            /* MOE_ACT_* */
     int32_t add_residual;   /* 0 or 1 */
+    int32_t max_ranks;      /* > 0: rank-limited routing (see below); 0: no limit */
 } moe_config;
 
 /* Human-readable name of a status code (static string, never NULL). */

@@ -60,6 +60,7 @@ class Workload:
     sel_bias_std: float = 0.0  # std of the selection-only bias (0: none)
     sel_skew: float = 0.0      # Zipf exponent added to the selection-only bias
     add_residual: bool = False
+    max_ranks: int = 0         # rank-limited routing: at most this many ranks per token (0: none)
 
     @property
     def torch_dtype(self):

@@ -61,7 +61,8 @@ def _load():
         lib.oracle_num_threads.restype = i32
         lib.oracle_sigmoid32.argtypes = [ctypes.c_float]
         lib.oracle_sigmoid32.restype = ctypes.c_float
-        lib.oracle_route.argtypes = [i64, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+        lib.oracle_route.argtypes = [i64, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, i32, i32,
+                                     vp, vp, vp]
         lib.oracle_route.restype = i32
         lib.oracle_capacity.argtypes = [i64, i32, i32, dbl, i64]
         lib.oracle_capacity.restype = i64
@@ -111,8 +112,10 @@ def sigmoid32(L: float) -> float:
 
 
 def route(x, w_router, k, score="softmax", renorm=True, logit_bias=None, sel_bias=None,
-          return_logits=False):
-    """Step 1 (Route).  Returns (topk_idx int32 [T,k], topk_gate fp32 [T,k][, logits fp32 [T,E]])."""
+          return_logits=False, R=0, max_ranks=0):
+    """Step 1 (Route).  Returns (topk_idx int32 [T,k], topk_gate fp32 [T,k][, logits fp32 [T,E]]).
+    max_ranks > 0 limits every token to experts on at most that many of the R
+    virtual ranks (contiguous blocks of E/R experts)."""
     x = _cpu(x)
     w = _cpu(w_router, x.dtype)
     T, d = x.shape
@@ -123,8 +126,8 @@ def route(x, w_router, k, score="softmax", renorm=True, logit_bias=None, sel_bia
     gate = torch.empty((T, k), dtype=torch.float32)
     logits = torch.empty((T, E), dtype=torch.float32) if return_logits else None
     rc = _load().oracle_route(T, d, E, k, _dtype_code(x), _SCORES[score], int(bool(renorm)),
-                              _ptr(x), _ptr(w), _ptr(lb), _ptr(sb), _ptr(idx), _ptr(gate),
-                              _ptr(logits))
+                              _ptr(x), _ptr(w), _ptr(lb), _ptr(sb), int(R), int(max_ranks),
+                              _ptr(idx), _ptr(gate), _ptr(logits))
     if rc != 0:
         raise ValueError("oracle_route: unsupported arguments")
     return (idx, gate, logits) if return_logits else (idx, gate)
@@ -216,7 +219,7 @@ def update_sel_bias(expert_counts, sel_bias, T, k, gamma):
 def layer_forward(x, w_router, *, k, E, R, d_ff, act, score="softmax", renorm=True,
                   capacity_factor=0.0, explicit_capacity=0, logit_bias=None, sel_bias=None,
                   w_up=None, w_down=None, shared_up=None, shared_down=None,
-                  add_residual=False, tokens=None):
+                  add_residual=False, tokens=None, max_ranks=0):
     """The four steps in the pages' order.  ``tokens`` restricts the expert
     compute and the combine to a subset of tokens (routing and dispatch always
     cover every token, since capacity decisions depend on all of them); each
@@ -227,7 +230,8 @@ def layer_forward(x, w_router, *, k, E, R, d_ff, act, score="softmax", renorm=Tr
     """
     x = _cpu(x)
     T, d = x.shape
-    idx, gate = route(x, w_router, k, score, renorm, logit_bias, sel_bias)
+    idx, gate = route(x, w_router, k, score, renorm, logit_bias, sel_bias, R=R,
+                      max_ranks=max_ranks)
     C = capacity(T, k, E, capacity_factor, explicit_capacity)
     disp = dispatch(idx, E, R, C)
     toks = torch.arange(T, dtype=torch.int64) if tokens is None else \

@@ -112,10 +112,13 @@ float oracle_sigmoid32(float L) {
  */
 int oracle_route(int64_t T, int d, int E, int k, int dtype, int score, int renorm,
                  const void* x, const void* w_router, const float* logit_bias,
-                 const float* sel_bias, int32_t* topk_idx, float* topk_gate,
-                 float* logits_out) {
+                 const float* sel_bias, int R, int max_ranks, int32_t* topk_idx,
+                 float* topk_gate, float* logits_out) {
     if (k < 1 || k > E) return -1;
     if (score == OR_SOFTMAX && sel_bias) return -1;
+    if (max_ranks > 0 && (R < 1 || E % R != 0 || max_ranks > R || max_ranks * (E / R) < k))
+        return -1;
+    const int per = (R > 0) ? E / R : E;
     int bad = 0;
 #pragma omp parallel
     {
@@ -139,6 +142,33 @@ int oracle_route(int64_t T, int d, int E, int k, int dtype, int score, int renor
                     }
                     taken[e] = 0;
                     if (logits_out) logits_out[t * E + e] = L[e];
+                }
+                /* Rank-limited routing (DeepSeek-V3 sends a token to experts on
+                   at most max_ranks devices; Ultralytics, Load Balancing and
+                   Capacity).  Reading: a rank's score is the best key among its
+                   experts; max_ranks rounds pick the best rank not yet picked
+                   (ties to the lower rank); experts of other ranks are taken
+                   out of the selection below. */
+                if (max_ranks > 0 && max_ranks < R) {
+                    char* rank_taken = (char*)calloc((size_t)R, 1);
+                    for (int m = 0; m < max_ranks; ++m) {
+                        int best_r = -1;
+                        float best_s = 0.f;
+                        for (int r = 0; r < R; ++r) {
+                            if (rank_taken[r]) continue;
+                            float sr = key[r * per];
+                            for (int e = r * per + 1; e < (r + 1) * per; ++e)
+                                if (key[e] > sr) sr = key[e];
+                            if (best_r < 0 || sr > best_s) {
+                                best_r = r;
+                                best_s = sr;
+                            }
+                        }
+                        rank_taken[best_r] = 1;
+                    }
+                    for (int e = 0; e < E; ++e)
+                        if (!rank_taken[e / per]) taken[e] = 1;  /* not selectable */
+                    free(rank_taken);
                 }
                 /* k rounds: the largest key not yet taken; ascending scan and a
                    strict comparison give ties to the lower index. */

@@ -55,7 +55,7 @@ def _cfg(**kw):
 
 
 def test_struct_layout_matches_header():
-    assert ctypes.sizeof(moe.moe_config) == 14 * 4
+    assert ctypes.sizeof(moe.moe_config) == 15 * 4
     assert ctypes.sizeof(moe.moe_buffers) == 14 * 8
 
 
@@ -78,6 +78,9 @@ def test_struct_layout_matches_header():
     (dict(T=-1), moe.MOE_ERR_INVALID_ARG),
     (dict(T=1 << 28, k=4, E=8), moe.MOE_ERR_INVALID_ARG),  # T*k >= 2^30
     (dict(capacity=-1), moe.MOE_ERR_INVALID_ARG),
+    (dict(max_ranks=2), moe.MOE_OK),
+    (dict(max_ranks=5), moe.MOE_ERR_INVALID_ARG),                    # more than R
+    (dict(max_ranks=1, k=3), moe.MOE_ERR_INVALID_ARG),               # 1 rank x 2 experts < k
 ])
 def test_check_config(kw, status):
     assert moe.moe_check_config(_cfg(**kw)) == status
@@ -146,6 +149,13 @@ def test_invalid_calls_fail_before_any_launch():
     with pytest.raises(moe.MoeError) as e:
         moe.moe_read_device_status(None, stream=0)
     assert e.value.status == moe.MOE_ERR_INVALID_ARG
+
+
+def test_rank_limited_fp32_router_is_unsupported():
+    c = _cfg(max_ranks=2)   # fp32 router: the rank limit runs on the tensor-core router only
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_route(c, 0x1000, 0x2000, None, None, 0x3000, 0x4000, 0x6000, stream=0)
+    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
 
 
 def test_empty_batch_is_a_noop():

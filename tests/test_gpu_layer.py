@@ -67,6 +67,19 @@ def test_layer_small(name, T, resid):
         assert ref["n_dropped"] > 0
 
 
+def test_layer_rank_limited_deepseek():
+    """The DeepSeek-shaped layer with rank-limited routing (4 of 8 ranks)."""
+    w = W.WORKLOADS["deepseek"].replace(max_ranks=4)
+    inp = W.make_inputs(w, T=128)
+    layer, y = _run_layer(w, to_dev(inp), 128, True)
+    ref = oracle.layer_forward(
+        inp["x"], inp["w_router"], k=w.k, E=w.E, R=w.R, d_ff=w.d_ff, act=w.act, score=w.score,
+        renorm=w.renorm, sel_bias=inp["sel_bias"], w_up=inp["w_up"], w_down=inp["w_down"],
+        shared_up=inp["shared_up"], shared_down=inp["shared_down"], add_residual=True,
+        max_ranks=4)
+    _compare(w, layer, y, ref, torch.arange(128))
+
+
 @pytest.mark.parametrize("s", [0.0, 1.5])
 def test_layer_identity_sweep_small(s):
     w = W.sweep(4096, s)

@@ -138,3 +138,41 @@ def test_route_deterministic():
     a = run_route(cfg, inp)
     b = run_route(cfg, inp)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("E,R,M,k,score", [(8, 4, 2, 2, "softmax"), (16, 4, 1, 3, "sigmoid"),
+                                            (64, 8, 3, 6, "softmax"), (96, 8, 2, 8, "sigmoid"),
+                                            (256, 8, 4, 8, "sigmoid"), (256, 32, 5, 8, "softmax")])
+def test_route_rank_limited_ties(E, R, M, k, score):
+    """Rank-limited routing (at most M of R ranks per token) on a coarse grid
+    with many exact ties, bit for bit against the oracle."""
+    T, d = 300, 64
+    g = W._gen(E * 7 + M, "cpu")
+    x = W._grid_int((T, d), -8, 8, 8.0, g, "cpu").to(torch.bfloat16)
+    wr = W._grid_int((E, d), -1, 1, 512.0, g, "cpu").to(torch.bfloat16)
+    sel = W._grid_int((E,), -1, 1, 4096.0, g, "cpu") if score == "sigmoid" else None
+    w = W.Workload("rl", T, d, E, R, k, 64, "identity", "bf16", score, True, 0.0, 0, 0,
+                   "normal512", max_ranks=M)
+    cfg = cfg_for(w)
+    idx, gate = run_route(cfg, to_dev(dict(x=x, w_router=wr, logit_bias=None, sel_bias=sel)))
+    ridx, rgate = oracle.route(x, wr, k, score, True, None, sel, R=R, max_ranks=M)
+    assert torch.equal(idx, ridx), f"{int((idx != ridx).any(1).sum())} tokens differ"
+    assert_gates_close(gate, rgate, k)
+    per = E // R
+    assert all(len(set((idx[t] // per).tolist())) <= M for t in range(T))
+
+
+def test_route_rank_limited_deepseek_shape():
+    """DeepSeek-V3's limit (a token's experts on at most 4 of 8 ranks) on the
+    DeepSeek-shaped router, every token of a 2048-token batch."""
+    w = W.WORKLOADS["deepseek"].replace(max_ranks=4)
+    inp = W.make_inputs(w, ffn=False, T=2048)
+    cfg = cfg_for(w, T=2048)
+    idx, gate = run_route(cfg, to_dev(inp))
+    ridx, rgate = oracle.route(inp["x"], inp["w_router"], w.k, w.score, w.renorm, None,
+                               inp["sel_bias"], R=w.R, max_ranks=4)
+    assert torch.equal(idx, ridx)
+    assert_gates_close(gate, rgate, w.k)
+    free, _ = oracle.route(inp["x"], inp["w_router"], w.k, w.score, w.renorm, None,
+                           inp["sel_bias"])
+    assert not torch.equal(free, ridx)   # the limit actually binds on this workload

@@ -462,3 +462,51 @@ def test_balancing_reduces_load_imbalance():
         bias = oracle.update_sel_bias(c.int(), bias, T, k, gamma=2.0 ** -8)
     _, s1 = spread(bias)
     assert s1 < 1.25 and s1 < s0, (s0, s1)
+
+
+# --------------------------------------------------------------------------
+# Rank-limited routing (DeepSeek-V3: at most M devices per token)
+# --------------------------------------------------------------------------
+
+def _brute_rank_limited(key, k, R, M):
+    """Sort ranks by (-best key, rank), keep the first M, then sort the
+    surviving experts by (-key, expert): a different procedure from the
+    oracle's rounds of selection."""
+    T, E = key.shape
+    per = E // R
+    out = []
+    for t in range(T):
+        best = [max(float(key[t, e]) for e in range(r * per, (r + 1) * per)) for r in range(R)]
+        ranks = sorted(range(R), key=lambda r: (-best[r], r))[:M]
+        allowed = [e for e in range(E) if e // per in ranks]
+        out.append(sorted(allowed, key=lambda e: (-float(key[t, e]), e))[:k])
+    return torch.tensor(out, dtype=torch.int32)
+
+
+@pytest.mark.parametrize("E,R,M,k,score", [(8, 4, 2, 2, "softmax"), (16, 4, 1, 3, "sigmoid"),
+                                            (16, 8, 3, 4, "sigmoid"), (12, 3, 2, 5, "softmax"),
+                                            (8, 8, 2, 2, "sigmoid")])
+def test_rank_limited_routing_bruteforce(E, R, M, k, score):
+    x, w = _tiny_router(16, E, 4, seed=40 + E + R + M)
+    sel = (torch.tensor([((e * 7) % 3 - 1) / 4096.0 for e in range(E)], dtype=torch.float32)
+           if score == "sigmoid" else None)
+    idx, gate, L = oracle.route(x, w, k, score, True, None, sel, return_logits=True, R=R,
+                                max_ranks=M)
+    key = L if score == "softmax" else torch.sigmoid(L.double()).float() + (sel if sel is not None else 0)
+    assert torch.equal(idx, _brute_rank_limited(key, k, R, M))
+    per = E // R
+    assert all(len(set((idx[t] // per).tolist())) <= M for t in range(idx.shape[0]))
+
+
+def test_rank_limit_of_all_ranks_is_unlimited():
+    w, inp = _skewed_router(T=256)
+    a, ga = oracle.route(inp["x"], inp["w_router"], w.k, "sigmoid", True, None, inp["sel_bias"])
+    b, gb = oracle.route(inp["x"], inp["w_router"], w.k, "sigmoid", True, None, inp["sel_bias"],
+                         R=w.R, max_ranks=w.R)
+    assert torch.equal(a, b) and torch.equal(ga, gb)
+
+
+def test_rank_limit_rejects_too_few_experts():
+    x, w = _tiny_router(4, 8, 4, seed=1)
+    with pytest.raises(ValueError):
+        oracle.route(x, w, 5, "softmax", True, R=4, max_ranks=2)   # 2 ranks x 2 experts < 5
