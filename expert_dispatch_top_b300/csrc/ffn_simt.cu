@@ -3,8 +3,13 @@
 // Ultralytics glossary "Expert Parallelism", "How Tokens Move Between GPUs",
 // step 3: every expert processes the rows dispatched to it.  fp32 experts
 // cannot use the bf16 tensor-core path (and tf32 would miss a 1e-4 relative
-// accuracy budget), so they run as a tiled FFMA GEMM: 64 x 64 output tiles,
-// K in chunks of 16 through shared memory, 4 x 4 outputs per thread.
+// accuracy budget), so they run as a tiled FFMA GEMM:
+//   out[rows of group g, :] = epi( A[rows, :K] . B[g]^T )
+// 128 x 128 output tiles (SwiGLU: 128 x 64 gate columns and the matching 64
+// up columns), K in steps of 8 through double-buffered shared memory with the
+// next step's loads in registers, 8 x 8 outputs per thread split over rows
+// {4ty.., 64+4ty..} and columns {4tx.., 64+4tx..} so that every shared-memory
+// read is a conflict-free float4.
 //
 // Groups are ragged: group g owns rows [offsets[g], offsets[g+1]) of A and
 // out.  blockIdx.x enumerates (group, m-tile) pairs from the device-side
@@ -15,22 +20,20 @@
 namespace moe {
 namespace {
 
-constexpr int SBM = 64, SBN = 64, SBK = 16;
+constexpr int SBM = 128, SBN = 128, SBK = 8;
 
 __device__ __forceinline__ float gelu_f(float v) {
     return 0.5f * v * (1.f + erff(v * 0.70710678118654752440f));
 }
 __device__ __forceinline__ float silu_f(float v) { return v / (1.f + expf(-v)); }
 
-template <typename T, bool GATED>
+template <bool GATED>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a) {
-    __shared__ __align__(16) float As[SBK][SBM];
-    __shared__ __align__(16) float Bs[SBK][SBN];
-    __shared__ __align__(16) float Us[GATED ? SBK : 1][GATED ? SBN : 1];
+    __shared__ __align__(16) float As[2][SBK][SBM];
+    __shared__ __align__(16) float Bs[2][SBK][SBN];
     __shared__ int s_g, s_row0, s_rows;
     const int tid = threadIdx.x;
     if (tid == 0) {
-        // find (group, m-tile) of this block
         int rem = blockIdx.x, g = -1, row0 = 0, rows = 0;
         for (int q = 0; q < a.G; ++q) {
             const int lo = a.offsets ? a.offsets[q] : 0;
@@ -52,87 +55,131 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a) {
     const int g = s_g;
     if (g < 0) return;
     const int row0 = s_row0, rows = s_rows;
-    const int n0 = blockIdx.y * SBN;
     const int K = a.K, N = a.N;
+    // output columns of this block: SBN plain, or SBN/2 gate + SBN/2 up
+    const int ncol = GATED ? SBN / 2 : SBN;
+    const int n0 = blockIdx.y * ncol;
     const int b_rows = GATED ? 2 * N : N;
-    const T* A = static_cast<const T*>(a.A);
-    const T* B = static_cast<const T*>(a.B) + (int64_t)g * b_rows * K;
+    const float* A = static_cast<const float*>(a.A);
+    const float* B = static_cast<const float*>(a.B) + (int64_t)g * b_rows * K;
     const int tx = tid & 15, ty = tid >> 4;
 
-    float acc[4][4], accu[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = accu[i][j] = 0.f;
+    // global -> register loads: one float4 of A and one of B per thread per k-step
+    const int lr = tid >> 1;        // tile row 0..127
+    const int lk = (tid & 1) * 4;   // k offset 0 or 4
+    const bool a_ok = lr < rows;
+    const float* a_src = A + (int64_t)(row0 + (a_ok ? lr : 0)) * K + lk;
+    int brow;  // weight row feeding tile row lr
+    if (GATED)
+        brow = lr < 64 ? n0 + lr : N + n0 + (lr - 64);
+    else
+        brow = n0 + lr;
+    const bool b_ok = GATED ? ((lr < 64 ? n0 + lr : n0 + lr - 64) < N) : (brow < N);
+    const float* b_src = B + (int64_t)(b_ok ? brow : 0) * K + lk;
 
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    auto load = [&](int k0, float4& ra, float4& rb) {
+        const bool kin = k0 + lk < K;  // K % 4 == 0: a float4 is all in or all out
+        ra = (a_ok && kin) ? *reinterpret_cast<const float4*>(a_src + k0) : make_float4(0.f, 0.f, 0.f, 0.f);
+        rb = (b_ok && kin) ? *reinterpret_cast<const float4*>(b_src + k0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    auto store = [&](int buf, const float4& ra, const float4& rb) {
+        As[buf][lk + 0][lr] = ra.x;
+        As[buf][lk + 1][lr] = ra.y;
+        As[buf][lk + 2][lr] = ra.z;
+        As[buf][lk + 3][lr] = ra.w;
+        Bs[buf][lk + 0][lr] = rb.x;
+        Bs[buf][lk + 1][lr] = rb.y;
+        Bs[buf][lk + 2][lr] = rb.z;
+        Bs[buf][lk + 3][lr] = rb.w;
+    };
+
+    float4 ra, rb;
+    load(0, ra, rb);
+    store(0, ra, rb);
+    __syncthreads();
+    int buf = 0;
     for (int k0 = 0; k0 < K; k0 += SBK) {
-        // 64 x 16 tiles: 1024 elements each, one element per thread per pass
-        for (int i = tid; i < SBM * SBK; i += 256) {
-            const int r = i / SBK, kk = i % SBK;
-            const int gk = k0 + kk;
-            As[kk][r] = (r < rows && gk < K) ? Elem<T>::to_f(A[(int64_t)(row0 + r) * K + gk]) : 0.f;
-            const int n = n0 + r;
-            Bs[kk][r] = (n < N && gk < K) ? Elem<T>::to_f(B[(int64_t)n * K + gk]) : 0.f;
-            if (GATED)
-                Us[kk][r] = (n < N && gk < K) ? Elem<T>::to_f(B[(int64_t)(N + n) * K + gk]) : 0.f;
-        }
-        __syncthreads();
+        const bool more = k0 + SBK < K;
+        if (more) load(k0 + SBK, ra, rb);
 #pragma unroll
         for (int kk = 0; kk < SBK; ++kk) {
-            const float4 av = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
-            const float4 bv = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
-            const float ar[4] = {av.x, av.y, av.z, av.w};
-            const float br[4] = {bv.x, bv.y, bv.z, bv.w};
+            const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
+            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
+            const float ar[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float br[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
-            if (GATED) {
-                const float4 uv = *reinterpret_cast<const float4*>(&Us[kk][tx * 4]);
-                const float ur[4] = {uv.x, uv.y, uv.z, uv.w};
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
+        }
+        if (more) store(buf ^ 1, ra, rb);
+        __syncthreads();
+        buf ^= 1;
+    }
+    // epilogue: row r = {4ty + i, 64 + 4ty + i}; plain columns {4tx + j, 64 + 4tx + j};
+    // gated: gate column 4tx + j pairs with up column (tile column 64 + 4tx + j)
+    float* out = static_cast<float*>(a.out);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i) {
+        const int r = (i < 4) ? ty * 4 + i : 64 + ty * 4 + (i - 4);
+        if (r >= rows) continue;
+        float* orow = out + (int64_t)(row0 + r) * N;
+        if (GATED) {
+            const int n = n0 + tx * 4;
+            if (n < N) {
+                float4 o;
+                o.x = silu_f(acc[i][0]) * acc[i][4];
+                o.y = silu_f(acc[i][1]) * acc[i][5];
+                o.z = silu_f(acc[i][2]) * acc[i][6];
+                o.w = silu_f(acc[i][3]) * acc[i][7];
+                *reinterpret_cast<float4*>(orow + n) = o;
+            }
+        } else {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) accu[i][j] = fmaf(ar[i], ur[j], accu[i][j]);
+            for (int h = 0; h < 2; ++h) {
+                const int n = n0 + h * 64 + tx * 4;
+                if (n >= N) continue;
+                float4 o;
+                o.x = acc[i][4 * h + 0];
+                o.y = acc[i][4 * h + 1];
+                o.z = acc[i][4 * h + 2];
+                o.w = acc[i][4 * h + 3];
+                if (a.epi == EPI_GELU) {
+                    o.x = gelu_f(o.x);
+                    o.y = gelu_f(o.y);
+                    o.z = gelu_f(o.z);
+                    o.w = gelu_f(o.w);
+                }
+                *reinterpret_cast<float4*>(orow + n) = o;
             }
         }
-        __syncthreads();
     }
-    T* out = static_cast<T*>(a.out);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = ty * 4 + i;
-        if (r >= rows) continue;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int n = n0 + tx * 4 + j;
-            if (n >= N) continue;
-            float v = acc[i][j];
-            if (a.epi == EPI_GELU) v = gelu_f(v);
-            else if (GATED) v = silu_f(v) * accu[i][j];
-            out[(int64_t)(row0 + r) * N + n] = Elem<T>::from_f(v);
-        }
-    }
-}
-
-template <typename T>
-cudaError_t launch_simt_typed(const GemmArgs& a, cudaStream_t s) {
-    const int64_t rows_bound = a.offsets ? a.rows_cap : a.m_rows;
-    const int64_t mtiles = (rows_bound + SBM - 1) / SBM + a.G;
-    if (rows_bound == 0) return cudaSuccess;
-    dim3 grid((unsigned)mtiles, (unsigned)((a.N + SBN - 1) / SBN));
-    if (a.epi == EPI_SWIGLU)
-        gemm_simt_kernel<T, true><<<grid, 256, 0, s>>>(a);
-    else
-        gemm_simt_kernel<T, false><<<grid, 256, 0, s>>>(a);
-    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t s) {
-    if (a.dtype == MOE_DTYPE_F32) return launch_simt_typed<float>(a, s);
-    return launch_simt_typed<__nv_bfloat16>(a, s);
+    if (a.dtype != MOE_DTYPE_F32) return cudaErrorInvalidValue;  // bf16 runs on the tensor cores
+    if (a.K % 4 != 0 || a.N % 4 != 0) return cudaErrorInvalidValue;
+    const int64_t rows_bound = a.offsets ? a.rows_cap : a.m_rows;
+    if (rows_bound == 0) return cudaSuccess;
+    const int64_t mtiles = (rows_bound + SBM - 1) / SBM + a.G;
+    const bool gated = a.epi == EPI_SWIGLU;
+    const int ncol = gated ? SBN / 2 : SBN;
+    dim3 grid((unsigned)mtiles, (unsigned)((a.N + ncol - 1) / ncol));
+    if (gated)
+        gemm_simt_kernel<true><<<grid, 256, 0, s>>>(a);
+    else
+        gemm_simt_kernel<false><<<grid, 256, 0, s>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace moe
