@@ -92,6 +92,10 @@ def _load():
     lib.moe_combine.restype = i32
     lib.moe_layer_forward.argtypes = [cfgp] + [vp] * 8 + [ctypes.POINTER(moe_buffers), vp, vp, vp]
     lib.moe_layer_forward.restype = i32
+    lib.moe_combine_backward.argtypes = [cfgp] + [vp] * 7
+    lib.moe_combine_backward.restype = i32
+    lib.moe_dispatch_backward.argtypes = [cfgp] + [vp] * 4
+    lib.moe_dispatch_backward.restype = i32
     lib.moe_update_sel_bias.argtypes = [cfgp, vp, vp, ctypes.c_float, vp]
     lib.moe_update_sel_bias.restype = i32
     lib.moe_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
@@ -214,6 +218,19 @@ def moe_layer_forward(cfg, x, w_router, logit_bias, sel_bias, w_up, w_down, shar
                                      _p(sel_bias), _p(w_up), _p(w_down), _p(shared_up),
                                      _p(shared_down), ctypes.byref(buffers), _p(y), _p(ws),
                                      _stream(stream)), "moe_layer_forward")
+
+
+def moe_combine_backward(cfg, dy, yp, slot_row, topk_gate, d_yp, d_gate, stream=None):
+    """Reverse of the combine exchange: d_yp rows and gate gradients."""
+    _check(_load().moe_combine_backward(ctypes.byref(cfg), _p(dy), _p(yp), _p(slot_row),
+                                        _p(topk_gate), _p(d_yp), _p(d_gate), _stream(stream)),
+           "moe_combine_backward")
+
+
+def moe_dispatch_backward(cfg, d_xp, slot_row, dx, stream=None):
+    """Reverse of the dispatch exchange: dx[t] = sum of its kept rows' gradients."""
+    _check(_load().moe_dispatch_backward(ctypes.byref(cfg), _p(d_xp), _p(slot_row), _p(dx),
+                                         _stream(stream)), "moe_dispatch_backward")
 
 
 def moe_update_sel_bias(cfg, expert_counts, sel_bias, gamma, stream=None):

@@ -386,6 +386,51 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w
     return combine_impl(cfg, yp, slot_row, gate, buf->shared_out, x, y, s);
 }
 
+moe_status moe_combine_backward(const moe_config* cfg, const void* dy, const void* yp,
+                                const int32_t* slot_row, const float* topk_gate, void* d_yp,
+                                float* d_gate, moe_stream_t stream) {
+    moe_status st = moe_check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (cfg->T == 0) return MOE_OK;
+    if (!dy || !yp || !slot_row || !topk_gate || !d_yp || !d_gate) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dy) || !aligned16(yp) || !aligned16(d_yp) || !aligned4(slot_row) ||
+        !aligned4(topk_gate) || !aligned4(d_gate))
+        return MOE_ERR_INVALID_ARG;
+    CombineBwdArgs a;
+    a.dy = dy;
+    a.yp = yp;
+    a.slot_row = slot_row;
+    a.gate = topk_gate;
+    a.d_yp = d_yp;
+    a.d_gate = d_gate;
+    a.T = cfg->T;
+    a.d = cfg->d;
+    a.k = cfg->k;
+    a.dtype = cfg->act_dtype;
+    return cuda_status(launch_combine_backward(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dispatch_backward(const moe_config* cfg, const void* d_xp, const int32_t* slot_row,
+                                 void* dx, moe_stream_t stream) {
+    moe_status st = moe_check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (cfg->T == 0) return MOE_OK;
+    if (!d_xp || !slot_row || !dx || !aligned16(d_xp) || !aligned16(dx) || !aligned4(slot_row))
+        return MOE_ERR_INVALID_ARG;
+    CombineArgs a;
+    a.yp = d_xp;
+    a.slot_row = slot_row;
+    a.gate = nullptr;  // the plain sum of the token's kept rows
+    a.shared = nullptr;
+    a.resid = nullptr;
+    a.y = dx;
+    a.T = cfg->T;
+    a.d = cfg->d;
+    a.k = cfg->k;
+    a.dtype = cfg->act_dtype;
+    return cuda_status(launch_combine(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_update_sel_bias(const moe_config* cfg, const int32_t* expert_counts, float* sel_bias,
                                float gamma, moe_stream_t stream) {
     moe_status st = moe_check_config(cfg);

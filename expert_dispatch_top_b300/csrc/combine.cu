@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
         float g_l = 0.f;
         if (lane < a.k) {
             r_l = a.slot_row[t * a.k + lane];
-            g_l = a.gate[t * a.k + lane];
+            g_l = a.gate ? a.gate[t * a.k + lane] : 1.f;  // no gates: the plain sum of rows
         }
         int r[KMAX];
         float g[KMAX];
@@ -99,7 +99,96 @@ void launch_combine_typed(const CombineArgs& a, unsigned blocks, cudaStream_t s)
         combine_kernel<T, 8, 1><<<blocks, 256, 0, s>>>(a);
 }
 
+// Backward of combine, one warp per token: for every kept slot j,
+// d_yp[slot_row[t,j]] = g[t,j] * dy[t] (one rounding) and
+// d_gate[t,j] = <dy[t], yp[slot_row[t,j]]> (fp32, lane partials then a
+// butterfly); dropped slots get d_gate = 0.
+template <typename T, int KMAX>
+__global__ void __launch_bounds__(256) combine_bwd_kernel(CombineBwdArgs a) {
+    constexpr int V = Elem<T>::kPerVec;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int nvec = a.d / V;
+    const int64_t row_bytes = (int64_t)a.d * sizeof(T);
+    const char* dy = static_cast<const char*>(a.dy);
+    const char* yp = static_cast<const char*>(a.yp);
+    char* dyp = static_cast<char*>(a.d_yp);
+    for (int64_t t = warp0; t < a.T; t += nwarps) {
+        int r_l = -1;
+        float g_l = 0.f;
+        if (lane < a.k) {
+            r_l = a.slot_row[t * a.k + lane];
+            g_l = a.gate[t * a.k + lane];
+        }
+        int r[KMAX];
+        float g[KMAX], dot[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            r[j] = __shfl_sync(0xffffffffu, r_l, j);
+            g[j] = __shfl_sync(0xffffffffu, g_l, j);
+            if (j >= a.k) r[j] = -1;
+            dot[j] = 0.f;
+        }
+        for (int c = lane; c < nvec; c += 32) {
+            float f[V];
+            Elem<T>::unpack(ld_nc_v4(dy + t * row_bytes + (int64_t)c * 16), f);
+            uint4 v[KMAX];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (r[j] >= 0) v[j] = ld_nc_v4(yp + (int64_t)r[j] * row_bytes + (int64_t)c * 16);
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (r[j] >= 0) {
+                    float y[V], o[V];
+                    Elem<T>::unpack(v[j], y);
+#pragma unroll
+                    for (int q = 0; q < V; ++q) {
+                        dot[j] = fmaf(f[q], y[q], dot[j]);
+                        o[q] = g[j] * f[q];
+                    }
+                    st_v4(dyp + (int64_t)r[j] * row_bytes + (int64_t)c * 16, Elem<T>::pack(o));
+                }
+        }
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dot[j] += __shfl_xor_sync(0xffffffffu, dot[j], o);
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (j < a.k) a.d_gate[t * a.k + j] = r[j] >= 0 ? dot[j] : 0.f;
+        }
+    }
+}
+
+template <typename T>
+void launch_combine_bwd_typed(const CombineBwdArgs& a, unsigned blocks, cudaStream_t s) {
+    if (a.k <= 2)
+        combine_bwd_kernel<T, 2><<<blocks, 256, 0, s>>>(a);
+    else if (a.k <= 4)
+        combine_bwd_kernel<T, 4><<<blocks, 256, 0, s>>>(a);
+    else
+        combine_bwd_kernel<T, 8><<<blocks, 256, 0, s>>>(a);
+}
+
 }  // namespace
+
+cudaError_t launch_combine_backward(const CombineBwdArgs& a, cudaStream_t s) {
+    if (a.T == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int64_t blocks = (a.T + 7) / 8;
+    const int64_t cap = (int64_t)sms * 16;
+    if (blocks > cap) blocks = cap;
+    if (a.dtype == MOE_DTYPE_F32)
+        launch_combine_bwd_typed<float>(a, (unsigned)blocks, s);
+    else
+        launch_combine_bwd_typed<__nv_bfloat16>(a, (unsigned)blocks, s);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
     if (a.T == 0) return cudaSuccess;

@@ -59,7 +59,19 @@ struct CombineArgs {
     int64_t T;
     int d, k, dtype;
 };
-cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);  // gate == null: unit gates
+
+struct CombineBwdArgs {
+    const void* dy;
+    const void* yp;
+    const int32_t* slot_row;
+    const float* gate;
+    void* d_yp;
+    float* d_gate;
+    int64_t T;
+    int d, k, dtype;
+};
+cudaError_t launch_combine_backward(const CombineBwdArgs& a, cudaStream_t s);
 
 // Epilogue of one grouped GEMM: out = epi(A . B^T).
 enum Epilogue { EPI_NONE = 0, EPI_GELU = 1, EPI_SWIGLU = 2 };

@@ -236,6 +236,28 @@ moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slo
                        void* y, moe_stream_t stream);
 
 /*
+ * Backward of Step 4 (the reverse of the combine exchange).  Combine is
+ * linear in the expert outputs and in the gates, so for dy = dL/dy [T,d]:
+ *   d_yp[slot_row[t,j]] = topk_gate[t,j] * dy[t] for every kept slot (one
+ *     rounding to the act dtype; rows no slot points to are left untouched);
+ *   d_gate[t,j] = sum_c dy[t,c] * yp[slot_row[t,j], c] (fp32), 0 if dropped.
+ * The residual and shared-expert terms pass dy through unchanged (no call
+ * needed).  dy [T,d], yp [max_rows,d], d_yp [max_rows,d]; d_gate [T,k] fp32.
+ */
+moe_status moe_combine_backward(const moe_config* cfg, const void* dy, const void* yp,
+                                const int32_t* slot_row, const float* topk_gate, void* d_yp,
+                                float* d_gate, moe_stream_t stream);
+
+/*
+ * Backward of Step 2 (the reverse of the dispatch exchange): every kept row
+ * of xp is a copy of its token, so dx[t] = sum over kept j of
+ * d_xp[slot_row[t,j]] (fp32 accumulation in slot order, one rounding; 0 for a
+ * fully dropped token).  d_xp [max_rows,d], dx [T,d] (act dtype).
+ */
+moe_status moe_dispatch_backward(const moe_config* cfg, const void* d_xp, const int32_t* slot_row,
+                                 void* dx, moe_stream_t stream);
+
+/*
  * Buffers of moe_layer_forward.  xp, yp, h (and shared_h, shared_out when
  * n_shared == 1) are required.  Any metadata pointer may be NULL; the
  * library then keeps that array in the workspace.  For IDENTITY experts,

@@ -76,6 +76,10 @@ def _load():
         lib.oracle_combine.restype = None
         lib.oracle_update_sel_bias.argtypes = [i64, i32, i32, vp, vp, ctypes.c_float]
         lib.oracle_update_sel_bias.restype = None
+        lib.oracle_combine_backward.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        lib.oracle_combine_backward.restype = None
+        lib.oracle_dispatch_backward.argtypes = [i64, i32, i32, i32, vp, vp, vp]
+        lib.oracle_dispatch_backward.restype = None
         _lib = lib
     return _lib
 
@@ -214,6 +218,33 @@ def update_sel_bias(expert_counts, sel_bias, T, k, gamma):
     _load().oracle_update_sel_bias(int(T), int(k), counts.numel(), _ptr(counts), _ptr(out),
                                    ctypes.c_float(gamma))
     return out
+
+
+def combine_backward(dy, yp, slot_row, topk_gate):
+    """Backward of combine: (d_yp fp64 [rows,d] (zero where no slot points),
+    d_gate fp64 [T,k])."""
+    dy = _cpu(dy)
+    yp = _cpu(yp, dy.dtype)
+    sr = _cpu(slot_row, torch.int32)
+    g = _cpu(topk_gate, torch.float32)
+    T, d = dy.shape
+    k = sr.shape[1]
+    d_yp = torch.zeros((max(yp.shape[0], 1), d), dtype=torch.float64)
+    d_gate = torch.zeros((T, k), dtype=torch.float64)
+    _load().oracle_combine_backward(T, d, k, _dtype_code(dy), _ptr(dy), _ptr(yp), _ptr(sr), _ptr(g),
+                                    _ptr(d_yp), _ptr(d_gate))
+    return d_yp[: yp.shape[0]], d_gate
+
+
+def dispatch_backward(d_xp, slot_row, T):
+    """Backward of dispatch: dx fp64 [T,d] = sum of the kept rows' gradients."""
+    d_xp = _cpu(d_xp)
+    sr = _cpu(slot_row, torch.int32)
+    d = d_xp.shape[1]
+    dx = torch.empty((T, d), dtype=torch.float64)
+    _load().oracle_dispatch_backward(T, d, sr.shape[1], _dtype_code(d_xp), _ptr(d_xp), _ptr(sr),
+                                     _ptr(dx))
+    return dx
 
 
 def layer_forward(x, w_router, *, k, E, R, d_ff, act, score="softmax", renorm=True,

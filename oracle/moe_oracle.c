@@ -408,3 +408,48 @@ void oracle_update_sel_bias(int64_t T, int k, int E, const int32_t* counts, floa
         else if (load < even) bias[e] = bias[e] + gamma;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Backward of the two exchanges (training is the pages' main setting:        */
+/* topicspectrum "Training teaches both experts and router").                 */
+/* Combine is y[t] = sum_j g[t,j] * yp[slot_row[t,j]] over kept slots, linear */
+/* in yp and in g, so with dy = dL/dy:                                         */
+/*   d_yp[slot_row[t,j]] = g[t,j] * dy[t]       (the reverse exchange),        */
+/*   d_gate[t,j]         = sum_c dy[t,c] * yp[slot_row[t,j], c],               */
+/* and 0 for dropped slots.  Dispatch is xp[slot_row[t,j]] = x[t], so          */
+/*   dx[t] = sum over kept j of d_xp[slot_row[t,j]].                          */
+/* ------------------------------------------------------------------------ */
+void oracle_combine_backward(int64_t T, int d, int k, int dtype, const void* dy, const void* yp,
+                             const int32_t* slot_row, const float* gate, double* d_yp,
+                             double* d_gate) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            const int32_t row = slot_row[t * k + j];
+            if (row < 0) {
+                d_gate[t * k + j] = 0.0;
+                continue;
+            }
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c) {
+                const double g = elem(dy, dtype, t * d + c);
+                dot += g * elem(yp, dtype, (int64_t)row * d + c);
+                d_yp[(int64_t)row * d + c] = (double)gate[t * k + j] * g;
+            }
+            d_gate[t * k + j] = dot;
+        }
+}
+
+void oracle_dispatch_backward(int64_t T, int d, int k, int dtype, const void* d_xp,
+                              const int32_t* slot_row, double* dx) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j) {
+                const int32_t row = slot_row[t * k + j];
+                if (row >= 0) acc += elem(d_xp, dtype, (int64_t)row * d + c);
+            }
+            dx[t * d + c] = acc;
+        }
+}

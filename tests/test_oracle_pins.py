@@ -510,3 +510,52 @@ def test_rank_limit_rejects_too_few_experts():
     x, w = _tiny_router(4, 8, 4, seed=1)
     with pytest.raises(ValueError):
         oracle.route(x, w, 5, "softmax", True, R=4, max_ranks=2)   # 2 ranks x 2 experts < 5
+
+
+# --------------------------------------------------------------------------
+# Backward of the exchanges: adjoint identities and library autograd
+# --------------------------------------------------------------------------
+
+def _exchange_case(T=40, E=8, k=3, d=16, cap=9, seed=12):
+    idx = W.random_topk(T, E, k, seed=seed, skew=1.2)
+    disp = oracle.dispatch(idx, E, 2, cap)
+    g = torch.Generator().manual_seed(seed)
+    yp = torch.randn((disp["rows"], d), generator=g, dtype=torch.float64).float()
+    dy = torch.randn((T, d), generator=g, dtype=torch.float64).float()
+    gate = torch.rand((T, k), generator=g)
+    return disp, yp, dy, gate
+
+
+def test_combine_backward_is_the_adjoint_and_matches_autograd():
+    disp, yp, dy, gate = _exchange_case()
+    d_yp, d_gate = oracle.combine_backward(dy, yp, disp["slot_row"], gate)
+    T = dy.shape[0]
+    rows = torch.arange(disp["rows"], dtype=torch.int32)
+    y = oracle.combine(torch.arange(T), yp, rows, disp["slot_row"], gate)
+    # <combine(yp), dy> = <yp, d_yp>: the reverse exchange is the adjoint
+    assert abs(float((y * dy.double()).sum()) - float((yp.double() * d_yp).sum())) < 1e-9
+    # library autograd of the same sum (fp64)
+    ypd = yp.double().clone().requires_grad_(True)
+    gd = gate.double().clone().requires_grad_(True)
+    sr = disp["slot_row"].long()
+    kept = sr >= 0
+    rows_used = ypd[sr.clamp(min=0)] * kept.unsqueeze(-1)          # [T,k,d]
+    out = (gd.unsqueeze(-1) * rows_used).sum(1)
+    (out * dy.double()).sum().backward()
+    assert torch.allclose(d_yp, ypd.grad, rtol=1e-12, atol=1e-12)
+    assert torch.allclose(d_gate, gd.grad * kept, rtol=1e-12, atol=1e-12)
+    assert torch.all(d_gate[~kept] == 0)
+
+
+def test_dispatch_backward_is_the_adjoint_of_permute():
+    disp, yp, dy, gate = _exchange_case(T=33, k=2, cap=5)
+    T, d = 33, 16
+    x = torch.randn((T, d), generator=torch.Generator().manual_seed(3)).float()
+    xp = oracle.permute(x, disp["slot_row"], disp["rows"])
+    d_xp = torch.randn(xp.shape, generator=torch.Generator().manual_seed(4)).float()
+    dx = oracle.dispatch_backward(d_xp, disp["slot_row"], T)
+    assert abs(float((xp.double() * d_xp.double()).sum()) - float((x.double() * dx).sum())) < 1e-9
+    # library autograd of a gather
+    xd = x.double().clone().requires_grad_(True)
+    (xd[disp["row_token"].long()] * d_xp.double()).sum().backward()
+    assert torch.allclose(dx, xd.grad, rtol=1e-12, atol=1e-12)
