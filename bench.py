@@ -46,7 +46,12 @@ UNIT = "tokens/s"
 # an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the
 # hash of ffn_tc.cu at capture time: reported only while the kernel source is
 # unchanged.  See profiles/ for the commands.
-TRAFFIC = {}
+TRAFFIC = {
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the full
+    # Mixtral-shaped step: up 2.19 GB read + 0.93 GB written, down 5.20 GB + 0.27 GB.
+    "mixtral": {"bytes": 2.19e9 + 0.92879e9 + 5.20e9 + 0.26515e9, "src_hash": "2ba60a5928c7afed",
+                "per": "step (up + down launches)"},
+}
 
 
 def _src_hash(path):
@@ -455,7 +460,7 @@ def run_ours(args, w):
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded dyadic grid; no dataset)",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "R": w.R,
-                   "d_ff": w.d_ff, "act": w.act, "score": w.score,
+                   "d_ff": w.d_ff, "act": w.act, "score": w.score, "max_ranks": w.max_ranks,
                    "capacity_factor": w.capacity_factor, "n_shared": w.n_shared,
                    "kept_rows": n_kept, "parallelism": f"replicas x{world}" if world > 1 else "none",
                    "l2": "inputs larger than L2 (x and expert weights); no flush"},
@@ -480,6 +485,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="mixtral")
     ap.add_argument("--tokens", type=int, default=0, help="override T (small profiling cases)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override E (small profiling cases with the same rows per expert)")
+    ap.add_argument("--max-ranks", type=int, default=-1, help="rank-limited routing (0: off)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-route-tokens", type=int, default=256)
@@ -489,6 +497,10 @@ def main():
     w = W.get(args.workload)
     if args.tokens:
         w = w.replace(T=args.tokens)
+    if args.experts:
+        w = w.replace(E=args.experts)
+    if args.max_ranks >= 0:
+        w = w.replace(max_ranks=args.max_ranks)
     if args.impl == "reference":
         run_reference(args, w)
     else:
