@@ -84,6 +84,9 @@ def _load():
     lib.moe_route.restype = i32
     lib.moe_dispatch.argtypes = [cfgp] + [vp] * 12
     lib.moe_dispatch.restype = i32
+    lib.moe_test_dispatch_stall.argtypes = [cfgp] + [vp] * 10 + [ctypes.c_int32, ctypes.c_uint32,
+                                                                  vp, vp]
+    lib.moe_test_dispatch_stall.restype = i32
     lib.moe_dispatch_noalloc.argtypes = [cfgp] + [vp] * 12
     lib.moe_dispatch_noalloc.restype = i32
     lib.moe_expert_ffn.argtypes = [cfgp] + [vp] * 13
@@ -185,6 +188,18 @@ def moe_dispatch(cfg, x, topk_idx, xp, row_token, slot_row, expert_counts, exper
                                 _p(slot_row), _p(expert_counts), _p(expert_offsets),
                                 _p(rank_counts), _p(rank_splits), _p(n_dropped), _p(ws),
                                 _stream(stream)), "moe_dispatch")
+
+
+def moe_test_dispatch_stall(cfg, x, topk_idx, xp, row_token, slot_row, expert_counts,
+                            expert_offsets, rank_counts, rank_splits, n_dropped, stall_block,
+                            wait_limit_us, ws, stream=None):
+    """Failure-detection hook: dispatch with one look-back block that never
+    publishes; the bounded wait runs out and sets MOE_DEV_LOOKBACK_TIMEOUT."""
+    _check(_load().moe_test_dispatch_stall(ctypes.byref(cfg), _p(x), _p(topk_idx), _p(xp),
+                                           _p(row_token), _p(slot_row), _p(expert_counts),
+                                           _p(expert_offsets), _p(rank_counts), _p(rank_splits),
+                                           _p(n_dropped), int(stall_block), int(wait_limit_us),
+                                           _p(ws), _stream(stream)), "moe_test_dispatch_stall")
 
 
 def moe_dispatch_noalloc(cfg, x, topk_idx, xp, row_token, slot_row, expert_counts, expert_offsets,

@@ -126,7 +126,8 @@ moe_status route_impl(const moe_config* c, const void* x, const void* w, const f
 moe_status dispatch_impl(const moe_config* c, const void* x, const int32_t* idx, void* xp,
                          int32_t* row_token, int32_t* slot_row, int32_t* counts, int32_t* offsets,
                          int32_t* rank_counts, int32_t* rank_splits, int32_t* n_dropped, void* ws,
-                         cudaStream_t s) {
+                         cudaStream_t s, int stall_block = -1,
+                         uint64_t wait_ns = kWaitTimeoutNs) {
     if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
     if (!counts || !offsets || !rank_counts || !n_dropped) return MOE_ERR_INVALID_ARG;
     if (c->T > 0 && (!x || !idx || !xp || !row_token || !slot_row)) return MOE_ERR_INVALID_ARG;
@@ -161,6 +162,8 @@ moe_status dispatch_impl(const moe_config* c, const void* x, const int32_t* idx,
     a.R = c->R;
     a.dtype = c->act_dtype;
     a.C = capacity_of(c);
+    a.stall_block = stall_block;
+    a.wait_ns = wait_ns;
     return cuda_status(launch_dispatch(a, s));
 }
 
@@ -326,6 +329,21 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
     return dispatch_impl(cfg, x, topk_idx, xp, row_token, slot_row, expert_counts, expert_offsets,
                          rank_counts, rank_splits, n_dropped, ws,
                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_test_dispatch_stall(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                                   void* xp, int32_t* row_token, int32_t* slot_row,
+                                   int32_t* expert_counts, int32_t* expert_offsets,
+                                   int32_t* rank_counts, int32_t* rank_splits, int32_t* n_dropped,
+                                   int32_t stall_block, uint32_t wait_limit_us, void* ws,
+                                   moe_stream_t stream) {
+    moe_status st = moe_check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (stall_block < 0 || wait_limit_us == 0 || wait_limit_us > 4000000u) return MOE_ERR_INVALID_ARG;
+    return dispatch_impl(cfg, x, topk_idx, xp, row_token, slot_row, expert_counts, expert_offsets,
+                         rank_counts, rank_splits, n_dropped, ws,
+                         reinterpret_cast<cudaStream_t>(stream), stall_block,
+                         (uint64_t)wait_limit_us * 1000ull);
 }
 
 moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* expert_offsets,

@@ -171,12 +171,13 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
             wpre[sb][e] = own;
             own += __popc(bits[sb][e]);
         }
+        const bool publish = (int)blk != a.stall_block;
         if (blk == 0) {
-            st_relaxed_u64(desc + e, kFlagIncl | (uint32_t)own);
+            if (publish) st_relaxed_u64(desc + e, kFlagIncl | (uint32_t)own);
             prefix[e] = 0;
             continue;
         }
-        st_relaxed_u64(desc + e, kFlagAgg | (uint32_t)own);
+        if (publish) st_relaxed_u64(desc + e, kFlagAgg | (uint32_t)own);
         int excl = 0;
         int64_t j = (int64_t)blk - 1;
         uint64_t t_start = 0;
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
             const uint64_t flag = v & (3ull << 32);
             if (flag == 0) {
                 if (t_start == 0) t_start = globaltimer_ns();
-                else if (globaltimer_ns() - t_start > kWaitTimeoutNs) {
+                else if (globaltimer_ns() - t_start > a.wait_ns) {
                     atomicOr(a.status, MOE_DEV_LOOKBACK_TIMEOUT);
                     break;
                 }
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
             t_start = 0;
         }
         prefix[e] = excl;
-        st_relaxed_u64(desc + e, kFlagIncl | (uint32_t)(excl + own));
+        if (publish) st_relaxed_u64(desc + e, kFlagIncl | (uint32_t)(excl + own));
     }
     __syncthreads();
     // Positions, keep/drop, rows.

@@ -126,5 +126,7 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x,
     a.R = cfg->R;
     a.dtype = cfg->act_dtype;
     a.C = moe_capacity(cfg);
+    a.stall_block = -1;
+    a.wait_ns = kWaitTimeoutNs;
     return launch_dispatch(a, strm) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -44,6 +44,8 @@ struct DispatchArgs {
     int64_t T;
     int d, E, k, R, dtype;
     int64_t C;           // < 0: no limit
+    int stall_block;     // test hook: this block never publishes its look-back state (-1: none)
+    uint64_t wait_ns;    // bound on each look-back wait
 };
 // Header bytes of the workspace that dispatch clears before it runs.
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);

@@ -174,6 +174,22 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
                         int32_t* n_dropped, void* ws, moe_stream_t stream);
 
 /*
+ * Failure-detection test hook (no counterpart on the pages): moe_dispatch with
+ * one scan block that never publishes its look-back state (stall_block >= 0,
+ * in ticket order) and a bound of wait_limit_us (1..4,000,000) on every
+ * look-back wait.  The block after it waits, gives up at the bound, sets
+ * MOE_DEV_LOOKBACK_TIMEOUT in the status word and carries on, so every kernel
+ * returns and the context stays usable; the dispatch outputs are then
+ * meaningless.  moe_dispatch itself uses a 4 s bound and never stalls.
+ */
+moe_status moe_test_dispatch_stall(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                                   void* xp, int32_t* row_token, int32_t* slot_row,
+                                   int32_t* expert_counts, int32_t* expert_offsets,
+                                   int32_t* rank_counts, int32_t* rank_splits, int32_t* n_dropped,
+                                   int32_t stall_block, uint32_t wait_limit_us, void* ws,
+                                   moe_stream_t stream);
+
+/*
  * moe_dispatch without a workspace, for callers that cannot allocate device
  * memory (a plugin handed only its input and output pointers; a serving loop
  * whose memory was all reserved by another allocator).  The pages have no
