@@ -72,6 +72,9 @@ def _run_ffn(counts, d, f, act, dtype, seed, rows_cap=None, shared=False):
     ([0, 1, 127, 128, 129, 300, 0, 513], 256, 384),
     ([40, 0, 0, 250], 512, 1024),
     ([700, 3], 1024, 256),
+    ([1500, 1100], 256, 256),
+    ([2000, 0, 1], 128, 384),
+    ([17, 33, 250, 5, 300, 1], 512, 512),
 ])
 def test_ffn_bf16_tensor_cores(act, counts, d, f):
     _run_ffn(counts, d, f, act, torch.bfloat16, seed=sum(counts) + d + f)
