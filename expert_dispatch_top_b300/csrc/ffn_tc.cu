@@ -68,8 +68,16 @@ struct TcParams {
     uint32_t* status;
 };
 
+// GELU in its tanh form with the hardware tanh: 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))).
+// It differs from the erf form by less than 5e-4 |v| (the form's own error plus
+// the 2^-11 relative error of tanh.approx), below the bf16 rounding of h
+// (2^-9 relative), and costs a handful of instructions instead of erff.
 __device__ __forceinline__ float gelu_f(float v) {
-    return 0.5f * v * (1.f + erff(v * 0.70710678118654752440f));
+    float t;
+    const float u = 0.7978845608028654f * fmaf(0.044715f * v, v * v, v);
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(u));
+    const float hv = 0.5f * v;
+    return fmaf(hv, t, hv);
 }
 __device__ __forceinline__ float silu_f(float v) { return v / (1.f + __expf(-v)); }
 
