@@ -131,6 +131,20 @@ class ClockSampler:
                 "samples": len(loaded), "power_w_max": max(r[2] for r in rows)}
 
 
+def replica_throughput(local_ms, tokens_per_rank, world, device="cpu"):
+    """Replicas-only scaling: every rank runs the whole layer on its own tokens.
+    The job's time is the slowest rank's (all_reduce MAX) and its throughput
+    counts every rank's tokens.  Returns (max_ms, tokens/s)."""
+    import torch
+    import torch.distributed as dist
+    ms = float(local_ms)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * tokens_per_rank / (ms / 1e3)
+
+
 def layer_work(w, n_kept):
     """Algorithmic work of one layer step (counted once, nothing dense over E)."""
     b = 4 if w.dtype == "f32" else 2
@@ -282,11 +296,7 @@ def run_ours(args, w):
             dist.barrier()
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return replica_throughput(v, w.T, world, dev)[0]
 
     for _ in range(max(args.warmup, 1)):
         layer(x)
