@@ -10,14 +10,16 @@
 // grid: multiples of 2^-12 below 2^10) the accumulation is exact too, so the
 // logits -- and every routing decision -- equal the FFMA kernels' bit for bit.
 //
-// Persistent kernel, one CTA per SM (192 threads, ~192 KB of shared memory so
-// that exactly one CTA holds the SM's 512 TMEM columns):
+// Persistent kernel, one CTA per SM (192 or 320 threads, ~200 KB of shared
+// memory so that exactly one CTA holds the SM's 512 TMEM columns):
 //   warp 0     TMA: a 128-token x 64 tile of x and the E x 64 tile of Wr
 //              (rows past E zero-filled) per stage;
 //   warp 1     TMEM allocation; one lane issues tcgen05.mma (M=128, N=Np,
 //              Np = E rounded up to a multiple of 16, at least 16) into one of
 //              two accumulators;
-//   warps 2-5  epilogue: each thread owns one token (one TMEM lane), reads
+//   warps 2-5  epilogue (and warps 6-9 when CTAs have several tiles: the two
+//              groups take alternate tiles, one TMEM buffer each, so two
+//              tiles' epilogues overlap): each thread owns one token (one TMEM lane), reads
 //              its E logits 32 at a time and keeps a sorted top-k in registers
 //              (ties to the lower expert index), then computes the gates and
 //              writes topk_idx / topk_gate.
@@ -50,7 +52,7 @@ constexpr int RM = 128, RK = 64;
 // rows of 32 rank scores; odd pitches keep the per-thread rows conflict-free.
 constexpr int STASH_PITCH = 33;
 constexpr int STASH_PITCH_RANKS = 97;
-constexpr int R_THREADS = 192;
+constexpr int R_THREADS_MAX = 64 + 2 * 128;  // producer, MMA, up to two epilogue warp groups
 constexpr int R_MAX_STAGES = 8;
 constexpr uint32_t R_TMEM_COLS = 512;
 constexpr int R_SMEM_TILES = 196608;  // bytes of stage ring
@@ -63,6 +65,7 @@ struct RtParams {
     int d, E, Np, k, score, renorm;
     int R, max_ranks;   // rank-limited routing when max_ranks > 0
     int stash_pitch;    // floats of shared memory per epilogue thread
+    int epi_groups;     // epilogue warp groups (1 or 2); group g owns TMEM buffer g when 2
     const float* logit_bias;
     const float* sel_bias;
     int32_t* idx;
@@ -146,7 +149,7 @@ __device__ __forceinline__ uint32_t pick_ranks(const float* sc, int R, int m, fl
 // tiles; on inputs whose sums are exact in fp32 this changes nothing.)
 __device__ __forceinline__ int k_start(int tile, int num_kb) { return (int)(((unsigned)tile * 37u) % (unsigned)num_kb); }
 
-__global__ void __launch_bounds__(R_THREADS, 1)
+__global__ void __launch_bounds__(R_THREADS_MAX, 1)
     route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     const RtParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -185,7 +188,7 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), R_TMEM_COLS);
     if (warp >= 2) {
-        for (int e = threadIdx.x - 64; e < 256; e += 128) {
+        for (int e = threadIdx.x - 64; e < 256; e += (int)blockDim.x - 64) {
             lb_s[e] = (p.logit_bias && e < p.E) ? p.logit_bias[e] : 0.f;
             sb_s[e] = (p.sel_bias && e < p.E) ? p.sel_bias[e] : 0.f;
         }
@@ -269,7 +272,10 @@ __global__ void __launch_bounds__(R_THREADS, 1)
         }
     } else {
         // ---------------- epilogue: one token per thread ----------------
+        // With two warp groups, group g takes this CTA's tiles i with i % 2 == g
+        // (they land in TMEM buffer g), so two tiles' epilogues run at once.
         const int q = warp & 3;
+        const int egroup = (warp - 2) >> 2;
         const int nchunks = (p.E + 31) / 32;
         const bool sigmoid = p.score == MOE_SCORE_SIGMOID;
         const bool has_lb = p.logit_bias != nullptr;
@@ -280,9 +286,12 @@ __global__ void __launch_bounds__(R_THREADS, 1)
         const bool limited = p.max_ranks > 0;
         const int per = p.E / p.R;
         const float inv_per = 1.0f / (float)per;  // (e + 1/2) * inv_per truncates to e / per exactly
-        int acc = 0;
-        uint32_t acc_phase = 0;
+        int local = -1;
         for (int tile = blockIdx.x; tile < p.m_tiles; tile += gridDim.x) {
+            ++local;
+            if (local % p.epi_groups != egroup) continue;
+            const int acc = local & 1;                       // the MMA alternates buffers per tile
+            const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;  // n-th use of that buffer
             const bool ok =
                 __all_sync(0xffffffffu, mbar_wait(accf0 + 8 * acc, acc_phase, abort_flag, p.status,
                                                   MOE_DEV_GEMM_TIMEOUT));
@@ -451,8 +460,6 @@ __global__ void __launch_bounds__(R_THREADS, 1)
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce0 + 8 * acc);
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1;
             if (t < p.T) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
@@ -503,7 +510,13 @@ cudaError_t launch_route_tc(const RouteArgs& a, cudaStream_t s) {
     p.R = a.R > 0 ? a.R : 1;
     p.max_ranks = (a.max_ranks > 0 && a.max_ranks < p.R && p.R <= 32) ? a.max_ranks : 0;
     p.stash_pitch = p.max_ranks > 0 ? STASH_PITCH_RANKS : STASH_PITCH;
-    const int extra = R_SMEM_FIXED + 128 * p.stash_pitch * 4;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int grid = p.m_tiles < sms ? p.m_tiles : sms;
+    // a second epilogue group pays off once CTAs have several tiles each
+    p.epi_groups = (p.max_ranks == 0 && p.m_tiles >= 2 * grid) ? 2 : 1;
+    const int extra = R_SMEM_FIXED + 128 * p.epi_groups * p.stash_pitch * 4;
     const int ring = (R_SMEM_MAX - extra) < R_SMEM_TILES ? (R_SMEM_MAX - extra) : R_SMEM_TILES;
     p.stage_bytes = RM * RK * 2 + p.Np * RK * 2;
     p.stages = ring / p.stage_bytes;
@@ -513,9 +526,6 @@ cudaError_t launch_route_tc(const RouteArgs& a, cudaStream_t s) {
         !make_tmap_bf16(&tmW, a.w, (uint64_t)a.d, (uint64_t)a.E, 1, (uint32_t)p.Np, 2))
         return cudaErrorInvalidValue;
     const int smem = p.stages * p.stage_bytes + extra;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     static int attr_bytes = 0;
     if (attr_bytes < smem) {
         cudaError_t e =
@@ -523,8 +533,7 @@ cudaError_t launch_route_tc(const RouteArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_bytes = smem;
     }
-    const int grid = p.m_tiles < sms ? p.m_tiles : sms;
-    route_tc_kernel<<<grid, R_THREADS, smem, s>>>(tmX, tmW, p);
+    route_tc_kernel<<<grid, 64 + 128 * p.epi_groups, smem, s>>>(tmX, tmW, p);
     return cudaGetLastError();
 }
 
