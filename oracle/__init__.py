@@ -76,6 +76,9 @@ def _load():
         lib.oracle_combine.restype = None
         lib.oracle_update_sel_bias.argtypes = [i64, i32, i32, vp, vp, ctypes.c_float]
         lib.oracle_update_sel_bias.restype = None
+        lib.oracle_expert_ffn_backward.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                                   vp]
+        lib.oracle_expert_ffn_backward.restype = None
         lib.oracle_combine_backward.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         lib.oracle_combine_backward.restype = None
         lib.oracle_dispatch_backward.argtypes = [i64, i32, i32, i32, vp, vp, vp]
@@ -218,6 +221,25 @@ def update_sel_bias(expert_counts, sel_bias, T, k, gamma):
     _load().oracle_update_sel_bias(int(T), int(k), counts.numel(), _ptr(counts), _ptr(out),
                                    ctypes.c_float(gamma))
     return out
+
+
+def expert_ffn_backward(rows, w_up, w_down, d_out, act, d_ff, weight_grads=True):
+    """Backward through one expert FFN: (d_in fp64 [n,d], d_w_up fp64, d_w_down fp64)."""
+    rows = _cpu(rows)
+    n, d = rows.shape
+    a = _ACTS[act] if isinstance(act, str) else int(act)
+    up_rows = 2 * d_ff if a == SWIGLU else d_ff
+    wu = _cpu(w_up, rows.dtype)
+    wd = _cpu(w_down, rows.dtype)
+    dy = _cpu(d_out, rows.dtype)
+    d_in = torch.zeros((n, d), dtype=torch.float64)
+    dwu = torch.zeros((up_rows, d), dtype=torch.float64) if weight_grads else None
+    dwd = torch.zeros((d, d_ff), dtype=torch.float64) if weight_grads else None
+    if n:
+        _load().oracle_expert_ffn_backward(n, d, int(d_ff), a, _dtype_code(rows), _ptr(rows),
+                                           _ptr(wu), _ptr(wd), _ptr(dy), _ptr(d_in), _ptr(dwu),
+                                           _ptr(dwd))
+    return d_in, dwu, dwd
 
 
 def combine_backward(dy, yp, slot_row, topk_gate):

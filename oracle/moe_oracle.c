@@ -453,3 +453,79 @@ void oracle_dispatch_backward(int64_t T, int d, int k, int dtype, const void* d_
             dx[t * d + c] = acc;
         }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Backward through one expert FFN, for its n_rows rows: given the output    */
+/* gradient d_out [n_rows,d], the input gradient d_in [n_rows,d] and, when   */
+/* the pointers are not NULL, the weight gradients d_w_up [f or 2f, d] and    */
+/* d_w_down [d, f] (accumulated over the rows).  fp64, no intermediate       */
+/* rounding.  GELU: h = gelu(a), a = W1 x; gelu'(a) = Phi(a) + a phi(a).      */
+/* SwiGLU: h = silu(g) u; silu'(g) = s (1 + g (1 - s)), s = sigmoid(g).       */
+/* ------------------------------------------------------------------------ */
+void oracle_expert_ffn_backward(int64_t n_rows, int d, int f, int act, int dtype, const void* rows,
+                                const void* w_up, const void* w_down, const void* d_out,
+                                double* d_in, double* d_w_up, double* d_w_down) {
+    const int up_rows = act == OR_SWIGLU ? 2 * f : f;
+    double* xr = (double*)malloc(sizeof(double) * d);
+    double* pre = (double*)malloc(sizeof(double) * up_rows);
+    double* h = (double*)malloc(sizeof(double) * f);
+    double* dh = (double*)malloc(sizeof(double) * f);
+    double* dpre = (double*)malloc(sizeof(double) * up_rows);
+    double* dy = (double*)malloc(sizeof(double) * d);
+    if (d_w_up) memset(d_w_up, 0, sizeof(double) * (size_t)up_rows * d);
+    if (d_w_down) memset(d_w_down, 0, sizeof(double) * (size_t)d * f);
+    for (int64_t r = 0; r < n_rows; ++r) {
+        for (int i = 0; i < d; ++i) {
+            xr[i] = elem(rows, dtype, r * d + i);
+            dy[i] = elem(d_out, dtype, r * d + i);
+        }
+        for (int n = 0; n < up_rows; ++n) {
+            double a = 0.0;
+            for (int i = 0; i < d; ++i) a += xr[i] * elem(w_up, dtype, (int64_t)n * d + i);
+            pre[n] = a;
+        }
+        for (int n = 0; n < f; ++n) {
+            if (act == OR_GELU) {
+                h[n] = gelu_exact(pre[n]);
+            } else {
+                h[n] = silu(pre[n]) * pre[f + n];
+            }
+        }
+        /* dh = W_down^T dy */
+        for (int n = 0; n < f; ++n) {
+            double a = 0.0;
+            for (int c = 0; c < d; ++c) a += dy[c] * elem(w_down, dtype, (int64_t)c * f + n);
+            dh[n] = a;
+        }
+        for (int n = 0; n < f; ++n) {
+            if (act == OR_GELU) {
+                const double a = pre[n];
+                const double phi = exp(-0.5 * a * a) / sqrt(2.0 * 3.14159265358979323846);
+                dpre[n] = dh[n] * (0.5 * (1.0 + erf(a / sqrt(2.0))) + a * phi);
+            } else {
+                const double g = pre[n], u = pre[f + n];
+                const double s = 1.0 / (1.0 + exp(-g));
+                dpre[n] = dh[n] * u * s * (1.0 + g * (1.0 - s));
+                dpre[f + n] = dh[n] * g * s;
+            }
+        }
+        /* d_in = W_up^T dpre */
+        for (int i = 0; i < d; ++i) {
+            double a = 0.0;
+            for (int n = 0; n < up_rows; ++n) a += dpre[n] * elem(w_up, dtype, (int64_t)n * d + i);
+            d_in[r * d + i] = a;
+        }
+        if (d_w_down)
+            for (int c = 0; c < d; ++c)
+                for (int n = 0; n < f; ++n) d_w_down[(int64_t)c * f + n] += dy[c] * h[n];
+        if (d_w_up)
+            for (int n = 0; n < up_rows; ++n)
+                for (int i = 0; i < d; ++i) d_w_up[(int64_t)n * d + i] += dpre[n] * xr[i];
+    }
+    free(xr);
+    free(pre);
+    free(h);
+    free(dh);
+    free(dpre);
+    free(dy);
+}

@@ -559,3 +559,24 @@ def test_dispatch_backward_is_the_adjoint_of_permute():
     xd = x.double().clone().requires_grad_(True)
     (xd[disp["row_token"].long()] * d_xp.double()).sum().backward()
     assert torch.allclose(dx, xd.grad, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_expert_ffn_backward_matches_autograd(act):
+    """Backward through one expert FFN against PyTorch autograd in fp64 (a
+    library routine), input and weight gradients, non-square shapes."""
+    g = torch.Generator().manual_seed(21)
+    n, d, f = 7, 24, 40
+    up_rows = 2 * f if act == "swiglu" else f
+    x = torch.randn((n, d), generator=g)
+    wu = torch.randn((up_rows, d), generator=g) * 0.3
+    wd = torch.randn((d, f), generator=g) * 0.3
+    dy = torch.randn((n, d), generator=g)
+    d_in, dwu, dwd = oracle.expert_ffn_backward(x, wu, wd, dy, act, f)
+    xd, wud, wdd = (t.double().clone().requires_grad_(True) for t in (x, wu, wd))
+    pre = xd @ wud.T
+    h = F.gelu(pre) if act == "gelu" else F.silu(pre[:, :f]) * pre[:, f:]
+    ((h @ wdd.T) * dy.double()).sum().backward()
+    assert torch.allclose(d_in, xd.grad, rtol=1e-10, atol=1e-12)
+    assert torch.allclose(dwu, wud.grad, rtol=1e-10, atol=1e-12)
+    assert torch.allclose(dwd, wdd.grad, rtol=1e-10, atol=1e-12)
