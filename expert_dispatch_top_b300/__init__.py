@@ -99,6 +99,10 @@ def _load():
     lib.moe_combine_backward.restype = i32
     lib.moe_dispatch_backward.argtypes = [cfgp] + [vp] * 4
     lib.moe_dispatch_backward.restype = i32
+    lib.moe_expert_ffn_backward_scratch_size.argtypes = [cfgp, i32]
+    lib.moe_expert_ffn_backward_scratch_size.restype = ctypes.c_size_t
+    lib.moe_expert_ffn_backward.argtypes = [cfgp] + [vp] * 9 + [ctypes.c_size_t, vp, vp]
+    lib.moe_expert_ffn_backward.restype = i32
     lib.moe_update_sel_bias.argtypes = [cfgp, vp, vp, ctypes.c_float, vp]
     lib.moe_update_sel_bias.restype = i32
     lib.moe_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
@@ -246,6 +250,22 @@ def moe_dispatch_backward(cfg, d_xp, slot_row, dx, stream=None):
     """Reverse of the dispatch exchange: dx[t] = sum of its kept rows' gradients."""
     _check(_load().moe_dispatch_backward(ctypes.byref(cfg), _p(d_xp), _p(slot_row), _p(dx),
                                          _stream(stream)), "moe_dispatch_backward")
+
+
+def moe_expert_ffn_backward_scratch_size(cfg, weight_grads=True) -> int:
+    return int(_load().moe_expert_ffn_backward_scratch_size(ctypes.byref(cfg), int(bool(weight_grads))))
+
+
+def moe_expert_ffn_backward(cfg, xp, expert_offsets, w_up, w_down, d_yp, d_xp, d_w_up, d_w_down,
+                            scratch, ws, stream=None):
+    """Backward through the expert FFNs: d_xp and (when not None) the weight
+    gradients d_w_up, d_w_down; scratch is a uint8 device tensor of at least
+    moe_expert_ffn_backward_scratch_size bytes."""
+    nbytes = 0 if scratch is None else scratch.numel() * scratch.element_size()
+    _check(_load().moe_expert_ffn_backward(ctypes.byref(cfg), _p(xp), _p(expert_offsets), _p(w_up),
+                                           _p(w_down), _p(d_yp), _p(d_xp), _p(d_w_up),
+                                           _p(d_w_down), _p(scratch), ctypes.c_size_t(nbytes),
+                                           _p(ws), _stream(stream)), "moe_expert_ffn_backward")
 
 
 def moe_update_sel_bias(cfg, expert_counts, sel_bias, gamma, stream=None):

@@ -449,6 +449,73 @@ moe_status moe_dispatch_backward(const moe_config* cfg, const void* d_xp, const 
     return cuda_status(launch_combine(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t moe_expert_ffn_backward_scratch_size(const moe_config* cfg, int weight_grads) {
+    if (moe_check_config(cfg) != MOE_OK || check_ffn_config(cfg) != MOE_OK) return 0;
+    if (cfg->act == MOE_ACT_IDENTITY) return 0;
+    return ffn_backward_scratch_bytes(max_rows_of(cfg), cfg->E, cfg->d, cfg->d_ff,
+                                      cfg->act == MOE_ACT_SWIGLU, elem_bytes(cfg), weight_grads != 0);
+}
+
+moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* xp,
+                                   const int32_t* expert_offsets, const void* w_up,
+                                   const void* w_down, const void* d_yp, void* d_xp, void* d_w_up,
+                                   void* d_w_down, void* scratch, size_t scratch_bytes, void* ws,
+                                   moe_stream_t stream) {
+    moe_status st = moe_check_config(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = check_ffn_config(cfg)) != MOE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t rows = max_rows_of(cfg);
+    const int eb = elem_bytes(cfg);
+    if (cfg->act == MOE_ACT_IDENTITY) {
+        // identity experts: d_xp = d_yp, no weights
+        if (d_w_up || d_w_down) return MOE_ERR_INVALID_ARG;
+        if (rows == 0) return MOE_OK;
+        if (!d_yp || !d_xp) return MOE_ERR_INVALID_ARG;
+        if (d_yp == d_xp) return MOE_OK;
+        return cuda_status(
+            cudaMemcpyAsync(d_xp, d_yp, (size_t)rows * cfg->d * eb, cudaMemcpyDeviceToDevice, s));
+    }
+    if (!ws || !aligned16(ws) || !expert_offsets || !aligned4(expert_offsets) || !w_up || !w_down ||
+        !aligned16(w_up) || !aligned16(w_down) || !aligned16(d_w_up) || !aligned16(d_w_down))
+        return MOE_ERR_INVALID_ARG;
+    const bool wg = d_w_up || d_w_down;
+    if (scratch_bytes < moe_expert_ffn_backward_scratch_size(cfg, wg) || !scratch ||
+        (reinterpret_cast<uintptr_t>(scratch) & 255))
+        return MOE_ERR_INVALID_ARG;
+    if (rows > 0 && (!xp || !d_yp || !d_xp || !aligned16(xp) || !aligned16(d_yp) || !aligned16(d_xp)))
+        return MOE_ERR_INVALID_ARG;
+    if (cfg->act_dtype == MOE_DTYPE_BF16 && cfg->E > 256) return MOE_ERR_UNSUPPORTED;
+    if (rows == 0) {
+        // no routed rows: the weight gradients are zero
+        if (d_w_up && cudaMemsetAsync(d_w_up, 0, (size_t)cfg->E * (cfg->act == MOE_ACT_SWIGLU ? 2 : 1) *
+                                                     cfg->d_ff * cfg->d * eb, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (d_w_down &&
+            cudaMemsetAsync(d_w_down, 0, (size_t)cfg->E * cfg->d * cfg->d_ff * eb, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    FfnBwdArgs a;
+    a.xp = xp;
+    a.offsets = expert_offsets;
+    a.w_up = w_up;
+    a.w_down = w_down;
+    a.d_yp = d_yp;
+    a.d_xp = d_xp;
+    a.d_w_up = d_w_up;
+    a.d_w_down = d_w_down;
+    a.scratch = scratch;
+    a.status = at<uint32_t>(ws, layout_of(cfg).status);
+    a.rows_cap = rows;
+    a.E = cfg->E;
+    a.d = cfg->d;
+    a.f = cfg->d_ff;
+    a.epi = cfg->act == MOE_ACT_SWIGLU ? EPI_SWIGLU : EPI_GELU;
+    a.dtype = cfg->act_dtype;
+    return cuda_status(launch_ffn_backward(a, s));
+}
+
 moe_status moe_update_sel_bias(const moe_config* cfg, const int32_t* expert_counts, float* sel_bias,
                                float gamma, moe_stream_t stream) {
     moe_status st = moe_check_config(cfg);

@@ -1,0 +1,327 @@
+// ffn_backward.cu -- backward through the expert FFNs (training, the pages'
+// main setting: topicspectrum "Training teaches both experts and router").
+//
+// For each expert's rows (forward: pre = x W_up^T, h = act(pre), y = h W_down^T):
+//   1. pre  = xp . W_up^T                  recomputed (grouped GEMM, no epilogue)
+//   2. dh   = d_yp . W_down                (grouped GEMM on W_down^T)
+//   3. d_pre, h from pre and dh            (elementwise activation backward)
+//   4. d_xp = d_pre . W_up                 (grouped GEMM on W_up^T)
+//   5. dW_down[e] = sum over rows d_yp^T h, dW_up[e] = sum over rows d_pre^T xp
+// The GEMMs of steps 1, 2 and 4 run on the forward's grouped GEMM (tensor
+// cores for bf16, FFMA for fp32) with the expert weights transposed once per
+// call by a batched tiled transpose.  Step 5 sums over each expert's ragged
+// rows: bf16 runs it on the tensor cores in the grouped GEMM's K-grouped mode
+// over transposed, 64-row-padded copies of the activations; fp32 runs a tiled
+// FFMA kernel that reads the rows directly.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+// out[b][c][r] = in[b][r][c] for a batch of R x C matrices (32 x 32 tiles).
+template <typename T>
+__global__ void __launch_bounds__(256) transpose_kernel(const T* in, T* out, int R, int C) {
+    __shared__ T tile[32][33];
+    const int b = blockIdx.z;
+    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+    const T* src = in + (int64_t)b * R * C;
+    T* dst = out + (int64_t)b * R * C;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int i = ty; i < 32; i += 8) {
+        const int r = r0 + i, c = c0 + tx;
+        if (r < R && c < C) tile[i][tx] = src[(int64_t)r * C + c];
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int c = c0 + i, r = r0 + tx;
+        if (r < R && c < C) dst[(int64_t)c * R + r] = tile[tx][i];
+    }
+}
+
+__device__ __forceinline__ float sigm(float v) { return 1.f / (1.f + expf(-v)); }
+
+// Activation backward over the kept rows (offsets[E] of them), one thread per
+// hidden column.  SwiGLU: pre = [g | u]; GELU: pre = a.  Writes d_pre (same
+// shape as pre) and, when h is not null, the recomputed activation h.
+template <typename T>
+__global__ void __launch_bounds__(256) act_backward_kernel(const T* pre, const T* dh, T* d_pre, T* h,
+                                                           const int32_t* offsets, int E, int f,
+                                                           int gated, int64_t rows_cap) {
+    const int64_t rows = offsets[E] < rows_cap ? offsets[E] : rows_cap;
+    const int up = gated ? 2 * f : f;
+    const int64_t n = rows * f;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / f;
+        const int c = (int)(i - r * f);
+        const float gd = Elem<T>::to_f(dh[r * f + c]);
+        if (gated) {
+            const float g = Elem<T>::to_f(pre[r * up + c]);
+            const float u = Elem<T>::to_f(pre[r * up + f + c]);
+            const float s = sigm(g);
+            d_pre[r * up + c] = Elem<T>::from_f(gd * u * s * (1.f + g * (1.f - s)));
+            d_pre[r * up + f + c] = Elem<T>::from_f(gd * g * s);
+            if (h) h[r * f + c] = Elem<T>::from_f(g * s * u);
+        } else {
+            const float a = Elem<T>::to_f(pre[r * up + c]);
+            const float cdf = 0.5f * (1.f + erff(a * 0.70710678118654752440f));
+            const float pdf = 0.39894228040143267794f * expf(-0.5f * a * a);
+            d_pre[r * up + c] = Elem<T>::from_f(gd * (cdf + a * pdf));
+            if (h) h[r * f + c] = Elem<T>::from_f(a * cdf);
+        }
+    }
+}
+
+// Transposed copy of an expert-major activation buffer [rows, C] into
+// [C, P] with each expert's rows starting at a 64-aligned column (its rows
+// padded with zeros up to the next multiple of 64), so that each expert's
+// weight gradient is a GEMM over a whole number of 64-wide K blocks.
+__global__ void __launch_bounds__(256) transpose_pad_kernel(const __nv_bfloat16* in, __nv_bfloat16* out,
+                                                            const int32_t* offsets, int E, int C,
+                                                            int64_t P) {
+    __shared__ int poff[257];
+    __shared__ __nv_bfloat16 tile[32][34];
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int e = 0; e < E; ++e) {
+            poff[e] = run;
+            run += (offsets[e + 1] - offsets[e] + 63) / 64 * 64;
+        }
+        poff[E] = run;
+    }
+    __syncthreads();
+    const int total = poff[E];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    // padded column block of 32 (never straddles an expert: segments are 64-aligned)
+    for (int pb = blockIdx.x * 32; pb < total; pb += gridDim.x * 32)
+    for (int c0 = 0; c0 < C; c0 += 32) {
+        int lo = 0, hi = E - 1;  // expert owning padded column pb
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (poff[mid] <= pb) lo = mid;
+            else hi = mid - 1;
+        }
+        const int e = lo;
+        const int rows_e = offsets[e + 1] - offsets[e];
+        const int j0 = pb - poff[e];  // row within the expert
+        __syncthreads();
+        for (int i = ty; i < 32; i += 8) {
+            const int j = j0 + i, c = c0 + tx;
+            __nv_bfloat16 v = __float2bfloat16_rn(0.f);
+            if (j < rows_e && c < C) v = in[(int64_t)(offsets[e] + j) * C + c];
+            tile[i][tx] = v;
+        }
+        __syncthreads();
+        for (int i = ty; i < 32; i += 8) {
+            const int c = c0 + i;
+            if (c < C) out[(int64_t)c * P + pb + tx] = tile[tx][i];
+        }
+    }
+}
+
+// fp32 weight gradient: dW[g][m][n] = sum over rows r of group g of A[r][m] * B[r][n]
+// (64 x 64 tiles, 4 x 4 per thread, 16 rows per step).
+__global__ void __launch_bounds__(256) wgrad_simt_kernel(const float* A, const float* B, float* dW,
+                                                         const int32_t* offsets, int M, int N) {
+    __shared__ __align__(16) float As[16][64];
+    __shared__ __align__(16) float Bs[16][64];
+    const int g = blockIdx.z;
+    const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+    const int lo = offsets[g], hi = offsets[g + 1];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    float acc[4][4] = {};
+    for (int r0 = lo; r0 < hi; r0 += 16) {
+        for (int i = tid; i < 16 * 64; i += 256) {
+            const int rr = i / 64, cc = i % 64;
+            const int r = r0 + rr;
+            As[rr][cc] = (r < hi && m0 + cc < M) ? A[(int64_t)r * M + m0 + cc] : 0.f;
+            Bs[rr][cc] = (r < hi && n0 + cc < N) ? B[(int64_t)r * N + n0 + cc] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            const float4 a = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+            const float4 b = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+            const float ar[4] = {a.x, a.y, a.z, a.w}, br[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+    float* out = dW + (int64_t)g * M * N;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int m = m0 + ty * 4 + i;
+        if (m >= M) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = n0 + tx * 4 + j;
+            if (n < N) out[(int64_t)m * N + n] = acc[i][j];
+        }
+    }
+}
+
+template <typename T>
+cudaError_t transpose_batched(const void* in, void* out, int B, int R, int C, cudaStream_t s) {
+    dim3 grid((C + 31) / 32, (R + 31) / 32, B);
+    transpose_kernel<T><<<grid, 256, 0, s>>>(static_cast<const T*>(in), static_cast<T*>(out), R, C);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t ffn_backward_scratch_bytes(int64_t rows_cap, int E, int d, int f, int gated, int eb,
+                                  int weight_grads) {
+    const int up = gated ? 2 * f : f;
+    auto al = [](size_t v) { return (v + 255) / 256 * 256; };
+    size_t n = 0;
+    n += al((size_t)rows_cap * up * eb);   // pre
+    n += al((size_t)rows_cap * f * eb);    // dh
+    n += al((size_t)rows_cap * up * eb);   // d_pre
+    n += al((size_t)E * up * d * eb);      // W_up^T
+    n += al((size_t)E * d * f * eb);       // W_down^T
+    if (weight_grads) {
+        n += al((size_t)rows_cap * f * eb);  // h
+        if (eb == 2) {
+            const size_t P = (size_t)((rows_cap + 64 * (int64_t)E + 63) / 64 * 64);
+            n += al((size_t)d * P * 2);    // d_yp^T
+            n += al((size_t)f * P * 2);    // h^T
+            n += al((size_t)up * P * 2);   // d_pre^T
+            n += al((size_t)d * P * 2);    // xp^T
+        }
+    }
+    return n;
+}
+
+cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
+    const int gated = a.epi == EPI_SWIGLU;
+    const int up = gated ? 2 * a.f : a.f;
+    const int eb = a.dtype == MOE_DTYPE_F32 ? 4 : 2;
+    const bool wg = a.d_w_up || a.d_w_down;
+    auto al = [](size_t v) { return (v + 255) / 256 * 256; };
+    char* sp = static_cast<char*>(a.scratch);
+    void* pre = sp;
+    sp += al((size_t)a.rows_cap * up * eb);
+    void* dh = sp;
+    sp += al((size_t)a.rows_cap * a.f * eb);
+    void* d_pre = sp;
+    sp += al((size_t)a.rows_cap * up * eb);
+    void* w_upT = sp;
+    sp += al((size_t)a.E * up * a.d * eb);
+    void* w_downT = sp;
+    sp += al((size_t)a.E * a.d * a.f * eb);
+    void* h = nullptr;
+    if (wg) {
+        h = sp;
+        sp += al((size_t)a.rows_cap * a.f * eb);
+    }
+    cudaError_t e;
+    // transposed weights: W_up [E, up, d] -> [E, d, up]; W_down [E, d, f] -> [E, f, d]
+    e = eb == 4 ? transpose_batched<float>(a.w_up, w_upT, a.E, up, a.d, s)
+                : transpose_batched<__nv_bfloat16>(a.w_up, w_upT, a.E, up, a.d, s);
+    if (e != cudaSuccess) return e;
+    e = eb == 4 ? transpose_batched<float>(a.w_down, w_downT, a.E, a.d, a.f, s)
+                : transpose_batched<__nv_bfloat16>(a.w_down, w_downT, a.E, a.d, a.f, s);
+    if (e != cudaSuccess) return e;
+    auto gemm = [&](const void* A, const void* B, void* out, int N, int K) {
+        GemmArgs g;
+        g.A = A;
+        g.B = B;
+        g.out = out;
+        g.offsets = a.offsets;
+        g.rows_cap = a.rows_cap;
+        g.m_rows = 0;
+        g.G = a.E;
+        g.N = N;
+        g.K = K;
+        g.epi = EPI_NONE;
+        g.dtype = a.dtype;
+        g.status = a.status;
+        g.kgrouped = 0;
+        return eb == 4 ? launch_gemm_simt(g, s) : launch_gemm_tc(g, s);
+    };
+    if ((e = gemm(a.xp, a.w_up, pre, up, a.d)) != cudaSuccess) return e;       // 1
+    if ((e = gemm(a.d_yp, w_downT, dh, a.f, a.d)) != cudaSuccess) return e;    // 2
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (eb == 4)
+        act_backward_kernel<float><<<sms * 8, 256, 0, s>>>(
+            static_cast<const float*>(pre), static_cast<const float*>(dh), static_cast<float*>(d_pre),
+            static_cast<float*>(h), a.offsets, a.E, a.f, gated, a.rows_cap);
+    else
+        act_backward_kernel<__nv_bfloat16><<<sms * 8, 256, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(pre), static_cast<const __nv_bfloat16*>(dh),
+            static_cast<__nv_bfloat16*>(d_pre), static_cast<__nv_bfloat16*>(h), a.offsets, a.E, a.f,
+            gated, a.rows_cap);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;                     // 3
+    if ((e = gemm(d_pre, w_upT, a.d_xp, a.d, up)) != cudaSuccess) return e;    // 4
+    if (!wg) return cudaSuccess;
+    // 5: weight gradients
+    if (eb == 4) {
+        if (a.d_w_down) {
+            dim3 grid((a.f + 63) / 64, (a.d + 63) / 64, a.E);
+            wgrad_simt_kernel<<<grid, 256, 0, s>>>(static_cast<const float*>(a.d_yp),
+                                                   static_cast<const float*>(h),
+                                                   static_cast<float*>(a.d_w_down), a.offsets, a.d, a.f);
+        }
+        if (a.d_w_up) {
+            dim3 grid((a.d + 63) / 64, (up + 63) / 64, a.E);
+            wgrad_simt_kernel<<<grid, 256, 0, s>>>(static_cast<const float*>(d_pre),
+                                                   static_cast<const float*>(a.xp),
+                                                   static_cast<float*>(a.d_w_up), a.offsets, up, a.d);
+        }
+        return cudaGetLastError();
+    }
+    const int64_t P = (a.rows_cap + 64 * (int64_t)a.E + 63) / 64 * 64;
+    void* dypT = sp;
+    sp += al((size_t)a.d * P * 2);
+    void* hT = sp;
+    sp += al((size_t)a.f * P * 2);
+    void* dpreT = sp;
+    sp += al((size_t)up * P * 2);
+    void* xpT = sp;
+    sp += al((size_t)a.d * P * 2);
+    const unsigned pblocks = (unsigned)((P + 31) / 32 < 4096 ? (P + 31) / 32 : 4096);
+    auto tpad = [&](const void* in, void* out, int C) {
+        transpose_pad_kernel<<<pblocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in),
+                                                  static_cast<__nv_bfloat16*>(out), a.offsets, a.E, C,
+                                                  P);
+        return cudaGetLastError();
+    };
+    auto kgemm = [&](const void* At, const void* Bt, void* out, int M, int N) {
+        GemmArgs g;
+        g.A = At;       // [M, P]
+        g.B = Bt;       // [N, P]
+        g.out = out;    // [E, M, N]
+        g.offsets = a.offsets;
+        g.rows_cap = M;
+        g.m_rows = 0;
+        g.G = a.E;
+        g.N = N;
+        g.K = (int)P;
+        g.epi = EPI_NONE;
+        g.dtype = a.dtype;
+        g.status = a.status;
+        g.kgrouped = 1;
+        return launch_gemm_tc(g, s);
+    };
+    if (a.d_w_down) {
+        if ((e = tpad(a.d_yp, dypT, a.d)) != cudaSuccess) return e;
+        if ((e = tpad(h, hT, a.f)) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(a.d_w_down, 0, (size_t)a.E * a.d * a.f * 2, s)) != cudaSuccess) return e;
+        if ((e = kgemm(dypT, hT, a.d_w_down, a.d, a.f)) != cudaSuccess) return e;
+    }
+    if (a.d_w_up) {
+        if ((e = tpad(d_pre, dpreT, up)) != cudaSuccess) return e;
+        if ((e = tpad(a.xp, xpT, a.d)) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(a.d_w_up, 0, (size_t)a.E * up * a.d * 2, s)) != cudaSuccess) return e;
+        if ((e = kgemm(dpreT, xpT, a.d_w_up, up, a.d)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace moe

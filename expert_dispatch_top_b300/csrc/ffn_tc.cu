@@ -31,6 +31,13 @@
 // 128 gate rows and the matching 128 up rows, so the accumulator holds gate
 // and up side by side and the epilogue writes 128 output columns per tile.
 //
+// K-grouped mode (weight gradients): group g's output is a whole [M, N]
+// matrix, out[g] = A[:, K_g] . B[:, K_g]^T, where A [M, K] and B [N, K] are
+// activations transposed so that each group's rows form a 64-aligned range
+// K_g of the contraction dimension.  Tiles run over (group, n-tile, m-tile)
+// as above, but every tile's K loop covers only its group's K blocks; groups
+// with no rows have no tiles (the caller zeroes their output).
+//
 // Every mbarrier wait is bounded by %globaltimer: on timeout the kernel sets
 // MOE_DEV_GEMM_TIMEOUT, raises an abort flag seen by the other roles, drains
 // its own MMAs (bounded) and frees TMEM before returning.
@@ -64,6 +71,7 @@ struct TcParams {
     int num_kb;
     int n_tiles;
     int out_cols;  // output columns per tile (128 SwiGLU, 256 otherwise)
+    int kg_M;      // K-grouped mode: rows of each group's output matrix
     __nv_bfloat16* out;
     uint32_t* status;
 };
@@ -84,10 +92,15 @@ __device__ __forceinline__ float silu_f(float v) { return v / (1.f + __expf(-v))
 // Tile -> (group, n-tile, m-tile) from the per-group tile table.
 struct TileInfo {
     int g, m_tile, n_tile, row0, rows;
+    int kb0, nkb;  // K blocks of the tile
 };
 
+// Row-offset mode: rowoff/grows hold each group's first row and row count.
+// K-grouped mode: they hold each group's first K block and K-block count.
+template <bool KG>
 __device__ __forceinline__ TileInfo decode_tile(int tile, int G, const int* tstart, const int* mt,
-                                                const int* rowoff, const int* grows, int n_tiles) {
+                                                const int* rowoff, const int* grows,
+                                                const TcParams& p) {
     int lo = 0, hi = G - 1;  // last g with tstart[g] <= tile
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -99,13 +112,34 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, int G, const int* tsta
     const int local = tile - tstart[lo];
     ti.n_tile = local / mt[lo];
     ti.m_tile = local - ti.n_tile * mt[lo];
-    ti.row0 = rowoff[lo] + ti.m_tile * BM;
-    ti.rows = grows[lo] - ti.m_tile * BM;
+    if (KG) {
+        ti.row0 = ti.m_tile * BM;
+        ti.rows = p.kg_M - ti.row0;
+        ti.kb0 = rowoff[lo];
+        ti.nkb = grows[lo];
+    } else {
+        ti.row0 = rowoff[lo] + ti.m_tile * BM;
+        ti.rows = grows[lo] - ti.m_tile * BM;
+        ti.kb0 = 0;
+        ti.nkb = p.num_kb;
+    }
     if (ti.rows > BM) ti.rows = BM;
-    (void)n_tiles;
     return ti;
 }
 
+// Exclusive prefix sum over a warp.
+__device__ __forceinline__ int warp_excl_scan(int v, int lane, int* total) {
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    *total = __shfl_sync(0xffffffffu, incl, 31);
+    return incl - v;
+}
+
+template <bool KG>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
@@ -150,44 +184,53 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (warp == 2) {
         // Per-group tile table: lane l covers groups [8l, 8l+8).
-        int cnt[8];
-        int sum = 0;
+        int cnt[8], kbs[8];
+        int sum = 0, ksum = 0;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const int g = lane * 8 + q;
             cnt[q] = 0;
+            kbs[q] = 0;
             if (g < p.G) {
                 const int lo = p.offsets ? p.offsets[g] : 0;
                 const int hi = p.offsets ? p.offsets[g + 1] : (int)p.m_rows;
-                const int m = (hi - lo + BM - 1) / BM;
-                mt[g] = m > 0 ? m : 1;
-                rowoff[g] = lo;
-                grows[g] = hi - lo;
-                cnt[q] = m * p.n_tiles;
+                if (KG) {
+                    const int m = (p.kg_M + BM - 1) / BM;
+                    kbs[q] = (hi - lo + BK - 1) / BK;
+                    mt[g] = m;
+                    grows[g] = kbs[q];
+                    cnt[q] = kbs[q] > 0 ? m * p.n_tiles : 0;
+                } else {
+                    const int m = (hi - lo + BM - 1) / BM;
+                    mt[g] = m > 0 ? m : 1;
+                    rowoff[g] = lo;
+                    grows[g] = hi - lo;
+                    cnt[q] = m * p.n_tiles;
+                }
                 sum += cnt[q];
+                ksum += kbs[q];
             }
         }
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += n;
-        }
-        int run = incl - sum;
+        int total_tiles, total_kb;
+        int run = warp_excl_scan(sum, lane, &total_tiles);
+        int krun = warp_excl_scan(ksum, lane, &total_kb);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const int g = lane * 8 + q;
-            if (g < p.G) tstart[g] = run;
+            if (g < p.G) {
+                tstart[g] = run;
+                if (KG) rowoff[g] = krun;
+            }
             run += cnt[q];
+            krun += kbs[q];
         }
-        if (lane == 31) *total_s = incl;
+        if (lane == 31) *total_s = total_tiles;
     }
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total = *total_s;
-    const int n_tiles = p.n_tiles;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -195,16 +238,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-                const TileInfo ti = decode_tile(tile, p.G, tstart, mt, rowoff, grows, n_tiles);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                const TileInfo ti = decode_tile<KG>(tile, p.G, tstart, mt, rowoff, grows, p);
+                for (int kb = 0; kb < ti.nkb; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT)) break;
                     const uint32_t fb = full0 + 8 * stage;
                     mbar_expect_tx(fb, STAGE_BYTES);
                     const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
                     const uint32_t sb = sa + A_STAGE;
-                    const int k0 = kb * BK;
+                    const int k0 = (ti.kb0 + kb) * BK;
                     tma_load_2d(sa, &tmA, k0, ti.row0, fb);
-                    if (p.epi == EPI_SWIGLU) {
+                    if (KG) {
+                        tma_load_3d(sb, &tmB, k0, ti.n_tile * BN, 0, fb);
+                    } else if (p.epi == EPI_SWIGLU) {
                         tma_load_3d(sb, &tmB, k0, ti.n_tile * 128, ti.g, fb);
                         tma_load_3d(sb + B_STAGE / 2, &tmB, k0, p.N + ti.n_tile * 128, ti.g, fb);
                     } else {
@@ -232,7 +277,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                const int nkb = KG ? decode_tile<KG>(tile, p.G, tstart, mt, rowoff, grows, p).nkb
+                                   : p.num_kb;
+                for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT)) {
                         ok = false;
                         break;
@@ -270,7 +317,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const TileInfo ti = decode_tile(tile, p.G, tstart, mt, rowoff, grows, n_tiles);
+            const TileInfo ti = decode_tile<KG>(tile, p.G, tstart, mt, rowoff, grows, p);
+            __nv_bfloat16* obase = KG ? p.out + (int64_t)ti.g * p.kg_M * p.N : p.out;
             // every lane waits, then the warp agrees, so the .sync.aligned TMEM loads
             // below always run converged
             const bool ok = __all_sync(0xffffffffu, mbar_wait(accf0 + 8 * acc, acc_phase, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT));
@@ -314,7 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (lr < ti.rows && gc < p.N) {
                         const uint4 w = *reinterpret_cast<const uint4*>(my_stg + r * STG_PITCH +
                                                                         (lane & 7) * 16);
-                        st_v4(p.out + (int64_t)(ti.row0 + q * 32 + r) * p.N + gc, w);
+                        st_v4(obase + (int64_t)(ti.row0 + q * 32 + r) * p.N + gc, w);
                     }
                 }
                 __syncwarp();
@@ -355,13 +403,16 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
     if (gemm_tc_supported(a) != 0) return cudaErrorInvalidValue;
     const int64_t rows_cap = a.offsets ? a.rows_cap : a.m_rows;
     if (rows_cap <= 0) return cudaSuccess;
+    const bool kg = a.kgrouped != 0;
+    if (kg && (!a.offsets || a.epi != EPI_NONE)) return cudaErrorInvalidValue;
     const bool gated = a.epi == EPI_SWIGLU;
     const int b_rows = gated ? 2 * a.N : a.N;
     CUtensorMap tmA, tmB;
-    // A is read with 2-D loads, the stacked weights with 3-D loads (group index).
+    // A is read with 2-D loads, the stacked weights with 3-D loads (group index;
+    // a single [N, K] matrix in K-grouped mode).
     if (!make_tmap_bf16(&tmA, a.A, (uint64_t)a.K, (uint64_t)rows_cap, 1, BM, 2) ||
-        !make_tmap_bf16(&tmB, a.B, (uint64_t)a.K, (uint64_t)b_rows, (uint64_t)a.G, gated ? 128 : BN,
-                        3))
+        !make_tmap_bf16(&tmB, a.B, (uint64_t)a.K, (uint64_t)b_rows, kg ? 1 : (uint64_t)a.G,
+                        gated ? 128 : BN, 3))
         return cudaErrorInvalidValue;
     TcParams p;
     p.offsets = a.offsets;
@@ -375,21 +426,29 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
     p.n_tiles = (a.N + p.out_cols - 1) / p.out_cols;
     p.out = static_cast<__nv_bfloat16*>(a.out);
     p.status = a.status;
+    p.kg_M = kg ? (int)rows_cap : 0;
 
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t tiles_bound = ((rows_cap + BM - 1) / BM + p.G) * p.n_tiles;
+    const int64_t tiles_bound =
+        kg ? (int64_t)p.G * ((rows_cap + BM - 1) / BM) * p.n_tiles
+           : ((rows_cap + BM - 1) / BM + p.G) * p.n_tiles;
     int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
     if (grid < 1) grid = 1;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[kg]) {
+        cudaError_t e = kg ? cudaFuncSetAttribute(tc_gemm_kernel<true>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)
+                           : cudaFuncSetAttribute(tc_gemm_kernel<false>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[kg] = true;
     }
-    tc_gemm_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
+    if (kg)
+        tc_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
+    else
+        tc_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
     return cudaGetLastError();
 }
 

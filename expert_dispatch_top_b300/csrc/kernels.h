@@ -87,11 +87,34 @@ struct GemmArgs {
     int64_t m_rows;         // rows of the single group when offsets is null
     int G, N, K, epi, dtype;
     uint32_t* status;
+    // K-grouped mode (tensor-core kernel only): out[g] [rows_cap, N] = A[:, Kg] . B[:, Kg]^T
+    // where A is [rows_cap, K], B is [N, K] and group g owns the 64-aligned K range
+    // that ceil((offsets[g+1]-offsets[g]) / 64) blocks take after the previous groups'.
+    int kgrouped = 0;
 };
 cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s);
 // Returns 0 if the tensor-core grouped GEMM supports the shape, else non-zero.
 int gemm_tc_supported(const GemmArgs& a);
+
+// Backward through the expert FFNs (input gradient, optional weight gradients).
+struct FfnBwdArgs {
+    const void* xp;          // [rows_cap, d]
+    const int32_t* offsets;  // [E+1] device
+    const void* w_up;        // [E, up_rows, d]
+    const void* w_down;      // [E, d, f]
+    const void* d_yp;        // [rows_cap, d]
+    void* d_xp;              // [rows_cap, d]
+    void* d_w_up;            // [E, up_rows, d] or null
+    void* d_w_down;          // [E, d, f] or null
+    void* scratch;           // ffn_backward_scratch_bytes
+    uint32_t* status;
+    int64_t rows_cap;
+    int E, d, f, epi, dtype;
+};
+size_t ffn_backward_scratch_bytes(int64_t rows_cap, int E, int d, int f, int gated, int eb,
+                                  int weight_grads);
+cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s);
 
 cudaError_t launch_update_sel_bias(const int32_t* counts, float* bias, int E, int64_t T, int k,
                                    float gamma, cudaStream_t s);

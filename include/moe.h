@@ -274,6 +274,38 @@ moe_status moe_dispatch_backward(const moe_config* cfg, const void* d_xp, const 
                                  void* dx, moe_stream_t stream);
 
 /*
+ * Backward of Step 3 (training: topicspectrum "Training teaches both experts
+ * and router").  For each expert e and each of its rows r (forward:
+ * pre = xp[r] W_up[e]^T, h = act(pre), yp[r] = h W_down[e]^T) and
+ * d_yp = dL/dyp:
+ *   dh = d_yp[r] W_down[e];  d_pre = act'(pre) * dh  (SwiGLU: d_gate =
+ *   dh*u*silu'(g), d_up = dh*silu(g); GELU: dh*(Phi(a) + a*phi(a)));
+ *   d_xp[r] = d_pre W_up[e];
+ *   d_w_down[e] = sum over e's rows of d_yp[r]^T h;
+ *   d_w_up[e]   = sum over e's rows of d_pre^T xp[r].
+ * xp, d_yp, d_xp [max_rows, d]; expert_offsets [E+1] (device); weights and
+ * weight gradients shaped like moe_expert_ffn's weights.  d_w_up and
+ * d_w_down are outputs (overwritten, not accumulated); either may be NULL to
+ * skip it.  Rows of d_xp past offsets[E] are left untouched.  Routed experts
+ * only: the shared expert's backward is this call with a one-expert config
+ * (E = 1, k = 1) over its T rows.
+ * scratch: device memory of at least
+ * moe_expert_ffn_backward_scratch_size(cfg, weight_grads) bytes, 256-byte
+ * aligned, owned by the caller (weight_grads non-zero when either weight
+ * gradient is asked for).  ws supplies the device status word.
+ * bf16: pre, dh and d_pre are rounded to bf16 once each; the three
+ * contractions and the weight gradients run on the tensor cores with fp32
+ * accumulation (each weight gradient rounded to bf16 once).  fp32: FFMA.
+ * IDENTITY: d_xp = d_yp (weight gradients must be NULL, scratch unused).
+ */
+size_t moe_expert_ffn_backward_scratch_size(const moe_config* cfg, int weight_grads);
+moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* xp,
+                                   const int32_t* expert_offsets, const void* w_up,
+                                   const void* w_down, const void* d_yp, void* d_xp, void* d_w_up,
+                                   void* d_w_down, void* scratch, size_t scratch_bytes, void* ws,
+                                   moe_stream_t stream);
+
+/*
  * Buffers of moe_layer_forward.  xp, yp, h (and shared_h, shared_out when
  * n_shared == 1) are required.  Any metadata pointer may be NULL; the
  * library then keeps that array in the workspace.  For IDENTITY experts,
