@@ -265,6 +265,53 @@ def run_reference(args, w):
 # ---------------------------------------------------------------------------
 # GPU path
 # ---------------------------------------------------------------------------
+def time_ffn_backward(args, w, cfg, b, inp, stream, peaks):
+    """Opt-in (--backward): time moe_expert_ffn_backward (input and both weight
+    gradients) over the forward's dispatched rows, with a seeded d_yp.
+
+    Tensor flops per call: the recomputed up projection (2 rows d up), dh
+    (2 rows d f), d_xp (2 rows up d), dW_down (2 rows d f), dW_up (2 rows up d);
+    the bf16 weight and activation transposes are HBM traffic, not flops."""
+    import torch
+
+    import expert_dispatch_top_b300 as moe
+    import moe_workloads as W
+
+    rows = int(b.expert_offsets[-1].item())
+    up = w.up_rows
+    g = W._gen(w.seed + 100, b.xp.device)
+    d_yp = W._grid_normal(tuple(b.yp.shape), 0.5, 2.0 ** -9, 4.0, g, b.xp.device).to(b.yp.dtype)
+    d_xp = torch.empty_like(b.xp)
+    d_wu = torch.empty_like(inp["w_up"])
+    d_wd = torch.empty_like(inp["w_down"])
+    nbytes = moe.moe_expert_ffn_backward_scratch_size(cfg, True)
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device=b.xp.device)
+
+    def call():
+        moe.moe_expert_ffn_backward(cfg, b.xp, b.expert_offsets, inp["w_up"], inp["w_down"], d_yp,
+                                    d_xp, d_wu, d_wd, scratch, b.ws)
+
+    for _ in range(max(args.warmup, 1)):
+        call()
+    torch.cuda.synchronize()
+    n = max(args.steps // 4, 3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(b.ws) == 0
+    ms = e0.elapsed_time(e1) / n
+    flops = 2.0 * rows * w.d * (3 * up + 2 * w.d_ff)
+    tf = flops / (ms * 1e-3) / 1e12
+    out = {"ms": ms, "calls": n, "rows": rows, "tensor_flops_per_call": flops, "TFLOP/s": tf,
+           "scratch_bytes": nbytes}
+    if w.dtype == "bf16":
+        out["frac_bf16_sustained"] = tf / peaks["bf16_sus"]
+    return out
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -452,6 +499,8 @@ def run_ours(args, w):
                     "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
                     "traffic": None, "peak_kind": f"HBM copy ({peaks['src']})",
                     "algorithmic_bytes_per_step": work["permute_bytes"]}
+    if args.backward and not ident:
+        kernels["ffn_backward"] = time_ffn_backward(args, w, cfg, b, inp, stream, peaks)
     kernels["route"]["frac_fp32_ffma"] = kernels["route"]["TFLOP/s_fp32"] / \
         fp32_ffma_peak_tflops(sms, peaks["sm_mhz"])
     kernels["route"]["frac_hbm"] = kernels["route"]["GB/s"] / peaks["hbm"]
@@ -500,6 +549,8 @@ def main():
     ap.add_argument("--max-ranks", type=int, default=-1, help="rank-limited routing (0: off)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="also time the expert-FFN backward (kernels.ffn_backward)")
     ap.add_argument("--ref-route-tokens", type=int, default=256)
     ap.add_argument("--ref-ffn-tokens", type=int, default=32)
     args = ap.parse_args()

@@ -7,12 +7,14 @@
 //   3. d_pre, h from pre and dh            (elementwise activation backward)
 //   4. d_xp = d_pre . W_up                 (grouped GEMM on W_up^T)
 //   5. dW_down[e] = sum over rows d_yp^T h, dW_up[e] = sum over rows d_pre^T xp
-// The GEMMs of steps 1, 2 and 4 run on the forward's grouped GEMM (tensor
-// cores for bf16, FFMA for fp32) with the expert weights transposed once per
+// The GEMMs of steps 1, 2 and 4 run on the forward's grouped GEMM.  bf16: on
+// the tensor cores, steps 2 and 4 reading the weights as stored through the
+// GEMM's MN-major B mode; fp32: FFMA, with the weights transposed once per
 // call by a batched tiled transpose.  Step 5 sums over each expert's ragged
 // rows: bf16 runs it on the tensor cores in the grouped GEMM's K-grouped mode
-// over transposed, 64-row-padded copies of the activations; fp32 runs a tiled
-// FFMA kernel that reads the rows directly.
+// over transposed, 64-row-padded copies of the activations (that mode also
+// writes the zero gradients of experts without rows); fp32 runs a tiled FFMA
+// kernel that reads the rows directly.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -181,8 +183,10 @@ size_t ffn_backward_scratch_bytes(int64_t rows_cap, int E, int d, int f, int gat
     n += al((size_t)rows_cap * up * eb);   // pre
     n += al((size_t)rows_cap * f * eb);    // dh
     n += al((size_t)rows_cap * up * eb);   // d_pre
-    n += al((size_t)E * up * d * eb);      // W_up^T
-    n += al((size_t)E * d * f * eb);       // W_down^T
+    if (eb == 4) {
+        n += al((size_t)E * up * d * eb);  // W_up^T
+        n += al((size_t)E * d * f * eb);   // W_down^T
+    }
     if (weight_grads) {
         n += al((size_t)rows_cap * f * eb);  // h
         if (eb == 2) {
@@ -209,24 +213,28 @@ cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
     sp += al((size_t)a.rows_cap * a.f * eb);
     void* d_pre = sp;
     sp += al((size_t)a.rows_cap * up * eb);
-    void* w_upT = sp;
-    sp += al((size_t)a.E * up * a.d * eb);
-    void* w_downT = sp;
-    sp += al((size_t)a.E * a.d * a.f * eb);
+    void* w_upT = nullptr;
+    void* w_downT = nullptr;
+    if (eb == 4) {
+        w_upT = sp;
+        sp += al((size_t)a.E * up * a.d * eb);
+        w_downT = sp;
+        sp += al((size_t)a.E * a.d * a.f * eb);
+    }
     void* h = nullptr;
     if (wg) {
         h = sp;
         sp += al((size_t)a.rows_cap * a.f * eb);
     }
     cudaError_t e;
-    // transposed weights: W_up [E, up, d] -> [E, d, up]; W_down [E, d, f] -> [E, f, d]
-    e = eb == 4 ? transpose_batched<float>(a.w_up, w_upT, a.E, up, a.d, s)
-                : transpose_batched<__nv_bfloat16>(a.w_up, w_upT, a.E, up, a.d, s);
-    if (e != cudaSuccess) return e;
-    e = eb == 4 ? transpose_batched<float>(a.w_down, w_downT, a.E, a.d, a.f, s)
-                : transpose_batched<__nv_bfloat16>(a.w_down, w_downT, a.E, a.d, a.f, s);
-    if (e != cudaSuccess) return e;
-    auto gemm = [&](const void* A, const void* B, void* out, int N, int K) {
+    if (eb == 4) {
+        // transposed weights: W_up [E, up, d] -> [E, d, up]; W_down [E, d, f] -> [E, f, d]
+        if ((e = transpose_batched<float>(a.w_up, w_upT, a.E, up, a.d, s)) != cudaSuccess) return e;
+        if ((e = transpose_batched<float>(a.w_down, w_downT, a.E, a.d, a.f, s)) != cudaSuccess)
+            return e;
+    }
+    // out = A . B^T with B [E, N, K] (b_mn = 0), or out = A . B with B [E, K, N] (b_mn = 1)
+    auto gemm = [&](const void* A, const void* B, void* out, int N, int K, int b_mn) {
         GemmArgs g;
         g.A = A;
         g.B = B;
@@ -241,10 +249,12 @@ cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
         g.dtype = a.dtype;
         g.status = a.status;
         g.kgrouped = 0;
+        g.b_mn = b_mn;
         return eb == 4 ? launch_gemm_simt(g, s) : launch_gemm_tc(g, s);
     };
-    if ((e = gemm(a.xp, a.w_up, pre, up, a.d)) != cudaSuccess) return e;       // 1
-    if ((e = gemm(a.d_yp, w_downT, dh, a.f, a.d)) != cudaSuccess) return e;    // 2
+    const bool tc = eb == 2;
+    if ((e = gemm(a.xp, a.w_up, pre, up, a.d, 0)) != cudaSuccess) return e;  // 1
+    if ((e = gemm(a.d_yp, tc ? a.w_down : w_downT, dh, a.f, a.d, tc)) != cudaSuccess) return e;  // 2
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -258,7 +268,7 @@ cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
             static_cast<__nv_bfloat16*>(d_pre), static_cast<__nv_bfloat16*>(h), a.offsets, a.E, a.f,
             gated, a.rows_cap);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;                     // 3
-    if ((e = gemm(d_pre, w_upT, a.d_xp, a.d, up)) != cudaSuccess) return e;    // 4
+    if ((e = gemm(d_pre, tc ? a.w_up : w_upT, a.d_xp, a.d, up, tc)) != cudaSuccess) return e;  // 4
     if (!wg) return cudaSuccess;
     // 5: weight gradients
     if (eb == 4) {
@@ -312,13 +322,11 @@ cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
     if (a.d_w_down) {
         if ((e = tpad(a.d_yp, dypT, a.d)) != cudaSuccess) return e;
         if ((e = tpad(h, hT, a.f)) != cudaSuccess) return e;
-        if ((e = cudaMemsetAsync(a.d_w_down, 0, (size_t)a.E * a.d * a.f * 2, s)) != cudaSuccess) return e;
         if ((e = kgemm(dypT, hT, a.d_w_down, a.d, a.f)) != cudaSuccess) return e;
     }
     if (a.d_w_up) {
         if ((e = tpad(d_pre, dpreT, up)) != cudaSuccess) return e;
         if ((e = tpad(a.xp, xpT, a.d)) != cudaSuccess) return e;
-        if ((e = cudaMemsetAsync(a.d_w_up, 0, (size_t)a.E * up * a.d * 2, s)) != cudaSuccess) return e;
         if ((e = kgemm(dpreT, xpT, a.d_w_up, up, a.d)) != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -31,6 +31,11 @@
 // 128 gate rows and the matching 128 up rows, so the accumulator holds gate
 // and up side by side and the epilogue writes 128 output columns per tile.
 //
+// MN-major B (input gradients of the backward): B is given as [G, K, N] with
+// N contiguous, i.e. the forward's weights read without a transpose.  A stage
+// holds four TMA boxes of 64 N-columns x 64 K-rows (128-byte swizzle), and the
+// MMA reads B through MN-major descriptors (chunk stride 8 KB).  No epilogue.
+//
 // K-grouped mode (weight gradients): group g's output is a whole [M, N]
 // matrix, out[g] = A[:, K_g] . B[:, K_g]^T, where A [M, K] and B [N, K] are
 // activations transposed so that each group's rows form a 64-aligned range
@@ -63,6 +68,8 @@ constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_BYTES + TABLE_BYTES
 constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
+constexpr uint32_t kIdescBmn = idesc_bf16_bmn(BM, BN);
+constexpr int MN_CHUNK = 64 * BK * 2;  // one 64-column x 64-row box of an MN-major B: 8 KB
 
 struct TcParams {
     const int32_t* offsets;
@@ -139,7 +146,7 @@ __device__ __forceinline__ int warp_excl_scan(int v, int lane, int* total) {
     return incl - v;
 }
 
-template <bool KG>
+template <bool KG, bool BMN>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
@@ -199,7 +206,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     kbs[q] = (hi - lo + BK - 1) / BK;
                     mt[g] = m;
                     grows[g] = kbs[q];
-                    cnt[q] = kbs[q] > 0 ? m * p.n_tiles : 0;
+                    cnt[q] = m * p.n_tiles;  // a group without rows gets zero tiles written
                 } else {
                     const int m = (hi - lo + BM - 1) / BM;
                     mt[g] = m > 0 ? m : 1;
@@ -249,6 +256,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tma_load_2d(sa, &tmA, k0, ti.row0, fb);
                     if (KG) {
                         tma_load_3d(sb, &tmB, k0, ti.n_tile * BN, 0, fb);
+                    } else if (BMN) {
+#pragma unroll
+                        for (int c = 0; c < BN / 64; ++c)
+                            tma_load_3d(sb + c * MN_CHUNK, &tmB, ti.n_tile * BN + c * 64, k0, ti.g, fb);
                     } else if (p.epi == EPI_SWIGLU) {
                         tma_load_3d(sb, &tmB, k0, ti.n_tile * 128, ti.g, fb);
                         tma_load_3d(sb + B_STAGE / 2, &tmB, k0, p.N + ti.n_tile * 128, ti.g, fb);
@@ -288,9 +299,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
                     const uint32_t sb = sa + A_STAGE;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_bf16(d_tmem, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), kIdesc,
-                                 (kb | kk) != 0 ? 1u : 0u);
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        if (BMN)  // 16 K rows of 128 B per MMA
+                            mma_bf16(d_tmem, sw128_desc(sa + kk * 32),
+                                     sw128_mn_desc(sb + kk * 2048, MN_CHUNK), kIdescBmn,
+                                     (kb | kk) != 0 ? 1u : 0u);
+                        else
+                            mma_bf16(d_tmem, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), kIdesc,
+                                     (kb | kk) != 0 ? 1u : 0u);
+                    }
                     commit(empty0 + 8 * stage);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -331,7 +348,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int h = 0; h < 2; ++h) {
                     const int col = c64 * 64 + h * 32;
                     float v[32];
-                    tmem_ld32(tbase + (uint32_t)col, v);
+                    if (KG && ti.nkb == 0) {  // warp-uniform: the group has no rows
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    } else {
+                        tmem_ld32(tbase + (uint32_t)col, v);
+                    }
                     if (p.epi == EPI_SWIGLU) {
                         float u[32];
                         tmem_ld32(tbase + (uint32_t)(128 + col), u);
@@ -393,6 +415,7 @@ int gemm_tc_supported(const GemmArgs& a) {
     if (a.K % BK != 0 || a.N % 64 != 0) return 2;
     if (a.G < 1 || a.G > MAX_GROUPS) return 3;
     if (a.rows_cap >= (1ll << 31) || a.K > (1 << 20)) return 4;
+    if (a.b_mn && (a.kgrouped || a.epi != EPI_NONE)) return 6;
     if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B) |
          reinterpret_cast<uintptr_t>(a.out)) & 15)
         return 5;
@@ -404,16 +427,22 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
     const int64_t rows_cap = a.offsets ? a.rows_cap : a.m_rows;
     if (rows_cap <= 0) return cudaSuccess;
     const bool kg = a.kgrouped != 0;
+    const bool bmn = a.b_mn != 0;
     if (kg && (!a.offsets || a.epi != EPI_NONE)) return cudaErrorInvalidValue;
     const bool gated = a.epi == EPI_SWIGLU;
     const int b_rows = gated ? 2 * a.N : a.N;
     CUtensorMap tmA, tmB;
     // A is read with 2-D loads, the stacked weights with 3-D loads (group index;
     // a single [N, K] matrix in K-grouped mode).
-    if (!make_tmap_bf16(&tmA, a.A, (uint64_t)a.K, (uint64_t)rows_cap, 1, BM, 2) ||
-        !make_tmap_bf16(&tmB, a.B, (uint64_t)a.K, (uint64_t)b_rows, kg ? 1 : (uint64_t)a.G,
-                        gated ? 128 : BN, 3))
+    if (!make_tmap_bf16(&tmA, a.A, (uint64_t)a.K, (uint64_t)rows_cap, 1, BM, 2))
         return cudaErrorInvalidValue;
+    if (bmn) {  // [G, K, N]: boxes of 64 N-columns x 64 K-rows
+        if (!make_tmap_bf16(&tmB, a.B, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.G, BK, 3))
+            return cudaErrorInvalidValue;
+    } else if (!make_tmap_bf16(&tmB, a.B, (uint64_t)a.K, (uint64_t)b_rows, kg ? 1 : (uint64_t)a.G,
+                               gated ? 128 : BN, 3)) {
+        return cudaErrorInvalidValue;
+    }
     TcParams p;
     p.offsets = a.offsets;
     p.m_rows = a.m_rows;
@@ -436,19 +465,17 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
            : ((rows_cap + BM - 1) / BM + p.G) * p.n_tiles;
     int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
     if (grid < 1) grid = 1;
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[kg]) {
-        cudaError_t e = kg ? cudaFuncSetAttribute(tc_gemm_kernel<true>,
-                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)
-                           : cudaFuncSetAttribute(tc_gemm_kernel<false>,
-                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    const int mode = kg ? 1 : bmn ? 2 : 0;
+    auto kern = mode == 1 ? tc_gemm_kernel<true, false>
+                          : mode == 2 ? tc_gemm_kernel<false, true> : tc_gemm_kernel<false, false>;
+    static bool attr_set[3] = {false, false, false};
+    if (!attr_set[mode]) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr_set[kg] = true;
+        attr_set[mode] = true;
     }
-    if (kg)
-        tc_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
-    else
-        tc_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
+    kern<<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
     return cudaGetLastError();
 }
 

@@ -91,6 +91,9 @@ struct GemmArgs {
     // where A is [rows_cap, K], B is [N, K] and group g owns the 64-aligned K range
     // that ceil((offsets[g+1]-offsets[g]) / 64) blocks take after the previous groups'.
     int kgrouped = 0;
+    // MN-major B (tensor-core kernel, no epilogue): B is [G, K, N] row-major, i.e.
+    // out = A . B[g] with the weights read as stored.
+    int b_mn = 0;
 };
 cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s);

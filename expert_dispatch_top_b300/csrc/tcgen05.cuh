@@ -129,6 +129,24 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
            ((uint32_t)(M >> 4) << 24);
 }
 
+// Same with B MN-major (bit 16: B is read with N as the contiguous dimension).
+__host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) {
+    return idesc_bf16(M, N) | (1u << 16);
+}
+
+// Descriptor of an MN-major operand with 128-byte swizzle: the tile is stored
+// as chunks of 64 MN-elements, each chunk one 128-byte row per K index (8-row
+// swizzle atoms of 1024 B, so 1024 B between groups of 8 K rows), and
+// chunk_bytes between consecutive chunks along MN.
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t chunk_bytes) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((chunk_bytes >> 4) & 0x3FFFu) << 16;  // leading byte offset: next MN chunk
+    d |= (uint64_t)(1024 >> 4) << 32;                      // stride byte offset: 8 K rows
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accum) {
     asm volatile(

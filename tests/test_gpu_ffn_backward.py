@@ -156,13 +156,19 @@ def test_ffn_backward_layer_sized(shape):
     others[samp] = False
     assert torch.all(d_xp[others.to(DEV)] == 0)
     gw = torch.Generator().manual_seed(29)
+    # weight gradients of a few experts (each oracle call forms a whole dW in fp64),
+    # an empty one among them for the DeepSeek shape
+    wg_experts = {0, 5} if shape == "mixtral" else {0, 3, 17, 30}
     for e in range(len(counts)):
         lo, hi = int(offs[e]), int(offs[e + 1])
         rows = samp[(samp >= lo) & (samp < hi)]
         ref_in, ref_wu, ref_wd = oracle.expert_ffn_backward(xp[rows], w_up[e], w_dn[e], d_yp[rows],
-                                                            "swiglu", f)
+                                                            "swiglu", f,
+                                                            weight_grads=e in wg_experts)
         if rows.numel():
             assert_rows_close(d_xp[rows.to(DEV)], ref_in, 2e-2)
+        if e not in wg_experts:
+            continue
         # weight-gradient rows checked on a sample (the full matrices are large),
         # against the whole matrix's scale
         ru = torch.randperm(ref_wu.shape[0], generator=gw)[:96]
