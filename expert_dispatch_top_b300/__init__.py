@@ -27,7 +27,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT,
 MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_ACT_GELU, MOE_ACT_SWIGLU, MOE_ACT_IDENTITY = 0, 1, 2
-MOE_DEV_LOOKBACK_TIMEOUT, MOE_DEV_GEMM_TIMEOUT, MOE_DEV_BAD_INDEX = 0x1, 0x2, 0x4
+MOE_DEV_GEMM_TIMEOUT, MOE_DEV_BAD_INDEX = 0x2, 0x4
 
 _ACTS = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU, "identity": MOE_ACT_IDENTITY}
 _SCORES = {"softmax": MOE_SCORE_SOFTMAX, "sigmoid": MOE_SCORE_SIGMOID}
@@ -84,9 +84,9 @@ def _load():
     lib.moe_route.restype = i32
     lib.moe_dispatch.argtypes = [cfgp] + [vp] * 12
     lib.moe_dispatch.restype = i32
-    lib.moe_test_dispatch_stall.argtypes = [cfgp] + [vp] * 10 + [ctypes.c_int32, ctypes.c_uint32,
-                                                                  vp, vp]
-    lib.moe_test_dispatch_stall.restype = i32
+    lib.moe_test_expert_ffn_stall.argtypes = [cfgp] + [vp] * 4 + [ctypes.c_int32, ctypes.c_uint32,
+                                                                vp, vp]
+    lib.moe_test_expert_ffn_stall.restype = i32
     lib.moe_dispatch_noalloc.argtypes = [cfgp] + [vp] * 12
     lib.moe_dispatch_noalloc.restype = i32
     lib.moe_expert_ffn.argtypes = [cfgp] + [vp] * 13
@@ -194,16 +194,13 @@ def moe_dispatch(cfg, x, topk_idx, xp, row_token, slot_row, expert_counts, exper
                                 _stream(stream)), "moe_dispatch")
 
 
-def moe_test_dispatch_stall(cfg, x, topk_idx, xp, row_token, slot_row, expert_counts,
-                            expert_offsets, rank_counts, rank_splits, n_dropped, stall_block,
-                            wait_limit_us, ws, stream=None):
-    """Failure-detection hook: dispatch with one look-back block that never
-    publishes; the bounded wait runs out and sets MOE_DEV_LOOKBACK_TIMEOUT."""
-    _check(_load().moe_test_dispatch_stall(ctypes.byref(cfg), _p(x), _p(topk_idx), _p(xp),
-                                           _p(row_token), _p(slot_row), _p(expert_counts),
-                                           _p(expert_offsets), _p(rank_counts), _p(rank_splits),
-                                           _p(n_dropped), int(stall_block), int(wait_limit_us),
-                                           _p(ws), _stream(stream)), "moe_test_dispatch_stall")
+def moe_test_expert_ffn_stall(cfg, xp, expert_offsets, w_up, h, stall_kb, wait_limit_us, ws,
+                              stream=None):
+    """Failure-detection hook: the FFN up projection with one pipeline stage
+    never loaded; the bounded wait runs out and sets MOE_DEV_GEMM_TIMEOUT."""
+    _check(_load().moe_test_expert_ffn_stall(ctypes.byref(cfg), _p(xp), _p(expert_offsets),
+                                             _p(w_up), _p(h), int(stall_kb), int(wait_limit_us),
+                                             _p(ws), _stream(stream)), "moe_test_expert_ffn_stall")
 
 
 def moe_dispatch_noalloc(cfg, x, topk_idx, xp, row_token, slot_row, expert_counts, expert_offsets,

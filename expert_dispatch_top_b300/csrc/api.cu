@@ -37,22 +37,22 @@ int64_t max_rows_of(const moe_config* c) {
 
 // Byte offsets of every workspace section.
 struct Layout {
-    size_t status = 0, ticket = 4, done = 8;
-    size_t counts, desc, splits_acc;
+    size_t status = 0;
+    size_t totals, hist, prefix, splits_acc;
     size_t topk_idx, topk_gate, slot_row, row_token, expert_counts, offsets, rank_counts,
         rank_splits, n_dropped;
-    size_t clear_bytes;  // bytes [4, clear_bytes) are zeroed before dispatch
     size_t total;
 };
 
 Layout layout_of(const moe_config* c) {
     Layout L;
     size_t o = kAlign;
-    L.counts = o;
+    L.totals = o;
     o = align_up(o + (size_t)c->E * 4);
-    L.clear_bytes = o;
-    L.desc = o;
-    o = align_up(o + (size_t)dispatch_blocks(c->T) * c->E * 8);
+    L.hist = o;
+    o = align_up(o + (size_t)dispatch_blocks(c->T) * c->E * 4);
+    L.prefix = o;
+    o = align_up(o + (size_t)dispatch_blocks(c->T) * c->E * 4);
     L.splits_acc = o;
     o = align_up(o + (size_t)c->R * c->R * 4);
     const size_t tk = (size_t)c->T * c->k;
@@ -126,8 +126,7 @@ moe_status route_impl(const moe_config* c, const void* x, const void* w, const f
 moe_status dispatch_impl(const moe_config* c, const void* x, const int32_t* idx, void* xp,
                          int32_t* row_token, int32_t* slot_row, int32_t* counts, int32_t* offsets,
                          int32_t* rank_counts, int32_t* rank_splits, int32_t* n_dropped, void* ws,
-                         cudaStream_t s, int stall_block = -1,
-                         uint64_t wait_ns = kWaitTimeoutNs) {
+                         cudaStream_t s) {
     if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
     if (!counts || !offsets || !rank_counts || !n_dropped) return MOE_ERR_INVALID_ARG;
     if (c->T > 0 && (!x || !idx || !xp || !row_token || !slot_row)) return MOE_ERR_INVALID_ARG;
@@ -136,8 +135,6 @@ moe_status dispatch_impl(const moe_config* c, const void* x, const int32_t* idx,
         !aligned4(rank_splits) || !aligned4(n_dropped))
         return MOE_ERR_INVALID_ARG;
     const Layout L = layout_of(c);
-    cudaError_t e = cudaMemsetAsync(at<char>(ws, 4), 0, L.clear_bytes - 4, s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
     DispatchArgs a;
     a.x = x;
     a.idx = idx;
@@ -150,10 +147,9 @@ moe_status dispatch_impl(const moe_config* c, const void* x, const int32_t* idx,
     a.rank_splits = rank_splits;
     a.n_dropped = n_dropped;
     a.status = at<uint32_t>(ws, L.status);
-    a.ticket = at<uint32_t>(ws, L.ticket);
-    a.done = at<uint32_t>(ws, L.done);
-    a.counts = at<int32_t>(ws, L.counts);
-    a.desc = at<uint64_t>(ws, L.desc);
+    a.totals = at<int32_t>(ws, L.totals);
+    a.hist = at<int32_t>(ws, L.hist);
+    a.prefix = at<int32_t>(ws, L.prefix);
     a.splits_acc = at<int32_t>(ws, L.splits_acc);
     a.T = c->T;
     a.d = c->d;
@@ -162,8 +158,6 @@ moe_status dispatch_impl(const moe_config* c, const void* x, const int32_t* idx,
     a.R = c->R;
     a.dtype = c->act_dtype;
     a.C = capacity_of(c);
-    a.stall_block = stall_block;
-    a.wait_ns = wait_ns;
     return cuda_status(launch_dispatch(a, s));
 }
 
@@ -331,19 +325,37 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
-moe_status moe_test_dispatch_stall(const moe_config* cfg, const void* x, const int32_t* topk_idx,
-                                   void* xp, int32_t* row_token, int32_t* slot_row,
-                                   int32_t* expert_counts, int32_t* expert_offsets,
-                                   int32_t* rank_counts, int32_t* rank_splits, int32_t* n_dropped,
-                                   int32_t stall_block, uint32_t wait_limit_us, void* ws,
-                                   moe_stream_t stream) {
+moe_status moe_test_expert_ffn_stall(const moe_config* cfg, const void* xp,
+                                     const int32_t* expert_offsets, const void* w_up, void* h,
+                                     int32_t stall_kb, uint32_t wait_limit_us, void* ws,
+                                     moe_stream_t stream) {
     moe_status st = moe_check_config(cfg);
     if (st != MOE_OK) return st;
-    if (stall_block < 0 || wait_limit_us == 0 || wait_limit_us > 4000000u) return MOE_ERR_INVALID_ARG;
-    return dispatch_impl(cfg, x, topk_idx, xp, row_token, slot_row, expert_counts, expert_offsets,
-                         rank_counts, rank_splits, n_dropped, ws,
-                         reinterpret_cast<cudaStream_t>(stream), stall_block,
-                         (uint64_t)wait_limit_us * 1000ull);
+    if ((st = check_ffn_config(cfg)) != MOE_OK) return st;
+    if (cfg->act_dtype != MOE_DTYPE_BF16 || cfg->act == MOE_ACT_IDENTITY) return MOE_ERR_UNSUPPORTED;
+    if (stall_kb < 0 || stall_kb >= cfg->d / 64 || wait_limit_us == 0 || wait_limit_us > 4000000u)
+        return MOE_ERR_INVALID_ARG;
+    const int64_t rows = max_rows_of(cfg);
+    if (rows == 0 || !ws || !aligned16(ws) || !xp || !expert_offsets || !w_up || !h ||
+        !aligned16(xp) || !aligned4(expert_offsets) || !aligned16(w_up) || !aligned16(h))
+        return MOE_ERR_INVALID_ARG;
+    GemmArgs g;
+    g.A = xp;
+    g.B = w_up;
+    g.out = h;
+    g.offsets = expert_offsets;
+    g.rows_cap = rows;
+    g.m_rows = 0;
+    g.G = cfg->E;
+    g.N = cfg->d_ff;
+    g.K = cfg->d;
+    g.epi = cfg->act == MOE_ACT_SWIGLU ? EPI_SWIGLU : EPI_GELU;
+    g.dtype = cfg->act_dtype;
+    g.status = at<uint32_t>(ws, layout_of(cfg).status);
+    g.stall_kb = stall_kb;
+    g.wait_ns = (uint64_t)wait_limit_us * 1000ull;
+    if (gemm_tc_supported(g) != 0) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(launch_gemm_tc(g, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* expert_offsets,

@@ -9,34 +9,38 @@
 // are the virtual ranks (expert e on rank e / (E/R)); the send counts the
 // all-to-all would have used are reported as rank_splits.
 //
-// Two kernels:
-//   count_kernel  -- per-expert loads (block histogram in shared memory, one
-//                    global atomic per expert and block); the last block to
-//                    finish turns them into capacity-clipped counts and the
-//                    expert offsets.  It also clears the scan state used by
-//                    place_kernel.
-//   place_kernel  -- 32, 64 or 128 tokens per block, blocks ordered by an atomic ticket.
-//                    A per-expert decoupled look-back over the blocks gives
-//                    each assignment its position among the same expert's
-//                    assignments in token order; the position decides
-//                    keep/drop against C and the row; then the block copies
-//                    its tokens' rows with 16-byte vectors.
-// The look-back only ever waits on blocks that drew an earlier ticket, which
-// are already running, and every wait is bounded (status word on timeout).
+// The tokens are cut into blocks of TB = 32, 64 or 128 tokens, and three
+// kernels run on them:
+//   count_kernel  -- one CTA per token block: its per-expert assignment counts
+//                    (shared-memory histogram), stored expert-major.
+//   scan_kernel   -- one CTA per expert: the exclusive prefix of that expert's
+//                    counts over the blocks (its assignments in earlier
+//                    blocks, i.e. in earlier tokens) and its total.
+//   place_kernel  -- one CTA per token block: the capacity-clipped totals give
+//                    the expert offsets (every CTA scans the E totals; CTA 0
+//                    stores the metadata outputs); an assignment's position
+//                    among its expert's assignments in token order is the
+//                    block's prefix plus its rank inside the block, which
+//                    decides keep/drop against C and the row; then the block
+//                    copies its tokens' rows with 16-byte vectors.
+// Nothing waits on another CTA: the order comes from the scan, not from a
+// look-back chain, so no kernel here spins.  scan_kernel and place_kernel are
+// programmatic dependents of the kernel before them: each starts while its
+// predecessor runs, does what does not need the predecessor's results (place:
+// the per-block bitmaps), and waits (griddepcontrol.wait) before reading them.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 namespace {
 
-constexpr int kPlaceTokens = 32;  // smallest place_kernel block: one warp's worth of tokens
+constexpr int kPlaceTokens = 32;  // smallest token block: one warp's worth of tokens
 constexpr int kPlaceThreads = 256;
 constexpr int kMaxRanks = 32;     // virtual ranks supported by the send-count accumulator
-constexpr uint64_t kFlagAgg = 1ull << 32;   // descriptor holds the block's own count
-constexpr uint64_t kFlagIncl = 2ull << 32;  // descriptor holds the inclusive prefix
+constexpr int kScanThreads = 256, kScanItems = 4;
 
 // Block-wide exclusive scan of one int per thread (blockDim.x <= 1024).
-__device__ int block_exclusive_scan(int v, int* scratch /* >= 32 ints */, int* total) {
+__device__ int block_exclusive_scan(int v, int* scratch /* >= 33 ints */, int* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = v;
 #pragma unroll
@@ -65,84 +69,97 @@ __device__ int block_exclusive_scan(int v, int* scratch /* >= 32 ints */, int* t
     return out;
 }
 
-__global__ void __launch_bounds__(256) count_kernel(DispatchArgs a, int64_t n_desc) {
-    __shared__ int hist[256];
-    __shared__ int scratch[33];
-    __shared__ bool last;
+// Programmatic dependent launch: let the next kernel on the stream start, and
+// (in that kernel) wait for this grid's completion and memory.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Per-block, per-expert assignment counts: hist[e * nblk + b].
+__global__ void __launch_bounds__(256) count_kernel(DispatchArgs a, int tb, int nblk) {
+    __shared__ int h[256];
     const int tid = threadIdx.x;
-    for (int e = tid; e < a.E; e += blockDim.x) hist[e] = 0;
-    // clear the look-back descriptors and the split accumulator for place_kernel
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + tid; i < n_desc;
-         i += (int64_t)gridDim.x * blockDim.x)
-        a.desc[i] = 0ull;
-    int32_t* splits = a.rank_splits ? a.rank_splits : a.splits_acc;
-    if (blockIdx.x == 0)
+    const int b = blockIdx.x;
+    pdl_launch_dependents();
+    for (int e = tid; e < a.E; e += blockDim.x) h[e] = 0;
+    if (b == 0) {
+        int32_t* splits = a.rank_splits ? a.rank_splits : a.splits_acc;
         for (int i = tid; i < a.R * a.R; i += blockDim.x) splits[i] = 0;
+    }
     __syncthreads();
-    const int64_t n = a.T * a.k;
+    const int64_t t0 = (int64_t)b * tb;
+    const int64_t t1 = t0 + tb < a.T ? t0 + tb : a.T;
+    const int64_t n = (t1 - t0) * a.k;
+    const int32_t* idx = a.idx + t0 * a.k;
     bool bad = false;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + tid; i < n;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int e = a.idx[i];
+    for (int64_t i = tid; i < n; i += blockDim.x) {
+        const int e = idx[i];
         if ((unsigned)e < (unsigned)a.E)
-            atomicAdd(&hist[e], 1);
+            atomicAdd(&h[e], 1);
         else
             bad = true;
     }
     if (bad) atomicOr(a.status, MOE_DEV_BAD_INDEX);
     __syncthreads();
-    for (int e = tid; e < a.E; e += blockDim.x)
-        if (hist[e]) atomicAdd(&a.counts[e], hist[e]);
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) last = atomicAdd(a.done, 1u) == gridDim.x - 1;
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    // Last block: capacity-clipped counts, offsets, per-rank receive counts.
-    int cnt = 0, kept = 0;
-    if (tid < a.E) {
-        cnt = atomicAdd(&a.counts[tid], 0);
-        kept = (a.C >= 0 && cnt > a.C) ? (int)a.C : cnt;
-        a.expert_counts[tid] = cnt;
+    if (b < nblk)
+        for (int e = tid; e < a.E; e += blockDim.x) a.hist[(int64_t)e * nblk + b] = h[e];
+}
+
+// Expert e = blockIdx.x: prefix[e * nblk + b] = sum of hist[e * nblk + j] over
+// j < b, and totals[e] = the sum over all blocks.
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(DispatchArgs a, int nblk) {
+    __shared__ int scratch[33];
+    pdl_launch_dependents();
+    pdl_wait();  // count_kernel's histograms
+    const int e = blockIdx.x;
+    const int32_t* in = a.hist + (int64_t)e * nblk;
+    int32_t* out = a.prefix + (int64_t)e * nblk;
+    int carry = 0;
+    for (int base = 0; base < nblk; base += kScanThreads * kScanItems) {
+        const int i0 = base + threadIdx.x * kScanItems;
+        int v[kScanItems];
+        int sum = 0;
+#pragma unroll
+        for (int j = 0; j < kScanItems; ++j) {
+            v[j] = i0 + j < nblk ? in[i0 + j] : 0;
+            sum += v[j];
+        }
+        int total = 0;
+        int run = carry + block_exclusive_scan(sum, scratch, &total);
+#pragma unroll
+        for (int j = 0; j < kScanItems; ++j) {
+            if (i0 + j < nblk) out[i0 + j] = run;
+            run += v[j];
+        }
+        carry += total;
     }
-    int total = 0;
-    const int off = block_exclusive_scan(tid < a.E ? kept : 0, scratch, &total);
-    if (tid < a.E) a.expert_offsets[tid] = off;
-    if (tid == 0) {
-        a.expert_offsets[a.E] = total;
-        a.n_dropped[0] = (int32_t)(n - total);
-    }
-    __syncthreads();
-    // rank r owns experts [r*E/R, (r+1)*E/R): a difference of offsets
-    const int per = a.E / a.R;
-    for (int r = tid; r < a.R; r += blockDim.x)
-        a.rank_counts[r] = a.expert_offsets[(r + 1) * per] - a.expert_offsets[r * per];
+    if (threadIdx.x == 0) a.totals[e] = carry;
 }
 
 // SUB sub-tiles of 32 tokens per block (TB = 32*SUB tokens): warp s < SUB
 // ranks sub-tile s with per-expert lane bitmaps; larger blocks amortise the
-// block's fixed costs (ticket, look-back, barriers) over more row copies.
+// block's fixed costs (offsets, barriers) over more row copies.
 template <typename T, int SUB>
-__global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
+__global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a, int nblk) {
     constexpr int TB = 32 * SUB;
     __shared__ uint32_t bits[SUB][256];  // per sub-tile and expert: lanes (tokens) that chose it
     __shared__ int wpre[SUB][256];       // per sub-tile and expert: assignments in earlier sub-tiles
     __shared__ int prefix[256];          // per expert: assignments in earlier blocks
-    __shared__ int offs[256];
+    __shared__ int offs[257];
     __shared__ int rows[TB][8];
     __shared__ int split_acc[kMaxRanks * kMaxRanks];  // [src][dst] kept rows of this block
-    __shared__ uint32_t blk_s;
+    __shared__ int scratch[33];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) blk_s = atomicAdd(a.ticket, 1u);
+    const int blk = blockIdx.x;
+    // blockIdx.y: column chunk of the row copies; chunk 0 also writes the metadata
+    const bool chunk0 = blockIdx.y == 0;
     for (int e = tid; e < a.E; e += kPlaceThreads) {
 #pragma unroll
         for (int sb = 0; sb < SUB; ++sb) bits[sb][e] = 0u;
-        offs[e] = a.expert_offsets[e];
     }
     for (int i = tid; i < a.R * a.R; i += kPlaceThreads) split_acc[i] = 0;
     __syncthreads();
-    const uint32_t blk = blk_s;
     const int64_t t0 = (int64_t)blk * TB;
     const int64_t t = t0 + warp * 32 + lane;  // meaningful for warps < SUB
     const bool live = warp < SUB && t < a.T;
@@ -162,8 +179,6 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
         }
     }
     __syncthreads();
-    // Per-expert decoupled look-back over the preceding blocks.
-    uint64_t* desc = a.desc + (int64_t)blk * a.E;
     for (int e = tid; e < a.E; e += kPlaceThreads) {
         int own = 0;
 #pragma unroll
@@ -171,37 +186,42 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
             wpre[sb][e] = own;
             own += __popc(bits[sb][e]);
         }
-        const bool publish = (int)blk != a.stall_block;
-        if (blk == 0) {
-            if (publish) st_relaxed_u64(desc + e, kFlagIncl | (uint32_t)own);
-            prefix[e] = 0;
-            continue;
+    }
+    // scan_kernel's prefixes and totals from here on
+    pdl_wait();
+    {
+        const int e = tid;  // E <= 256 = blockDim.x
+        int total = 0, kept = 0, pre = 0;
+        if (e < a.E) {
+            total = a.totals[e];
+            kept = (a.C >= 0 && total > a.C) ? (int)a.C : total;
+            pre = blk < nblk ? a.prefix[(int64_t)e * nblk + blk] : 0;
         }
-        if (publish) st_relaxed_u64(desc + e, kFlagAgg | (uint32_t)own);
-        int excl = 0;
-        int64_t j = (int64_t)blk - 1;
-        uint64_t t_start = 0;
-        while (j >= 0) {
-            const uint64_t v = ld_relaxed_u64(a.desc + j * a.E + e);
-            const uint64_t flag = v & (3ull << 32);
-            if (flag == 0) {
-                if (t_start == 0) t_start = globaltimer_ns();
-                else if (globaltimer_ns() - t_start > a.wait_ns) {
-                    atomicOr(a.status, MOE_DEV_LOOKBACK_TIMEOUT);
-                    break;
-                }
-                __nanosleep(32);
-                continue;
+        int sum = 0;
+        const int off = block_exclusive_scan(kept, scratch, &sum);
+        if (e < a.E) {
+            offs[e] = off;
+            prefix[e] = pre;
+            if (blk == 0 && chunk0) {
+                a.expert_counts[e] = total;
+                a.expert_offsets[e] = off;
             }
-            excl += (int)(uint32_t)v;
-            if (flag == kFlagIncl) break;
-            --j;
-            t_start = 0;
         }
-        prefix[e] = excl;
-        if (publish) st_relaxed_u64(desc + e, kFlagIncl | (uint32_t)(excl + own));
+        if (tid == 0) {
+            offs[a.E] = sum;
+            if (blk == 0 && chunk0) {
+                a.expert_offsets[a.E] = sum;
+                a.n_dropped[0] = (int32_t)(a.T * a.k - sum);
+            }
+        }
     }
     __syncthreads();
+    if (blk == 0 && chunk0) {
+        // rank r owns experts [r*E/R, (r+1)*E/R): a difference of offsets
+        const int per = a.E / a.R;
+        for (int r = tid; r < a.R; r += kPlaceThreads)
+            a.rank_counts[r] = offs[(r + 1) * per] - offs[r * per];
+    }
     // Positions, keep/drop, rows.
     if (warp < SUB) {
         const int per = a.E / a.R;
@@ -216,17 +236,19 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
                 const int pos = prefix[e] + wpre[warp][e] + __popc(bits[warp][e] & lanemask_lt());
                 if (a.C < 0 || pos < a.C) {
                     row = offs[e] + pos;
-                    a.row_token[row] = (int32_t)t;
-                    atomicAdd(&split_acc[src * a.R + e / per], 1);
+                    if (chunk0) {
+                        a.row_token[row] = (int32_t)t;
+                        atomicAdd(&split_acc[src * a.R + e / per], 1);
+                    }
                 }
             }
-            if (live) a.slot_row[t * a.k + j] = row;
+            if (live && chunk0) a.slot_row[t * a.k + j] = row;
             rows[warp * 32 + lane][j] = row;
         }
     }
     __syncthreads();
     // This block's send counts -> rank_splits (a few global atomics per block).
-    {
+    if (chunk0) {
         int32_t* splits = a.rank_splits ? a.rank_splits : a.splits_acc;
         for (int i = tid; i < a.R * a.R; i += kPlaceThreads) {
             const int v = split_acc[i];
@@ -234,16 +256,20 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
         }
     }
     // Row copies: x[t] -> xp[row] for every kept row, 16-byte vectors, eight
-    // loads in flight per thread.  Rows of >= 256 chunks (4 KB): one warp per
-    // token, lanes along the row.  Shorter rows: the block's 256 threads walk
-    // the (token, chunk) space of its TB rows together, each stepping its pair
-    // by 256 chunks, so short rows keep as many bytes in flight as long ones.
+    // loads in flight per thread; this CTA copies the row columns of its chunk,
+    // 16-byte vectors [vlo, vhi).  Chunks of >= 256 vectors (4 KB): one warp per
+    // token, lanes along the row.  Narrower chunks: the block's 256 threads walk
+    // the (token, vector) space of its TB rows together, each stepping its pair
+    // by 256 vectors, so short rows keep as many bytes in flight as long ones.
     const int nvec = a.d * (int)sizeof(T) / 16;
+    const int vlo = (int)((int64_t)blockIdx.y * nvec / gridDim.y);
+    const int vhi = (int)((int64_t)(blockIdx.y + 1) * nvec / gridDim.y);
+    const int w = vhi - vlo;
     const int64_t row_bytes = (int64_t)a.d * sizeof(T);
-    const char* x = static_cast<const char*>(a.x);
-    char* xp = static_cast<char*>(a.xp);
+    const char* x = static_cast<const char*>(a.x) + (int64_t)vlo * 16;
+    char* xp = static_cast<char*>(a.xp) + (int64_t)vlo * 16;
     const int ntok = (int)((a.T - t0) < TB ? (a.T - t0) : TB);
-    if (nvec >= kPlaceThreads) {
+    if (w >= kPlaceThreads) {
         for (int tok = warp; tok < ntok; tok += kPlaceThreads / 32) {
             int r[8];
             int nk = 0;
@@ -254,15 +280,15 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
             }
             if (nk == 0) continue;
             const char* src = x + (t0 + tok) * row_bytes;
-            for (int c0 = lane; c0 < nvec; c0 += 256) {
+            for (int c0 = lane; c0 < w; c0 += 256) {
                 uint4 v[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    if (c0 + 32 * u < nvec) v[u] = ld_nc_v4(src + (int64_t)(c0 + 32 * u) * 16);
+                    if (c0 + 32 * u < w) v[u] = ld_nc_v4(src + (int64_t)(c0 + 32 * u) * 16);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int c = c0 + 32 * u;
-                    if (c >= nvec) break;
+                    if (c >= w) break;
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         if (r[j] >= 0) st_v4(xp + (int64_t)r[j] * row_bytes + (int64_t)c * 16, v[u]);
@@ -271,7 +297,7 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
         }
         return;
     }
-    int tok = tid / nvec, c = tid - (tid / nvec) * nvec;
+    int tok = tid / w, c = tid - (tid / w) * w;
     while (tok < ntok) {
         uint4 v[8];
         int vt[8], vc[8];
@@ -281,8 +307,8 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a) {
             vc[u] = c;
             if (tok < ntok) v[u] = ld_nc_v4(x + (t0 + tok) * row_bytes + (int64_t)c * 16);
             c += kPlaceThreads;
-            while (c >= nvec) {
-                c -= nvec;
+            while (c >= w) {
+                c -= w;
                 ++tok;
             }
         }
@@ -315,35 +341,61 @@ int place_sub(int64_t T) {
     return 1;
 }
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel on the stream runs, and waits for it in device code.
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kernel, dim3 grid, unsigned block, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Column chunks per token block: enough CTAs for about four per SM, chunks of
+// at least 64 vectors (1 KB).
+int place_chunks(const DispatchArgs& a, int nblk, int elem_bytes) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (nblk <= 0) return 1;
+    const int nvec = a.d * elem_bytes / 16;
+    int S = (int)((4LL * sms + nblk - 1) / nblk);
+    const int max_s = nvec / 64 > 1 ? nvec / 64 : 1;
+    if (S > max_s) S = max_s;
+    return S < 1 ? 1 : S;
+}
+
 template <typename T>
-void launch_place(const DispatchArgs& a, int sub, int64_t nblk, cudaStream_t s) {
-    if (sub == 4)
-        place_kernel<T, 4><<<(unsigned)nblk, kPlaceThreads, 0, s>>>(a);
-    else if (sub == 2)
-        place_kernel<T, 2><<<(unsigned)nblk, kPlaceThreads, 0, s>>>(a);
-    else
-        place_kernel<T, 1><<<(unsigned)nblk, kPlaceThreads, 0, s>>>(a);
+cudaError_t launch_place(const DispatchArgs& a, int sub, int nblk, cudaStream_t s) {
+    // one CTA writes the metadata when T = 0
+    const dim3 grid(nblk > 0 ? (unsigned)nblk : 1u, (unsigned)place_chunks(a, nblk, (int)sizeof(T)));
+    if (sub == 4) return launch_pdl(place_kernel<T, 4>, grid, kPlaceThreads, s, a, nblk);
+    if (sub == 2) return launch_pdl(place_kernel<T, 2>, grid, kPlaceThreads, s, a, nblk);
+    return launch_pdl(place_kernel<T, 1>, grid, kPlaceThreads, s, a, nblk);
 }
 }  // namespace
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
+    if (a.E < 1 || a.E > 256 || a.k < 1 || a.k > 8 || a.R < 1 || a.R > kMaxRanks)
+        return cudaErrorInvalidValue;
     const int sub = place_sub(a.T);
-    const int64_t nblk = (a.T + 32 * sub - 1) / (32 * sub);
-    const int64_t n_desc = nblk * a.E;
-    const int64_t n = a.T * a.k;
-    int64_t cb = (n + 256 * 8 - 1) / (256 * 8);
-    const int64_t cb_desc = (n_desc + 256 * 4 - 1) / (256 * 4);
-    if (cb_desc > cb) cb = cb_desc;
-    if (cb < 1) cb = 1;
-    if (cb > 296) cb = 296;
-    count_kernel<<<(unsigned)cb, 256, 0, s>>>(a, n_desc);
+    const int64_t nblk64 = (a.T + 32 * sub - 1) / (32 * sub);
+    if (nblk64 > (1 << 30)) return cudaErrorInvalidValue;
+    const int nblk = (int)nblk64;
+    count_kernel<<<nblk > 0 ? (unsigned)nblk : 1u, 256, 0, s>>>(a, 32 * sub, nblk);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || nblk == 0) return e;
-    if (a.dtype == MOE_DTYPE_F32)
-        launch_place<float>(a, sub, nblk, s);
-    else
-        launch_place<__nv_bfloat16>(a, sub, nblk, s);
-    return cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(scan_kernel, dim3((unsigned)a.E), kScanThreads, s, a, nblk);
+    if (e != cudaSuccess) return e;
+    if (a.dtype == MOE_DTYPE_F32) return launch_place<float>(a, sub, nblk, s);
+    return launch_place<__nv_bfloat16>(a, sub, nblk, s);
 }
 
 }  // namespace moe

@@ -6,16 +6,16 @@
 // device memory was all reserved by another allocator at start-up.  They have
 // no way to provide the workspace moe_dispatch needs.  This entry point runs
 // the very same dispatch kernels, but points their scratch state (status
-// word, block ticket, finish counter, per-expert counts, look-back
-// descriptors, send-count accumulator) at the file-scope device array below.
+// word, per-expert totals, per-block counts and prefixes, send-count
+// accumulator) at the file-scope device array below.
 //
 // The array is a static __device__ object: every GPU that loads the library
 // holds kScratchBytes of it until the process exits.  Host code cannot use
 // the array's name as a device address (in host code it names a host-side
 // stand-in), so the first call on each device, with that device current,
 // looks the address up with cudaGetSymbolAddress and caches it.  Every call
-// shares the one array and finds the previous call's contents in it; each
-// call clears the parts that must start at zero before its kernels run.
+// shares the one array and finds the previous call's contents in it; the
+// kernels write every part they read before reading it.
 // Calls that overlap on the GPU (different streams, or several host threads
 // without ordering) race on the array.
 #include <mutex>
@@ -54,18 +54,18 @@ cudaError_t scratch_address(void** out) {
     return cudaSuccess;
 }
 
-// Scratch layout: status, ticket, finish counter | counts [E] | look-back
-// descriptors [ceil(T/32), E] | send-count accumulator [R, R].
+// Scratch layout: status | totals [E] | per-block counts [E, ceil(T/32)] |
+// per-block prefixes [E, ceil(T/32)] | send-count accumulator [R, R].
 struct NoAllocLayout {
-    size_t counts, desc, splits, clear, total;
+    size_t totals, hist, prefix, splits, total;
 };
 
 NoAllocLayout noalloc_layout(const moe_config* c) {
     NoAllocLayout L;
-    L.counts = kAlignNA;
-    L.desc = up256(L.counts + (size_t)c->E * 4);
-    L.clear = L.desc;
-    L.splits = up256(L.desc + (size_t)dispatch_blocks(c->T) * c->E * 8);
+    L.totals = kAlignNA;
+    L.hist = up256(L.totals + (size_t)c->E * 4);
+    L.prefix = up256(L.hist + (size_t)dispatch_blocks(c->T) * c->E * 4);
+    L.splits = up256(L.prefix + (size_t)dispatch_blocks(c->T) * c->E * 4);
     L.total = up256(L.splits + (size_t)c->R * c->R * 4);
     return L;
 }
@@ -99,8 +99,6 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x,
     if (scratch_address(&base) != cudaSuccess) return MOE_ERR_CUDA;
     char* s = static_cast<char*>(base);
     cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
-    // status word, ticket, finish counter and per-expert counts start at zero
-    if (cudaMemsetAsync(s, 0, L.clear, strm) != cudaSuccess) return MOE_ERR_CUDA;
 
     DispatchArgs a;
     a.x = x;
@@ -114,10 +112,9 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x,
     a.rank_splits = rank_splits;
     a.n_dropped = n_dropped;
     a.status = device_status ? device_status : reinterpret_cast<uint32_t*>(s);
-    a.ticket = reinterpret_cast<uint32_t*>(s + 4);
-    a.done = reinterpret_cast<uint32_t*>(s + 8);
-    a.counts = reinterpret_cast<int32_t*>(s + L.counts);
-    a.desc = reinterpret_cast<uint64_t*>(s + L.desc);
+    a.totals = reinterpret_cast<int32_t*>(s + L.totals);
+    a.hist = reinterpret_cast<int32_t*>(s + L.hist);
+    a.prefix = reinterpret_cast<int32_t*>(s + L.prefix);
     a.splits_acc = reinterpret_cast<int32_t*>(s + L.splits);
     a.T = cfg->T;
     a.d = cfg->d;
@@ -126,7 +123,5 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x,
     a.R = cfg->R;
     a.dtype = cfg->act_dtype;
     a.C = moe_capacity(cfg);
-    a.stall_block = -1;
-    a.wait_ns = kWaitTimeoutNs;
     return launch_dispatch(a, strm) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -40,8 +40,8 @@
 // matrix, out[g] = A[:, K_g] . B[:, K_g]^T, where A [M, K] and B [N, K] are
 // activations transposed so that each group's rows form a 64-aligned range
 // K_g of the contraction dimension.  Tiles run over (group, n-tile, m-tile)
-// as above, but every tile's K loop covers only its group's K blocks; groups
-// with no rows have no tiles (the caller zeroes their output).
+// as above, but every tile's K loop covers only its group's K blocks; the
+// tiles of a group without rows issue no MMA and store zeros.
 //
 // Every mbarrier wait is bounded by %globaltimer: on timeout the kernel sets
 // MOE_DEV_GEMM_TIMEOUT, raises an abort flag seen by the other roles, drains
@@ -79,6 +79,8 @@ struct TcParams {
     int n_tiles;
     int out_cols;  // output columns per tile (128 SwiGLU, 256 otherwise)
     int kg_M;      // K-grouped mode: rows of each group's output matrix
+    int stall_kb;  // failure-detection hook (-1: off)
+    uint64_t wait_ns;
     __nv_bfloat16* out;
     uint32_t* status;
 };
@@ -247,23 +249,31 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
                 const TileInfo ti = decode_tile<KG>(tile, p.G, tstart, mt, rowoff, grows, p);
                 for (int kb = 0; kb < ti.nkb; ++kb) {
-                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT)) break;
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT, p.wait_ns)) break;
                     const uint32_t fb = full0 + 8 * stage;
-                    mbar_expect_tx(fb, STAGE_BYTES);
                     const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
                     const uint32_t sb = sa + A_STAGE;
                     const int k0 = (ti.kb0 + kb) * BK;
-                    tma_load_2d(sa, &tmA, k0, ti.row0, fb);
-                    if (KG) {
+                    if (kb == p.stall_kb && tile == 0) {
+                        // test hook: leave this stage unfilled; the MMA issuer's wait runs out
+                    } else if (KG) {
+                        mbar_expect_tx(fb, STAGE_BYTES);
+                        tma_load_2d(sa, &tmA, k0, ti.row0, fb);
                         tma_load_3d(sb, &tmB, k0, ti.n_tile * BN, 0, fb);
                     } else if (BMN) {
+                        mbar_expect_tx(fb, STAGE_BYTES);
+                        tma_load_2d(sa, &tmA, k0, ti.row0, fb);
 #pragma unroll
                         for (int c = 0; c < BN / 64; ++c)
                             tma_load_3d(sb + c * MN_CHUNK, &tmB, ti.n_tile * BN + c * 64, k0, ti.g, fb);
                     } else if (p.epi == EPI_SWIGLU) {
+                        mbar_expect_tx(fb, STAGE_BYTES);
+                        tma_load_2d(sa, &tmA, k0, ti.row0, fb);
                         tma_load_3d(sb, &tmB, k0, ti.n_tile * 128, ti.g, fb);
                         tma_load_3d(sb + B_STAGE / 2, &tmB, k0, p.N + ti.n_tile * 128, ti.g, fb);
                     } else {
+                        mbar_expect_tx(fb, STAGE_BYTES);
+                        tma_load_2d(sa, &tmA, k0, ti.row0, fb);
                         tma_load_3d(sb, &tmB, k0, ti.n_tile * BN, ti.g, fb);
                     }
                     if (++stage == STAGES) {
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT)) {
+                if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -291,7 +301,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int nkb = KG ? decode_tile<KG>(tile, p.G, tstart, mt, rowoff, grows, p).nkb
                                    : p.num_kb;
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT)) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -338,7 +348,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             __nv_bfloat16* obase = KG ? p.out + (int64_t)ti.g * p.kg_M * p.N : p.out;
             // every lane waits, then the warp agrees, so the .sync.aligned TMEM loads
             // below always run converged
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(accf0 + 8 * acc, acc_phase, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT));
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(accf0 + 8 * acc, acc_phase, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT, p.wait_ns));
             if (!ok) break;
             fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
@@ -456,6 +466,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
     p.out = static_cast<__nv_bfloat16*>(a.out);
     p.status = a.status;
     p.kg_M = kg ? (int)rows_cap : 0;
+    p.stall_kb = a.stall_kb;
+    p.wait_ns = a.wait_ns ? a.wait_ns : kWaitTimeoutNs;
 
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);

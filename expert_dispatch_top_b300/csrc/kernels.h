@@ -36,19 +36,16 @@ struct DispatchArgs {
     int32_t* n_dropped;
     // workspace pieces
     uint32_t* status;
-    uint32_t* ticket;
-    uint32_t* done;
-    int32_t* counts;     // [E] accumulation
-    uint64_t* desc;      // [n_blk, E] lookback descriptors
-    int32_t* splits_acc; // [R*R] accumulation (used when rank_splits is null)
+    int32_t* totals;      // [E] assignments per expert (before capacity)
+    int32_t* hist;        // [E, blocks] per-block assignment counts (blocks <= dispatch_blocks(T))
+    int32_t* prefix;      // [E, blocks] exclusive per-expert prefixes over the blocks
+    int32_t* splits_acc;  // [R*R] accumulation (used when rank_splits is null)
     int64_t T;
     int d, E, k, R, dtype;
-    int64_t C;           // < 0: no limit
-    int stall_block;     // test hook: this block never publishes its look-back state (-1: none)
-    uint64_t wait_ns;    // bound on each look-back wait
+    int64_t C;            // < 0: no limit
 };
-// Header bytes of the workspace that dispatch clears before it runs.
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
+// Upper bound on the token blocks of one dispatch (sizes hist and prefix).
 int64_t dispatch_blocks(int64_t T);
 
 struct CombineArgs {
@@ -94,6 +91,10 @@ struct GemmArgs {
     // MN-major B (tensor-core kernel, no epilogue): B is [G, K, N] row-major, i.e.
     // out = A . B[g] with the weights read as stored.
     int b_mn = 0;
+    // Failure-detection hook: CTA 0 never loads K block stall_kb of its first
+    // tile (-1: off); wait_ns bounds every pipeline wait (0: the 4 s default).
+    int stall_kb = -1;
+    uint64_t wait_ns = 0;
 };
 cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s);

@@ -47,7 +47,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase of parity `parity`.  False on timeout (the
 // status bit is set and the abort flag raised) or when another role aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* status, uint32_t timeout_bit) {
+                                          uint32_t* status, uint32_t timeout_bit,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
 #pragma unroll 1
     for (int i = 0; i < 128; ++i)
         if (mbar_try_wait(bar, parity)) return true;
@@ -56,7 +57,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             atomicOr(status, timeout_bit);
             *abort_flag = 1;
             return false;
@@ -75,6 +76,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
+}
+
+// L2 prefetch of one box of a 2-D tensor map: no shared memory, no barrier;
+// boxes outside the tensor are ignored.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* tm, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,

@@ -61,7 +61,7 @@ enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
 enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1, MOE_ACT_IDENTITY = 2 };
 
 /* Bits of the device status word (first 4 bytes of the workspace). */
-#define MOE_DEV_LOOKBACK_TIMEOUT 0x1u /* dispatch scan waited too long on a predecessor */
+/* 0x1u: unused */
 #define MOE_DEV_GEMM_TIMEOUT 0x2u     /* expert GEMM pipeline wait gave up */
 #define MOE_DEV_BAD_INDEX 0x4u        /* an expert index outside [0, E) reached dispatch */
 
@@ -174,20 +174,21 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
                         int32_t* n_dropped, void* ws, moe_stream_t stream);
 
 /*
- * Failure-detection test hook (no counterpart on the pages): moe_dispatch with
- * one scan block that never publishes its look-back state (stall_block >= 0,
- * in ticket order) and a bound of wait_limit_us (1..4,000,000) on every
- * look-back wait.  The block after it waits, gives up at the bound, sets
- * MOE_DEV_LOOKBACK_TIMEOUT in the status word and carries on, so every kernel
- * returns and the context stays usable; the dispatch outputs are then
- * meaningless.  moe_dispatch itself uses a 4 s bound and never stalls.
+ * Failure-detection test hook (no counterpart on the pages): the up
+ * projection of moe_expert_ffn (bf16 tensor-core path; h = act(xp . W_up^T))
+ * with one pipeline stage left unfilled.  CTA 0 never loads K block stall_kb
+ * (0 <= stall_kb < d/64) of its first tile, so the MMA issuer's wait on that
+ * stage runs out after wait_limit_us (1..4,000,000; every pipeline wait of
+ * the launch gets this bound).  The kernel then sets MOE_DEV_GEMM_TIMEOUT in
+ * the status word, raises its abort flag, drains the MMAs it issued, frees its
+ * tensor memory and returns, so the context stays usable; h is then
+ * meaningless.  moe_expert_ffn itself uses a 4 s bound and never stalls.
+ * MOE_ERR_UNSUPPORTED for fp32 or IDENTITY configs.
  */
-moe_status moe_test_dispatch_stall(const moe_config* cfg, const void* x, const int32_t* topk_idx,
-                                   void* xp, int32_t* row_token, int32_t* slot_row,
-                                   int32_t* expert_counts, int32_t* expert_offsets,
-                                   int32_t* rank_counts, int32_t* rank_splits, int32_t* n_dropped,
-                                   int32_t stall_block, uint32_t wait_limit_us, void* ws,
-                                   moe_stream_t stream);
+moe_status moe_test_expert_ffn_stall(const moe_config* cfg, const void* xp,
+                                     const int32_t* expert_offsets, const void* w_up, void* h,
+                                     int32_t stall_kb, uint32_t wait_limit_us, void* ws,
+                                     moe_stream_t stream);
 
 /*
  * moe_dispatch without a workspace, for callers that cannot allocate device

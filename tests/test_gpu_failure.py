@@ -1,7 +1,8 @@
-"""Failure detection without a GPU fault: a scan block that never publishes
-makes its successor's bounded look-back wait run out.  The kernel records
-MOE_DEV_LOOKBACK_TIMEOUT in the status word and returns; the host reads the
-status, and the next normal dispatch on the same context is correct."""
+"""Failure detection without a GPU fault: a pipeline stage of the expert
+GEMM that is never loaded makes the MMA issuer's bounded wait run out.  The
+kernel records MOE_DEV_GEMM_TIMEOUT in the status word, raises its abort flag,
+drains its MMAs, frees tensor memory and returns; the host reads the status,
+and the next normal FFN call on the same context and workspace is correct."""
 import time
 
 import pytest
@@ -10,40 +11,62 @@ import torch
 import expert_dispatch_top_b300 as moe
 import moe_workloads as W
 import oracle
-from gpu_util import DEV, run_dispatch
+from gpu_util import DEV, assert_rows_close
 
 pytestmark = pytest.mark.gpu
 
 
-def test_lookback_wait_times_out_and_context_survives():
-    T, d, E, k, R = 256, 64, 8, 2, 4          # 8 scan blocks of 32 tokens
-    cfg = moe.make_config(T, d, E, k, R, 0, 0, "bf16", "softmax", True, 0.0, 0, "identity")
-    idx = W.random_topk(T, E, k, seed=2).to(DEV)
-    x = W._grid_int((T, d), -8, 8, 8.0, W._gen(2, DEV), DEV).to(torch.bfloat16)
-    rows = moe.moe_max_rows(cfg)
-    i32 = dict(dtype=torch.int32, device=DEV)
-    bufs = [torch.zeros((rows, d), dtype=torch.bfloat16, device=DEV), torch.zeros(rows, **i32),
-            torch.zeros((T, k), **i32), torch.zeros(E, **i32), torch.zeros(E + 1, **i32),
-            torch.zeros(R, **i32), torch.zeros((R, R), **i32), torch.zeros(1, **i32)]
+def _case(counts, d, f, act, seed):
+    E = len(counts)
+    offs = torch.zeros(E + 1, dtype=torch.int32)
+    offs[1:] = torch.cumsum(torch.tensor(counts, dtype=torch.int32), 0)
+    N = int(offs[-1])
+    rows_up = 2 * f if act == "swiglu" else f
+    g = W._gen(seed, "cpu")
+    w_up = W._grid_normal((E, rows_up, d), 0.08, 2.0 ** -9, 0.125, g, "cpu").to(torch.bfloat16)
+    w_dn = W._grid_normal((E, d, f), 0.08, 2.0 ** -9, 0.125, g, "cpu").to(torch.bfloat16)
+    xp = W._grid_int((N, d), -8, 8, 8.0, g, "cpu").to(torch.bfloat16)
+    cfg = moe.make_config(N, d, E, 1, 1, f, 0, "bf16", "softmax", True, 0.0, 0, act)
+    return cfg, offs, w_up, w_dn, xp
+
+
+@pytest.mark.parametrize("act", ["swiglu", "gelu"])
+def test_gemm_wait_times_out_and_context_survives(act):
+    counts, d, f = [300, 0, 200, 77], 256, 256
+    cfg, offs, w_up, w_dn, xp, = _case(counts, d, f, act, seed=5)
+    N = xp.shape[0]
+    xp_d, offs_d, wu_d, wd_d = xp.to(DEV), offs.to(DEV), w_up.to(DEV), w_dn.to(DEV)
+    h = torch.zeros((N, f), dtype=torch.bfloat16, device=DEV)
     ws = moe.alloc_workspace(cfg)
     t0 = time.time()
-    moe.moe_test_dispatch_stall(cfg, x, idx, *bufs, stall_block=1, wait_limit_us=20000, ws=ws)
+    moe.moe_test_expert_ffn_stall(cfg, xp_d, offs_d, wu_d, h, stall_kb=1, wait_limit_us=20000,
+                                  ws=ws)
     torch.cuda.synchronize()
     waited = time.time() - t0
     status = moe.moe_read_device_status(ws)
-    assert status & moe.MOE_DEV_LOOKBACK_TIMEOUT
+    assert status & moe.MOE_DEV_GEMM_TIMEOUT
     assert waited < 3.0                        # bounded by the 20 ms limit, not the default 4 s
-    # the same context and workspace still dispatch correctly
-    out = run_dispatch(cfg, x, idx.cpu(), ws=ws)
-    assert out["status"] == 0
-    ref = oracle.dispatch(idx.cpu(), E, R, -1)
-    assert torch.equal(out["slot_row"].cpu(), ref["slot_row"])
-    assert torch.equal(out["expert_offsets"].cpu(), ref["expert_offsets"])
+    assert moe.moe_read_device_status(ws) == 0  # reading clears it
+    # the same context and workspace still run the FFN correctly
+    yp = torch.full((N, d), 7.0, dtype=torch.bfloat16, device=DEV)
+    moe.moe_expert_ffn(cfg, xp_d, offs_d, wu_d, wd_d, h, yp, ws=ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    for e in range(len(counts)):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        if hi > lo:
+            ref = oracle.expert_ffn(xp[lo:hi], w_up[e], w_dn[e], act, f)
+            assert_rows_close(yp[lo:hi], ref, 2e-2)
 
 
 def test_stall_hook_rejects_bad_arguments():
-    cfg = moe.make_config(64, 64, 8, 2, 4, 0, 0, "bf16", "softmax", True, 0.0, 0, "identity")
+    cfg, offs, w_up, w_dn, xp = _case([64, 64], 128, 128, "gelu", seed=1)
+    ws = moe.alloc_workspace(cfg)
+    h = torch.zeros((128, 128), dtype=torch.bfloat16, device=DEV)
+    args = (xp.to(DEV), offs.to(DEV), w_up.to(DEV), h)
+    for kb, us in ((-1, 1000), (2, 1000), (0, 0), (0, 5000000)):   # d/64 = 2 K blocks
+        with pytest.raises(moe.MoeError):
+            moe.moe_test_expert_ffn_stall(cfg, *args, stall_kb=kb, wait_limit_us=us, ws=ws)
+    cfg32 = moe.make_config(128, 128, 2, 1, 1, 128, 0, "f32", "softmax", True, 0.0, 0, "gelu")
     with pytest.raises(moe.MoeError):
-        moe.moe_test_dispatch_stall(cfg, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000,
-                                    0x8000, None, 0x9000, stall_block=-1, wait_limit_us=10,
-                                    ws=0xa000)
+        moe.moe_test_expert_ffn_stall(cfg32, *args, stall_kb=0, wait_limit_us=1000, ws=ws)
