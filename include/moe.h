@@ -201,14 +201,14 @@ moe_status moe_test_expert_ffn_stall(const moe_config* cfg, const void* xp,
  *   the kernels OR their MOE_DEV_* bits into it; the caller zeroes it.
  *   Scratch state lives in one fixed 4 MiB device array inside the library
  *   (allocated when the library loads, on every GPU that loads it, until the
- *   process exits).  Limit: 256 + 4*E + 8*E*ceil(T/32) + 4*R*R bytes, each
- *   term rounded up to 256, must fit in 4 MiB (T*E <= ~16.7 million, e.g.
+ *   process exits).  Limit: 256 + 4*E + 2 * 4*E*ceil(T/32) + 4*R*R bytes,
+ *   each term rounded up to 256, must fit in 4 MiB (T*E <= ~16.7 million, e.g.
  *   T = 65536 with E = 128); larger shapes return MOE_ERR_INVALID_ARG before
  *   anything is enqueued.
  *   The first call on a device (with that device current) looks up the
  *   array's device address; make that first call before any stream capture.
- *   Every call shares the array and clears what must start at zero itself;
- *   calls that overlap on the GPU (other streams, unordered host threads)
+ *   Every call shares the array and writes each part of it before reading
+ *   it; calls that overlap on the GPU (other streams, unordered host threads)
  *   race on it.  Allocates nothing: no cudaMalloc, no cudaFree.
  */
 moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx,
