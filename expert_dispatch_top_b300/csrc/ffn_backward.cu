@@ -75,49 +75,125 @@ __global__ void __launch_bounds__(256) act_backward_kernel(const T* pre, const T
     }
 }
 
-// Transposed copy of an expert-major activation buffer [rows, C] into
-// [C, P] with each expert's rows starting at a 64-aligned column (its rows
-// padded with zeros up to the next multiple of 64), so that each expert's
-// weight gradient is a GEMM over a whole number of 64-wide K blocks.
-__global__ void __launch_bounds__(256) transpose_pad_kernel(const __nv_bfloat16* in, __nv_bfloat16* out,
-                                                            const int32_t* offsets, int E, int C,
-                                                            int64_t P) {
-    __shared__ int poff[257];
-    __shared__ __nv_bfloat16 tile[32][34];
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int e = 0; e < E; ++e) {
-            poff[e] = run;
-            run += (offsets[e + 1] - offsets[e] + 63) / 64 * 64;
-        }
-        poff[E] = run;
+// Padded row layout of the weight-gradient GEMMs: expert e's rows start at
+// padded row poff[e] = sum over e' < e of ceil(rows_e' / 64) * 64, and the rows
+// from its last row up to the next multiple of 64 are zero, so that each
+// expert's rows are a whole number of 64-row K blocks.  poff[E] = padded total.
+// Computed by the whole block (256 threads, E <= 256).
+__device__ __forceinline__ void pad_offsets(const int32_t* offsets, int E, int* poff,
+                                            int* wsum /* 8 ints */) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int v = tid < E ? (offsets[tid + 1] - offsets[tid] + 63) / 64 * 64 : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
     }
+    if (lane == 31) wsum[warp] = incl;
     __syncthreads();
-    const int total = poff[E];
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    // padded column block of 32 (never straddles an expert: segments are 64-aligned)
-    for (int pb = blockIdx.x * 32; pb < total; pb += gridDim.x * 32)
-    for (int c0 = 0; c0 < C; c0 += 32) {
-        int lo = 0, hi = E - 1;  // expert owning padded column pb
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (poff[mid] <= pb) lo = mid;
-            else hi = mid - 1;
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += wsum[w];
+    if (tid < E) poff[tid] = base + incl - v;
+    if (tid == 255) poff[E] = base + incl;
+    __syncthreads();
+}
+
+// Expert owning padded row p: the last e with poff[e] <= p.
+__device__ __forceinline__ int pad_owner(const int* poff, int E, int p) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (poff[mid] <= p) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// bf16 activation backward that also lays out the weight-gradient operands:
+// one padded row per block iteration, 8 columns per thread and vector.  Real
+// rows write d_pre (expert-major rows, for the input gradient) and the padded
+// copies d_pre_pad and h_pad; padding rows write zeros.
+template <bool GATED>
+__global__ void __launch_bounds__(256) act_backward_pad_kernel(
+    const __nv_bfloat16* pre, const __nv_bfloat16* dh, __nv_bfloat16* d_pre,
+    __nv_bfloat16* d_pre_pad, __nv_bfloat16* h_pad, const int32_t* offsets, int E, int f) {
+    __shared__ int poff[257];
+    __shared__ int wsum[8];
+    pad_offsets(offsets, E, poff, wsum);
+    const int up = GATED ? 2 * f : f;
+    const int nv = f / 8;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    for (int p = blockIdx.x; p < poff[E]; p += gridDim.x) {
+        const int e = pad_owner(poff, E, p);
+        const int j = p - poff[e];
+        const bool real = j < offsets[e + 1] - offsets[e];
+        const int64_t r = (int64_t)offsets[e] + j;
+        for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+            const int c = v * 8;
+            if (!real) {
+                *reinterpret_cast<uint4*>(h_pad + (int64_t)p * f + c) = zero;
+                *reinterpret_cast<uint4*>(d_pre_pad + (int64_t)p * up + c) = zero;
+                if (GATED) *reinterpret_cast<uint4*>(d_pre_pad + (int64_t)p * up + f + c) = zero;
+                continue;
+            }
+            float gd[8], a[8], hv[8], da[8];
+            Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(dh + r * f + c), gd);
+            Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(pre + r * up + c), a);
+            if (GATED) {
+                float u[8], du[8];
+                Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(pre + r * up + f + c), u);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float sg = sigm(a[i]);
+                    da[i] = gd[i] * u[i] * sg * (1.f + a[i] * (1.f - sg));
+                    du[i] = gd[i] * a[i] * sg;
+                    hv[i] = a[i] * sg * u[i];
+                }
+                const uint4 qu = Elem<__nv_bfloat16>::pack(du);
+                *reinterpret_cast<uint4*>(d_pre + r * up + f + c) = qu;
+                *reinterpret_cast<uint4*>(d_pre_pad + (int64_t)p * up + f + c) = qu;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float cdf = 0.5f * (1.f + erff(a[i] * 0.70710678118654752440f));
+                    const float pdf = 0.39894228040143267794f * expf(-0.5f * a[i] * a[i]);
+                    da[i] = gd[i] * (cdf + a[i] * pdf);
+                    hv[i] = a[i] * cdf;
+                }
+            }
+            const uint4 qa = Elem<__nv_bfloat16>::pack(da);
+            *reinterpret_cast<uint4*>(d_pre + r * up + c) = qa;
+            *reinterpret_cast<uint4*>(d_pre_pad + (int64_t)p * up + c) = qa;
+            *reinterpret_cast<uint4*>(h_pad + (int64_t)p * f + c) = Elem<__nv_bfloat16>::pack(hv);
         }
-        const int e = lo;
-        const int rows_e = offsets[e + 1] - offsets[e];
-        const int j0 = pb - poff[e];  // row within the expert
-        __syncthreads();
-        for (int i = ty; i < 32; i += 8) {
-            const int j = j0 + i, c = c0 + tx;
-            __nv_bfloat16 v = __float2bfloat16_rn(0.f);
-            if (j < rows_e && c < C) v = in[(int64_t)(offsets[e] + j) * C + c];
-            tile[i][tx] = v;
-        }
-        __syncthreads();
-        for (int i = ty; i < 32; i += 8) {
-            const int c = c0 + i;
-            if (c < C) out[(int64_t)c * P + pb + tx] = tile[tx][i];
+    }
+}
+
+// Padded copies of two expert-major [rows, C] bf16 buffers (xp and d_yp).
+__global__ void __launch_bounds__(256) pad_rows_kernel(const __nv_bfloat16* in0, __nv_bfloat16* out0,
+                                                       const __nv_bfloat16* in1, __nv_bfloat16* out1,
+                                                       const int32_t* offsets, int E, int C) {
+    __shared__ int poff[257];
+    __shared__ int wsum[8];
+    pad_offsets(offsets, E, poff, wsum);
+    const int nv = C / 8;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    for (int p = blockIdx.x; p < poff[E]; p += gridDim.x) {
+        const int e = pad_owner(poff, E, p);
+        const int j = p - poff[e];
+        const bool real = j < offsets[e + 1] - offsets[e];
+        const int64_t r = (int64_t)offsets[e] + j;
+        for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+            const int64_t o = (int64_t)p * C + v * 8;
+            if (real) {
+                const int64_t i = r * C + v * 8;
+                *reinterpret_cast<uint4*>(out0 + o) = ld_nc_v4(in0 + i);
+                *reinterpret_cast<uint4*>(out1 + o) = ld_nc_v4(in1 + i);
+            } else {
+                *reinterpret_cast<uint4*>(out0 + o) = zero;
+                *reinterpret_cast<uint4*>(out1 + o) = zero;
+            }
         }
     }
 }
@@ -179,6 +255,7 @@ size_t ffn_backward_scratch_bytes(int64_t rows_cap, int E, int d, int f, int gat
                                   int weight_grads) {
     const int up = gated ? 2 * f : f;
     auto al = [](size_t v) { return (v + 255) / 256 * 256; };
+    const size_t P = (size_t)((rows_cap + 64 * (int64_t)E + 63) / 64 * 64);  // padded rows bound
     size_t n = 0;
     n += al((size_t)rows_cap * up * eb);   // pre
     n += al((size_t)rows_cap * f * eb);    // dh
@@ -186,16 +263,12 @@ size_t ffn_backward_scratch_bytes(int64_t rows_cap, int E, int d, int f, int gat
     if (eb == 4) {
         n += al((size_t)E * up * d * eb);  // W_up^T
         n += al((size_t)E * d * f * eb);   // W_down^T
-    }
-    if (weight_grads) {
-        n += al((size_t)rows_cap * f * eb);  // h
-        if (eb == 2) {
-            const size_t P = (size_t)((rows_cap + 64 * (int64_t)E + 63) / 64 * 64);
-            n += al((size_t)d * P * 2);    // d_yp^T
-            n += al((size_t)f * P * 2);    // h^T
-            n += al((size_t)up * P * 2);   // d_pre^T
-            n += al((size_t)d * P * 2);    // xp^T
-        }
+        if (weight_grads) n += al((size_t)rows_cap * f * eb);  // h
+    } else if (weight_grads) {
+        n += al(P * f * 2);     // h, padded rows
+        n += al(P * up * 2);    // d_pre, padded rows
+        n += al(P * d * 2);     // xp, padded rows
+        n += al(P * d * 2);     // d_yp, padded rows
     }
     return n;
 }
@@ -204,30 +277,34 @@ cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
     const int gated = a.epi == EPI_SWIGLU;
     const int up = gated ? 2 * a.f : a.f;
     const int eb = a.dtype == MOE_DTYPE_F32 ? 4 : 2;
+    const bool tc = eb == 2;
     const bool wg = a.d_w_up || a.d_w_down;
+    if (tc && a.E > 256) return cudaErrorInvalidValue;
     auto al = [](size_t v) { return (v + 255) / 256 * 256; };
+    const size_t P = (size_t)((a.rows_cap + 64 * (int64_t)a.E + 63) / 64 * 64);
     char* sp = static_cast<char*>(a.scratch);
-    void* pre = sp;
-    sp += al((size_t)a.rows_cap * up * eb);
-    void* dh = sp;
-    sp += al((size_t)a.rows_cap * a.f * eb);
-    void* d_pre = sp;
-    sp += al((size_t)a.rows_cap * up * eb);
-    void* w_upT = nullptr;
-    void* w_downT = nullptr;
-    if (eb == 4) {
-        w_upT = sp;
-        sp += al((size_t)a.E * up * a.d * eb);
-        w_downT = sp;
-        sp += al((size_t)a.E * a.d * a.f * eb);
-    }
-    void* h = nullptr;
-    if (wg) {
-        h = sp;
-        sp += al((size_t)a.rows_cap * a.f * eb);
+    auto take = [&](size_t bytes) {
+        void* q = sp;
+        sp += al(bytes);
+        return q;
+    };
+    void* pre = take((size_t)a.rows_cap * up * eb);
+    void* dh = take((size_t)a.rows_cap * a.f * eb);
+    void* d_pre = take((size_t)a.rows_cap * up * eb);
+    void *w_upT = nullptr, *w_downT = nullptr, *h = nullptr;
+    void *h_pad = nullptr, *d_pre_pad = nullptr, *xp_pad = nullptr, *dyp_pad = nullptr;
+    if (!tc) {
+        w_upT = take((size_t)a.E * up * a.d * eb);
+        w_downT = take((size_t)a.E * a.d * a.f * eb);
+        if (wg) h = take((size_t)a.rows_cap * a.f * eb);
+    } else if (wg) {
+        h_pad = take(P * a.f * 2);
+        d_pre_pad = take(P * up * 2);
+        xp_pad = take(P * a.d * 2);
+        dyp_pad = take(P * a.d * 2);
     }
     cudaError_t e;
-    if (eb == 4) {
+    if (!tc) {
         // transposed weights: W_up [E, up, d] -> [E, d, up]; W_down [E, d, f] -> [E, f, d]
         if ((e = transpose_batched<float>(a.w_up, w_upT, a.E, up, a.d, s)) != cudaSuccess) return e;
         if ((e = transpose_batched<float>(a.w_down, w_downT, a.E, a.d, a.f, s)) != cudaSuccess)
@@ -248,30 +325,40 @@ cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
         g.epi = EPI_NONE;
         g.dtype = a.dtype;
         g.status = a.status;
-        g.kgrouped = 0;
         g.b_mn = b_mn;
-        return eb == 4 ? launch_gemm_simt(g, s) : launch_gemm_tc(g, s);
+        return tc ? launch_gemm_tc(g, s) : launch_gemm_simt(g, s);
     };
-    const bool tc = eb == 2;
     if ((e = gemm(a.xp, a.w_up, pre, up, a.d, 0)) != cudaSuccess) return e;  // 1
     if ((e = gemm(a.d_yp, tc ? a.w_down : w_downT, dh, a.f, a.d, tc)) != cudaSuccess) return e;  // 2
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (eb == 4)
+    // 3: activation backward (bf16 with weight gradients: also the padded operands)
+    if (tc && wg) {
+        if (gated)
+            act_backward_pad_kernel<true><<<sms * 8, 256, 0, s>>>(
+                static_cast<const __nv_bfloat16*>(pre), static_cast<const __nv_bfloat16*>(dh),
+                static_cast<__nv_bfloat16*>(d_pre), static_cast<__nv_bfloat16*>(d_pre_pad),
+                static_cast<__nv_bfloat16*>(h_pad), a.offsets, a.E, a.f);
+        else
+            act_backward_pad_kernel<false><<<sms * 8, 256, 0, s>>>(
+                static_cast<const __nv_bfloat16*>(pre), static_cast<const __nv_bfloat16*>(dh),
+                static_cast<__nv_bfloat16*>(d_pre), static_cast<__nv_bfloat16*>(d_pre_pad),
+                static_cast<__nv_bfloat16*>(h_pad), a.offsets, a.E, a.f);
+    } else if (!tc) {
         act_backward_kernel<float><<<sms * 8, 256, 0, s>>>(
             static_cast<const float*>(pre), static_cast<const float*>(dh), static_cast<float*>(d_pre),
             static_cast<float*>(h), a.offsets, a.E, a.f, gated, a.rows_cap);
-    else
+    } else {
         act_backward_kernel<__nv_bfloat16><<<sms * 8, 256, 0, s>>>(
             static_cast<const __nv_bfloat16*>(pre), static_cast<const __nv_bfloat16*>(dh),
-            static_cast<__nv_bfloat16*>(d_pre), static_cast<__nv_bfloat16*>(h), a.offsets, a.E, a.f,
-            gated, a.rows_cap);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;                     // 3
+            static_cast<__nv_bfloat16*>(d_pre), nullptr, a.offsets, a.E, a.f, gated, a.rows_cap);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = gemm(d_pre, tc ? a.w_up : w_upT, a.d_xp, a.d, up, tc)) != cudaSuccess) return e;  // 4
     if (!wg) return cudaSuccess;
     // 5: weight gradients
-    if (eb == 4) {
+    if (!tc) {
         if (a.d_w_down) {
             dim3 grid((a.f + 63) / 64, (a.d + 63) / 64, a.E);
             wgrad_simt_kernel<<<grid, 256, 0, s>>>(static_cast<const float*>(a.d_yp),
@@ -286,27 +373,17 @@ cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
         }
         return cudaGetLastError();
     }
-    const int64_t P = (a.rows_cap + 64 * (int64_t)a.E + 63) / 64 * 64;
-    void* dypT = sp;
-    sp += al((size_t)a.d * P * 2);
-    void* hT = sp;
-    sp += al((size_t)a.f * P * 2);
-    void* dpreT = sp;
-    sp += al((size_t)up * P * 2);
-    void* xpT = sp;
-    sp += al((size_t)a.d * P * 2);
-    const unsigned pblocks = (unsigned)((P + 31) / 32 < 4096 ? (P + 31) / 32 : 4096);
-    auto tpad = [&](const void* in, void* out, int C) {
-        transpose_pad_kernel<<<pblocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in),
-                                                  static_cast<__nv_bfloat16*>(out), a.offsets, a.E, C,
-                                                  P);
-        return cudaGetLastError();
-    };
-    auto kgemm = [&](const void* At, const void* Bt, void* out, int M, int N) {
+    pad_rows_kernel<<<sms * 4, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(a.xp), static_cast<__nv_bfloat16*>(xp_pad),
+        static_cast<const __nv_bfloat16*>(a.d_yp), static_cast<__nv_bfloat16*>(dyp_pad), a.offsets,
+        a.E, a.d);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // dW[e] = A_pad[K_e, :]^T . B_pad[K_e, :] over expert e's padded rows
+    auto kgemm = [&](const void* A, const void* B, void* out, int M, int N) {
         GemmArgs g;
-        g.A = At;       // [M, P]
-        g.B = Bt;       // [N, P]
-        g.out = out;    // [E, M, N]
+        g.A = A;      // [P, M]
+        g.B = B;      // [P, N]
+        g.out = out;  // [E, M, N]
         g.offsets = a.offsets;
         g.rows_cap = M;
         g.m_rows = 0;
@@ -319,16 +396,8 @@ cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
         g.kgrouped = 1;
         return launch_gemm_tc(g, s);
     };
-    if (a.d_w_down) {
-        if ((e = tpad(a.d_yp, dypT, a.d)) != cudaSuccess) return e;
-        if ((e = tpad(h, hT, a.f)) != cudaSuccess) return e;
-        if ((e = kgemm(dypT, hT, a.d_w_down, a.d, a.f)) != cudaSuccess) return e;
-    }
-    if (a.d_w_up) {
-        if ((e = tpad(d_pre, dpreT, up)) != cudaSuccess) return e;
-        if ((e = tpad(a.xp, xpT, a.d)) != cudaSuccess) return e;
-        if ((e = kgemm(dpreT, xpT, a.d_w_up, up, a.d)) != cudaSuccess) return e;
-    }
+    if (a.d_w_down && (e = kgemm(dyp_pad, h_pad, a.d_w_down, a.d, a.f)) != cudaSuccess) return e;
+    if (a.d_w_up && (e = kgemm(d_pre_pad, xp_pad, a.d_w_up, up, a.d)) != cudaSuccess) return e;
     return cudaSuccess;
 }
 

@@ -37,9 +37,11 @@
 // MMA reads B through MN-major descriptors (chunk stride 8 KB).  No epilogue.
 //
 // K-grouped mode (weight gradients): group g's output is a whole [M, N]
-// matrix, out[g] = A[:, K_g] . B[:, K_g]^T, where A [M, K] and B [N, K] are
-// activations transposed so that each group's rows form a 64-aligned range
-// K_g of the contraction dimension.  Tiles run over (group, n-tile, m-tile)
+// matrix, out[g] = A[K_g, :]^T . B[K_g, :], where A [K, M] and B [K, N] are
+// activation buffers whose rows are laid out so that each group's rows form a
+// 64-aligned range K_g (zero rows pad each group to a multiple of 64).  Both
+// operands are read MN-major, as stored: a stage holds two (A) and four (B)
+// TMA boxes of 64 columns x 64 rows.  Tiles run over (group, n-tile, m-tile)
 // as above, but every tile's K loop covers only its group's K blocks; the
 // tiles of a group without rows issue no MMA and store zeros.
 //
@@ -69,6 +71,7 @@ constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
 constexpr uint32_t kIdescBmn = idesc_bf16_bmn(BM, BN);
+constexpr uint32_t kIdescMn = idesc_bf16_bmn(BM, BN) | (1u << 15);  // A and B MN-major
 constexpr int MN_CHUNK = 64 * BK * 2;  // one 64-column x 64-row box of an MN-major B: 8 KB
 
 struct TcParams {
@@ -258,8 +261,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // test hook: leave this stage unfilled; the MMA issuer's wait runs out
                     } else if (KG) {
                         mbar_expect_tx(fb, STAGE_BYTES);
-                        tma_load_2d(sa, &tmA, k0, ti.row0, fb);
-                        tma_load_3d(sb, &tmB, k0, ti.n_tile * BN, 0, fb);
+#pragma unroll
+                        for (int c = 0; c < BM / 64; ++c)
+                            tma_load_2d(sa + c * MN_CHUNK, &tmA, ti.row0 + c * 64, k0, fb);
+#pragma unroll
+                        for (int c = 0; c < BN / 64; ++c)
+                            tma_load_3d(sb + c * MN_CHUNK, &tmB, ti.n_tile * BN + c * 64, k0, 0, fb);
                     } else if (BMN) {
                         mbar_expect_tx(fb, STAGE_BYTES);
                         tma_load_2d(sa, &tmA, k0, ti.row0, fb);
@@ -310,7 +317,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t sb = sa + A_STAGE;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        if (BMN)  // 16 K rows of 128 B per MMA
+                        if (KG)  // both operands MN-major: 16 K rows of 128 B per MMA
+                            mma_bf16(d_tmem, sw128_mn_desc(sa + kk * 2048, MN_CHUNK),
+                                     sw128_mn_desc(sb + kk * 2048, MN_CHUNK), kIdescMn,
+                                     (kb | kk) != 0 ? 1u : 0u);
+                        else if (BMN)  // 16 K rows of 128 B per MMA
                             mma_bf16(d_tmem, sw128_desc(sa + kk * 32),
                                      sw128_mn_desc(sb + kk * 2048, MN_CHUNK), kIdescBmn,
                                      (kb | kk) != 0 ? 1u : 0u);
@@ -426,6 +437,7 @@ int gemm_tc_supported(const GemmArgs& a) {
     if (a.G < 1 || a.G > MAX_GROUPS) return 3;
     if (a.rows_cap >= (1ll << 31) || a.K > (1 << 20)) return 4;
     if (a.b_mn && (a.kgrouped || a.epi != EPI_NONE)) return 6;
+    if (a.kgrouped && (a.rows_cap % 64 != 0 || !a.offsets || a.epi != EPI_NONE)) return 7;
     if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B) |
          reinterpret_cast<uintptr_t>(a.out)) & 15)
         return 5;
@@ -444,9 +456,13 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
     CUtensorMap tmA, tmB;
     // A is read with 2-D loads, the stacked weights with 3-D loads (group index;
     // a single [N, K] matrix in K-grouped mode).
-    if (!make_tmap_bf16(&tmA, a.A, (uint64_t)a.K, (uint64_t)rows_cap, 1, BM, 2))
+    if (kg) {  // A [K, M] and B [K, N]: boxes of 64 columns x 64 K-rows
+        if (!make_tmap_bf16(&tmA, a.A, (uint64_t)rows_cap, (uint64_t)a.K, 1, BK, 2) ||
+            !make_tmap_bf16(&tmB, a.B, (uint64_t)a.N, (uint64_t)a.K, 1, BK, 3))
+            return cudaErrorInvalidValue;
+    } else if (!make_tmap_bf16(&tmA, a.A, (uint64_t)a.K, (uint64_t)rows_cap, 1, BM, 2)) {
         return cudaErrorInvalidValue;
-    if (bmn) {  // [G, K, N]: boxes of 64 N-columns x 64 K-rows
+    } else if (bmn) {  // [G, K, N]: boxes of 64 N-columns x 64 K-rows
         if (!make_tmap_bf16(&tmB, a.B, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.G, BK, 3))
             return cudaErrorInvalidValue;
     } else if (!make_tmap_bf16(&tmB, a.B, (uint64_t)a.K, (uint64_t)b_rows, kg ? 1 : (uint64_t)a.G,
