@@ -88,26 +88,28 @@ __device__ __forceinline__ float sigmoid_approx(float L) {
 }
 
 // Sorted top-k (k <= 8) in registers: key, a payload value and the index.
+// The list always has 8 entries, in descending key order: 8 - k sentinels
+// (key +inf, never displaced) followed by the k best so far, so the k-th best
+// is always entry 7.  A fixed position keeps the list in registers (reading
+// entry k - 1 for a runtime k would make it an indexed array in local memory).
 struct TopK {
     float key[8], val[8];
     int idx[8];
-    float kth_key;
-    int kth_idx;
-    __device__ __forceinline__ void init() {
+    __device__ __forceinline__ void init(int k) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            key[j] = -INFINITY;
+            const bool sentinel = j < 8 - k;
+            key[j] = sentinel ? INFINITY : -INFINITY;
             val[j] = 0.f;
-            idx[j] = 0x7fffffff;
+            idx[j] = sentinel ? -1 : 0x7fffffff;
         }
-        kth_key = -INFINITY;
-        kth_idx = 0x7fffffff;
     }
-    __device__ __forceinline__ void insert(float kv, float v, int e, int k) {
-        if (!key_better(kv, e, kth_key, kth_idx)) return;
+    __device__ __forceinline__ float kth_key() const { return key[7]; }
+    __device__ __forceinline__ void insert(float kv, float v, int e) {
+        if (!key_better(kv, e, key[7], idx[7])) return;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            if (j < k && key_better(kv, e, key[j], idx[j])) {
+            if (key_better(kv, e, key[j], idx[j])) {
                 const float tk = key[j], tv = val[j];
                 const int ti = idx[j];
                 key[j] = kv;
@@ -118,12 +120,6 @@ struct TopK {
                 e = ti;
             }
         }
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j == k - 1) {
-                kth_key = key[j];
-                kth_idx = idx[j];
-            }
     }
 };
 
@@ -320,7 +316,7 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256);
             const int64_t t = (int64_t)tile * RM + q * 32 + lane;
             TopK top;
-            top.init();
+            top.init(p.k);
             float v[32];
             // Rank-limited routing: rank score = best key among the rank's
             // experts; keep the max_ranks best ranks (ties to the lower rank).
@@ -384,7 +380,7 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
             if (!sigmoid) {
                 for (int c = 0; c < nchunks; ++c) {
                     tmem_ld32(tb + (uint32_t)(c * 32), v);
-                    const float thr = top.kth_key;
+                    const float thr = top.kth_key();
                     uint32_t mask = 0;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -397,15 +393,15 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                         const int i = __ffs(mask) - 1;
                         mask &= mask - 1;
                         const float L = stash[i];
-                        top.insert(L, L, c * 32 + i, p.k);
+                        top.insert(L, L, c * 32 + i);
                     }
                 }
             } else {
                 TopK approx;
-                approx.init();
+                approx.init(p.k);
                 for (int c = 0; c < nchunks; ++c) {
                     tmem_ld32(tb + (uint32_t)(c * 32), v);
-                    const float thr = approx.kth_key;
+                    const float thr = approx.kth_key();
                     uint32_t mask = 0;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -420,10 +416,10 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                         mask &= mask - 1;
                         const int e = c * 32 + i;
                         const float a = __fadd_rn(sigmoid_approx(stash[i]), sb_s[e]);
-                        approx.insert(a, 0.f, e, p.k);
+                        approx.insert(a, 0.f, e);
                     }
                 }
-                const float thresh = approx.kth_key - 2.f * kApproxDelta;
+                const float thresh = approx.kth_key() - 2.f * kApproxDelta;
                 for (int c = 0; c < nchunks; ++c) {
                     tmem_ld32(tb + (uint32_t)(c * 32), v);
                     uint32_t mask = 0;
@@ -441,19 +437,24 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                         const int e = c * 32 + i;
                         const float s = sigmoid_exact(stash[i]);
                         const float key = has_sb ? __fadd_rn(s, sb_s[e]) : s;
-                        top.insert(key, s, e, p.k);
+                        top.insert(key, s, e);
                     }
                 }
             }
             // gates
+            // the k chosen experts are entries 8-k .. 7, best first
+            const int j0 = 8 - p.k;
             float g[8];
             if (!sigmoid) {
-                const float m = top.val[0];
+                float m = -INFINITY;  // the best logit
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j == j0) m = top.val[j];
                 float z = 0.f;
                 if (p.renorm) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        if (j < p.k) z += expf(top.val[j] - m);
+                        if (j >= j0) z += expf(top.val[j] - m);
                 } else {
                     for (int c = 0; c < nchunks; ++c) {
                         tmem_ld32(tb + (uint32_t)(c * 32), v);
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                 float z = 0.f;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    if (j < p.k) z += top.val[j];
+                    if (j >= j0) z += top.val[j];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) g[j] = p.renorm ? top.val[j] / z : top.val[j];
             }
@@ -483,9 +484,9 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
             if (t < p.T) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    if (j < p.k) {
-                        p.idx[t * p.k + j] = top.idx[j];
-                        p.gate[t * p.k + j] = g[j];
+                    if (j >= j0) {
+                        p.idx[t * p.k + (j - j0)] = top.idx[j];
+                        p.gate[t * p.k + (j - j0)] = g[j];
                     }
             }
         }
