@@ -59,7 +59,6 @@ constexpr int R_SMEM_TILES = 196608;  // bytes of stage ring
 constexpr int R_SMEM_FIXED = 1024 /*align*/ + 256 /*barriers*/ + 2 * 256 * 4 /*biases*/;
 constexpr int R_SMEM_MAX = 232448;  // 227 KB per block
 constexpr float kApproxDelta = 1.0f / 256.0f;
-constexpr int kPrefetch = 8;  // K blocks of x prefetched into L2 ahead of the loads
 
 struct RtParams {
     int64_t T;
@@ -199,28 +198,9 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            // x is read once, from DRAM: prefetch it into L2 kPrefetch K blocks ahead
-            // of the loads (into the next tile near the end of one), so that the
-            // loads that feed the MMAs hit L2.
-            for (int i = 0; i < kPrefetch && i < p.num_kb && blockIdx.x < p.m_tiles; ++i) {
-                int kb = k_start(blockIdx.x, p.num_kb) + i;
-                if (kb >= p.num_kb) kb -= p.num_kb;
-                tma_prefetch_2d(&tmX, kb * RK, (int)blockIdx.x * RM);
-            }
             for (int tile = blockIdx.x; tile < p.m_tiles && !*abort_flag; tile += gridDim.x) {
                 const int kb0 = k_start(tile, p.num_kb);
-                const int next = tile + (int)gridDim.x;
                 for (int i = 0; i < p.num_kb; ++i) {
-                    const int j = i + kPrefetch;
-                    if (j < p.num_kb) {
-                        int kb = kb0 + j;
-                        if (kb >= p.num_kb) kb -= p.num_kb;
-                        tma_prefetch_2d(&tmX, kb * RK, tile * RM);
-                    } else if (next < p.m_tiles && j - p.num_kb < p.num_kb) {
-                        int kb = k_start(next, p.num_kb) + (j - p.num_kb);
-                        if (kb >= p.num_kb) kb -= p.num_kb;
-                        tma_prefetch_2d(&tmX, kb * RK, next * RM);
-                    }
                     int kb = kb0 + i;
                     if (kb >= p.num_kb) kb -= p.num_kb;
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status,

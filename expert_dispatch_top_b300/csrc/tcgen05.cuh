@@ -78,15 +78,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
         : "memory");
 }
 
-// L2 prefetch of one box of a 2-D tensor map: no shared memory, no barrier;
-// boxes outside the tensor are ignored.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* tm, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(tm)),
-                 "r"(c0), "r"(c1)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
                                             int c2, uint32_t bar) {
     asm volatile(
