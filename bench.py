@@ -163,13 +163,18 @@ def layer_work(w, n_kept):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline and --impl reference)
 # ---------------------------------------------------------------------------
-def oracle_step(w, inp, rng_seed, route_tokens, ffn_tokens):
+def oracle_step(w, inp, rng_seed, route_tokens, ffn_experts, disp_tokens=None, comb_tokens=256):
     """Time the oracle on a bounded sample and extrapolate to the workload:
-    route `route_tokens` tokens; dispatch every token (cheap); expert FFN and
-    combine for `ffn_tokens` tokens.  Returns (seconds for the whole
-    workload, description)."""
+    route `route_tokens` tokens; dispatch and permute `disp_tokens` tokens
+    (all T by default); the expert FFN of `ffn_experts` experts with as many of
+    their rows as the oracle has threads (it parallelises one call over its
+    rows, and every expert of the full workload has far more rows than
+    threads); combine `comb_tokens` tokens.  Each phase is scaled linearly to
+    the full workload (the FFN by rows).  Returns (seconds for the whole
+    workload, description, per-phase seconds)."""
     import torch
 
+    import moe_workloads as W
     import oracle
     T = w.T
     g = torch.Generator().manual_seed(rng_seed)
@@ -178,43 +183,50 @@ def oracle_step(w, inp, rng_seed, route_tokens, ffn_tokens):
     oracle.route(inp["x"][rs], inp["w_router"], w.k, w.score, w.renorm, inp["logit_bias"],
                  inp["sel_bias"])
     t_route = (time.perf_counter() - t0) * T / len(rs)
-    # dispatch needs every token's choice: take seeded choices of the same shape
-    import moe_workloads as W
-    idx = W.random_topk(T, w.E, w.k, seed=rng_seed)
-    C = oracle.capacity(T, w.k, w.E, w.capacity_factor)
+    # dispatch needs every sampled token's choice: take seeded choices of the same shape
+    nd = T if disp_tokens is None else max(1, min(T, disp_tokens))
+    ds = torch.sort(torch.randperm(T, generator=g)[:nd]).values
+    idx = W.random_topk(nd, w.E, w.k, seed=rng_seed)
+    C = oracle.capacity(nd, w.k, w.E, w.capacity_factor)
+    xs = inp["x"] if nd == T else inp["x"][ds]
     t0 = time.perf_counter()
     disp = oracle.dispatch(idx, w.E, w.R, C)
-    xp = oracle.permute(inp["x"], disp["slot_row"], disp["rows"])
-    t_disp = time.perf_counter() - t0
-    fs = torch.randperm(T, generator=g)[:ffn_tokens]
+    xp = oracle.permute(xs, disp["slot_row"], disp["rows"])
+    t_disp = (time.perf_counter() - t0) * T / nd
+    full_rows = disp["rows"] * T / nd  # kept rows of the whole workload, estimated
     t_ffn = 0.0
-    t_comb = 0.0
     n_rows_s = 0
+    n_exp = 0
+    off = disp["expert_offsets"]
+    rows_per_call = oracle.num_threads()
+    yp = torch.zeros((max(disp["rows"], 1), w.d), dtype=torch.float64)
     if w.act != "identity":
-        rows = disp["slot_row"][fs].flatten()
-        rows = rows[rows >= 0]
-        n_rows_s = rows.numel()
-        off = disp["expert_offsets"]
-        yp = torch.zeros((max(n_rows_s, 1), w.d), dtype=torch.float64)
+        order = torch.randperm(w.E, generator=g).tolist()
         t0 = time.perf_counter()
-        for e in range(w.E):
-            sel = ((rows >= off[e]) & (rows < off[e + 1])).nonzero().flatten()
-            if sel.numel():
-                yp[sel] = oracle.expert_ffn(xp[rows[sel].long()], inp["w_up"][e],
-                                            inp["w_down"][e], w.act, w.d_ff)
-        t_ffn = (time.perf_counter() - t0) * disp["rows"] / max(n_rows_s, 1)
-        row_map = torch.full((max(disp["rows"], 1),), 0, dtype=torch.int32)
-        row_map[rows.long()] = torch.arange(n_rows_s, dtype=torch.int32)
+        for e in order:
+            lo, hi = int(off[e]), int(off[e + 1])
+            if hi == lo:
+                continue
+            n = min(rows_per_call, hi - lo)
+            yp[lo:lo + n] = oracle.expert_ffn(xp[lo:lo + n], inp["w_up"][e], inp["w_down"][e],
+                                              w.act, w.d_ff)
+            n_rows_s += n
+            n_exp += 1
+            if n_exp == ffn_experts:
+                break
+        t_ffn = (time.perf_counter() - t0) * full_rows / max(n_rows_s, 1)
     else:
         yp = xp.double()
-        row_map = torch.arange(max(disp["rows"], 1), dtype=torch.int32)
+    row_map = torch.arange(max(disp["rows"], 1), dtype=torch.int32)
+    fs = torch.randperm(nd, generator=g)[:max(1, min(nd, comb_tokens))]
     t0 = time.perf_counter()
-    oracle.combine(fs, yp, row_map, disp["slot_row"], torch.rand((T, w.k), generator=g))
+    oracle.combine(fs, yp, row_map, disp["slot_row"], torch.rand((nd, w.k), generator=g))
     t_comb = (time.perf_counter() - t0) * T / len(fs)
     total = t_route + t_disp + t_ffn + t_comb
-    desc = (f"route {len(rs)} of {T} tokens, dispatch+permute all {T}, expert FFN on the "
-            f"{n_rows_s} rows of {len(fs)} sampled tokens (of {disp['rows']}), combine {len(fs)} "
-            f"tokens; each phase extrapolated linearly to the full workload")
+    desc = (f"route {len(rs)} of {T} tokens, dispatch+permute {nd} of {T}, expert FFN on "
+            f"{n_rows_s} rows ({n_exp} experts x up to {rows_per_call} rows, one row per oracle "
+            f"thread), combine {len(fs)} tokens; each phase extrapolated linearly to the full "
+            f"workload")
     return total, desc, dict(route=t_route, dispatch=t_disp, ffn=t_ffn, combine=t_comb)
 
 
@@ -228,21 +240,32 @@ def cpu_inputs(w, dev_inp=None):
 
 
 def run_reference(args, w):
-    import torch
-
+    """The oracle as it stands, on the host cores, one bounded sample per step,
+    sized so that all warm-up and timed steps together take about
+    --ref-budget-s seconds (or one minimal sample per step, if even that is
+    over budget)."""
     import oracle
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     inp = cpu_inputs(w)
-    rt, ft = args.ref_route_tokens, args.ref_ffn_tokens
-    for i in range(args.warmup):
-        oracle_step(w, inp, 100 + i, rt, ft)
+    # Calibration step (one of the warm-up steps) with one expert's FFN sample;
+    # the FFN is nearly all of the oracle's time, so only the number of sampled
+    # experts grows to fill the per-step budget.
+    rt, dt, fe = min(w.T, 256), min(w.T, 2048), 1
+    t0 = time.perf_counter()
+    oracle_step(w, inp, 99, rt, fe, dt)
+    cal = time.perf_counter() - t0
+    per_step = args.ref_budget_s / max(1, args.steps + args.warmup)
+    if cal < per_step:
+        fe = int(max(1, min(args.ref_ffn_experts, w.E, per_step / cal)))
+    for i in range(max(0, args.warmup - 1)):
+        oracle_step(w, inp, 100 + i, rt, fe, dt)
     times = []
     desc = ""
     t_wall = time.perf_counter()
     for i in range(args.steps):
-        t, desc, _ = oracle_step(w, inp, 1000 + i, rt, ft)
+        t, desc, _ = oracle_step(w, inp, 1000 + i, rt, fe, dt)
         times.append(t)
     wall = time.perf_counter() - t_wall
     per_step = statistics.mean(times)
@@ -509,7 +532,7 @@ def run_ours(args, w):
     if world == 1 and not args.no_cpu_baseline:
         import oracle
         inp_cpu = cpu_inputs(w, inp)
-        t, desc, parts = oracle_step(w, inp_cpu, 7, args.ref_route_tokens, args.ref_ffn_tokens)
+        t, desc, parts = oracle_step(w, inp_cpu, 7, args.ref_route_tokens, args.ref_ffn_experts)
         cpu = {"value": w.T / t, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                "sample": desc, "phase_s": parts}
 
@@ -552,7 +575,10 @@ def main():
     ap.add_argument("--backward", action="store_true",
                     help="also time the expert-FFN backward (kernels.ffn_backward)")
     ap.add_argument("--ref-route-tokens", type=int, default=256)
-    ap.add_argument("--ref-ffn-tokens", type=int, default=32)
+    ap.add_argument("--ref-ffn-experts", type=int, default=8,
+                    help="experts whose FFN the oracle sample runs (rows: one per oracle thread)")
+    ap.add_argument("--ref-budget-s", type=float, default=150.0,
+                    help="host seconds for all --impl reference steps (samples are sized to fit)")
     args = ap.parse_args()
     import moe_workloads as W
     w = W.get(args.workload)
