@@ -48,8 +48,8 @@ UNIT = "tokens/s"
 # unchanged.  See profiles/ for the commands.
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the full
-    # Mixtral-shaped step: up 2.19 GB read + 0.93 GB written, down 5.20 GB + 0.27 GB.
-    "mixtral": {"bytes": 2.19e9 + 0.92879e9 + 5.20e9 + 0.26515e9, "src_hash": "2ba60a5928c7afed",
+    # Mixtral-shaped step: up 2.18 GB read + 0.928 GB written, down 5.20 GB + 0.265 GB.
+    "mixtral": {"bytes": 2.18e9 + 0.92834e9 + 5.20e9 + 0.2649e9, "src_hash": "cf736a73bf34ec4d",
                 "per": "step (up + down launches)"},
 }
 
