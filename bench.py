@@ -359,7 +359,8 @@ def run_ours(args, w):
     x = inp["x"]
     stream = torch.cuda.current_stream()
     ident = w.act == "identity"
-    per_step_launches = 4 + (0 if ident else 2 * (1 + w.n_shared))
+    # route 1, dispatch 3 (count, scan, place), combine 1, FFN 2 per expert set
+    per_step_launches = 5 + (0 if ident else 2 * (1 + w.n_shared))
 
     def barrier():
         if world > 1:
