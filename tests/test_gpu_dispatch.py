@@ -58,6 +58,10 @@ def _compare(cfg, x, idx, out, check_xp_full=True):
     (5000, 64, 8, 8, 1, 0.0, 0, 0.0),     # k = E: every expert takes every token
     (2048, 64, 32, 3, 32, 0.0, 7, 0.5),   # 32 virtual ranks, explicit capacity
     (257, 64, 3, 1, 3, 0.0, 0, 0.0),      # odd expert count
+    # few token blocks with long rows: each block's row copies split over column chunks
+    (300, 7168, 256, 8, 8, 0.0, 0, 0.5),
+    (129, 4096, 8, 2, 8, 0.0, 0, 0.0),
+    (200, 2048, 16, 4, 8, 1.0, 0, 1.0),
 ])
 def test_dispatch_matches_oracle(T, d, E, k, R, cf, cap, skew):
     cfg = _cfg(T, d, E, k, R, cf, cap)
@@ -65,6 +69,22 @@ def test_dispatch_matches_oracle(T, d, E, k, R, cf, cap, skew):
     x = W._grid_int((T, d), -8, 8, 8.0, W._gen(T, "cpu"), "cpu").to(torch.bfloat16).to(DEV)
     out = run_dispatch(cfg, x, idx)
     _compare(cfg, x, idx, out)
+
+
+def test_dispatch_no_tokens_writes_zero_metadata():
+    cfg = _cfg(0, 64, 8, 2, 4)
+    x = torch.zeros((1, 64), dtype=torch.bfloat16, device=DEV)
+    out = run_dispatch(cfg, x, torch.zeros((0, 2), dtype=torch.int32))
+    assert out["status"] == 0
+    for key in ("expert_counts", "expert_offsets", "rank_counts", "rank_splits", "n_dropped"):
+        assert torch.all(out[key] == 0), key
+
+
+def test_dispatch_fp32_long_rows_in_column_chunks():
+    cfg = _cfg(90, 3072, 8, 2, 4, dtype="f32")
+    idx = W.random_topk(90, 8, 2, seed=11, skew=0.7)
+    x = W._grid_int((90, 3072), -8, 8, 8.0, W._gen(11, "cpu"), "cpu").to(DEV)
+    _compare(cfg, x, idx, run_dispatch(cfg, x, idx))
 
 
 def test_dispatch_fp32_rows():
