@@ -485,7 +485,7 @@ def run_ours(args, w):
     kernels = {
         "route": {"ms": phase["route"],
                   "GB/s": work["route_bytes"] / (phase["route"] * 1e-3) / 1e9,
-                  "TFLOP/s_fp32": work["route_flops"] / (phase["route"] * 1e-3) / 1e12},
+                  "TFLOP/s": work["route_flops"] / (phase["route"] * 1e-3) / 1e12},
         "dispatch": {"ms": phase["dispatch"],
                      "GB/s": work["permute_bytes"] / (phase["dispatch"] * 1e-3) / 1e9},
         "combine": {"ms": phase["combine"],
@@ -525,8 +525,14 @@ def run_ours(args, w):
                     "algorithmic_bytes_per_step": work["permute_bytes"]}
     if args.backward and not ident:
         kernels["ffn_backward"] = time_ffn_backward(args, w, cfg, b, inp, stream, peaks)
-    kernels["route"]["frac_fp32_ffma"] = kernels["route"]["TFLOP/s_fp32"] / \
-        fp32_ffma_peak_tflops(sms, peaks["sm_mhz"])
+    # bf16 routers run on the tensor cores (a short kernel: burst peak), fp32 ones on FFMA
+    if w.dtype == "bf16":
+        kernels["route"]["pipe"] = "tensor (bf16)"
+        kernels["route"]["frac_tensor"] = kernels["route"]["TFLOP/s"] / peaks["bf16"]
+    else:
+        kernels["route"]["pipe"] = "FFMA (fp32)"
+        kernels["route"]["frac_fp32_ffma"] = kernels["route"]["TFLOP/s"] / \
+            fp32_ffma_peak_tflops(sms, peaks["sm_mhz"])
     kernels["route"]["frac_hbm"] = kernels["route"]["GB/s"] / peaks["hbm"]
 
     cpu = None
