@@ -49,7 +49,7 @@ UNIT = "tokens/s"
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the full
     # Mixtral-shaped step: up 2.18 GB read + 0.928 GB written, down 5.20 GB + 0.265 GB.
-    "mixtral": {"bytes": 2.18e9 + 0.92834e9 + 5.20e9 + 0.2649e9, "src_hash": "cf736a73bf34ec4d",
+    "mixtral": {"bytes": 2.18e9 + 0.92834e9 + 5.20e9 + 0.2649e9, "src_hash": "aaa35b3fa1d43b50",
                 "per": "step (up + down launches)"},
 }
 

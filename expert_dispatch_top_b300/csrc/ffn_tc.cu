@@ -496,12 +496,15 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
     const int mode = kg ? 1 : bmn ? 2 : 0;
     auto kern = mode == 1 ? tc_gemm_kernel<true, false>
                           : mode == 2 ? tc_gemm_kernel<false, true> : tc_gemm_kernel<false, false>;
-    static bool attr_set[3] = {false, false, false};
-    if (!attr_set[mode]) {
+    // the shared-memory limit is a per-device function attribute: set it once per
+    // device and kernel form (a repeated set from a racing thread is harmless)
+    constexpr int kDevs = 64;
+    static bool attr_set[kDevs][3] = {};
+    if (dev < 0 || dev >= kDevs || !attr_set[dev][mode]) {
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr_set[mode] = true;
+        if (dev >= 0 && dev < kDevs) attr_set[dev][mode] = true;
     }
     kern<<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
     return cudaGetLastError();

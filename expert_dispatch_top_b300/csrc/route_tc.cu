@@ -527,12 +527,15 @@ cudaError_t launch_route_tc(const RouteArgs& a, cudaStream_t s) {
         !make_tmap_bf16(&tmW, a.w, (uint64_t)a.d, (uint64_t)a.E, 1, (uint32_t)p.Np, 2))
         return cudaErrorInvalidValue;
     const int smem = p.stages * p.stage_bytes + extra;
-    static int attr_bytes = 0;
-    if (attr_bytes < smem) {
+    // the shared-memory limit is a per-device function attribute: raise it once per
+    // device to the largest size used so far
+    constexpr int kDevs = 64;
+    static int attr_bytes[kDevs] = {};
+    if (dev < 0 || dev >= kDevs || attr_bytes[dev] < smem) {
         cudaError_t e =
             cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        attr_bytes = smem;
+        if (dev >= 0 && dev < kDevs) attr_bytes[dev] = smem;
     }
     route_tc_kernel<<<grid, 64 + 128 * p.epi_groups, smem, s>>>(tmX, tmW, p);
     return cudaGetLastError();
