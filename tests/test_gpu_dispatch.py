@@ -58,6 +58,8 @@ def _compare(cfg, x, idx, out, check_xp_full=True):
     (5000, 64, 8, 8, 1, 0.0, 0, 0.0),     # k = E: every expert takes every token
     (2048, 64, 32, 3, 32, 0.0, 7, 0.5),   # 32 virtual ranks, explicit capacity
     (257, 64, 3, 1, 3, 0.0, 0, 0.0),      # odd expert count
+    (100, 64, 1, 1, 1, 0.0, 0, 0.0),      # a single expert
+    (100, 64, 1, 1, 1, 0.0, 10, 0.0),     # a single expert keeping its first 10 tokens
     # few token blocks with long rows: each block's row copies split over column chunks
     (300, 7168, 256, 8, 8, 0.0, 0, 0.5),
     (129, 4096, 8, 2, 8, 0.0, 0, 0.0),
