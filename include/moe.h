@@ -62,7 +62,7 @@ enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1, MOE_ACT_IDENTITY = 2 };
 
 /* Bits of the device status word (first 4 bytes of the workspace). */
 /* 0x1u: unused */
-#define MOE_DEV_GEMM_TIMEOUT 0x2u     /* expert GEMM pipeline wait gave up */
+#define MOE_DEV_GEMM_TIMEOUT 0x2u     /* a tensor-core pipeline wait (expert GEMM or router) gave up */
 #define MOE_DEV_BAD_INDEX 0x4u        /* an expert index outside [0, E) reached dispatch */
 
 /*
