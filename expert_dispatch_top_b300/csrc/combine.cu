@@ -9,8 +9,10 @@
 //
 // One warp per token, grid-stride; each lane moves 16-byte vectors.  The k
 // expert rows of a token, for U column vectors at a time, are independent
-// loads issued back to back (8 in flight per lane); fp32 accumulation in slot
-// order, one rounding to the output type.
+// loads issued back to back (8 in flight per lane); with one vector per step
+// (k > 4) and a shared-expert or residual row to add, those rows' vectors
+// join the same batch (PRE) instead of costing a second round trip.  fp32
+// accumulation in slot order, one rounding to the output type.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -19,7 +21,7 @@ namespace {
 
 // KMAX: compile-time bound on k; U: 16-byte column vectors per lane in flight.
 // U * KMAX = 8 keeps eight independent row loads in flight per lane.
-template <typename T, int KMAX, int U>
+template <typename T, int KMAX, int U, bool PRE>
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     constexpr int V = Elem<T>::kPerVec;
     const int lane = threadIdx.x & 31;
@@ -48,6 +50,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
         }
         for (int c0 = lane; c0 < nvec; c0 += 32 * U) {
             uint4 v[U][KMAX];
+            uint4 vs = make_uint4(0u, 0u, 0u, 0u), vr = vs;  // PRE: shared / residual vectors
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int c = c0 + 32 * u;
@@ -55,6 +58,8 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
                 for (int j = 0; j < KMAX; ++j)
                     if (c < nvec && r[j] >= 0)
                         v[u][j] = ld_nc_v4(yp + (int64_t)r[j] * row_bytes + (int64_t)c * 16);
+                if (PRE && c < nvec && sh) vs = ld_nc_v4(sh + t * row_bytes + (int64_t)c * 16);
+                if (PRE && c < nvec && rs) vr = ld_nc_v4(rs + t * row_bytes + (int64_t)c * 16);
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -73,13 +78,13 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
                     }
                 if (sh) {
                     float f[V];
-                    Elem<T>::unpack(ld_nc_v4(sh + t * row_bytes + (int64_t)c * 16), f);
+                    Elem<T>::unpack(PRE ? vs : ld_nc_v4(sh + t * row_bytes + (int64_t)c * 16), f);
 #pragma unroll
                     for (int q = 0; q < V; ++q) acc[q] += f[q];
                 }
                 if (rs) {
                     float f[V];
-                    Elem<T>::unpack(ld_nc_v4(rs + t * row_bytes + (int64_t)c * 16), f);
+                    Elem<T>::unpack(PRE ? vr : ld_nc_v4(rs + t * row_bytes + (int64_t)c * 16), f);
 #pragma unroll
                     for (int q = 0; q < V; ++q) acc[q] += f[q];
                 }
@@ -92,11 +97,13 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
 template <typename T>
 void launch_combine_typed(const CombineArgs& a, unsigned blocks, cudaStream_t s) {
     if (a.k <= 2)
-        combine_kernel<T, 2, 4><<<blocks, 256, 0, s>>>(a);
+        combine_kernel<T, 2, 4, false><<<blocks, 256, 0, s>>>(a);
     else if (a.k <= 4)
-        combine_kernel<T, 4, 2><<<blocks, 256, 0, s>>>(a);
+        combine_kernel<T, 4, 2, false><<<blocks, 256, 0, s>>>(a);
+    else if (a.shared || a.resid)
+        combine_kernel<T, 8, 1, true><<<blocks, 256, 0, s>>>(a);
     else
-        combine_kernel<T, 8, 1><<<blocks, 256, 0, s>>>(a);
+        combine_kernel<T, 8, 1, false><<<blocks, 256, 0, s>>>(a);
 }
 
 // Backward of combine, one warp per token: for every kept slot j,
