@@ -515,13 +515,21 @@ cudaError_t launch_route_tc(const RouteArgs& a, cudaStream_t s) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int grid = p.m_tiles < sms ? p.m_tiles : sms;
-    // a second epilogue group pays off once CTAs have several tiles each
-    p.epi_groups = (p.max_ranks == 0 && p.m_tiles >= 2 * grid) ? 2 : 1;
-    const int extra = R_SMEM_FIXED + 128 * p.epi_groups * p.stash_pitch * 4;
-    const int ring = (R_SMEM_MAX - extra) < R_SMEM_TILES ? (R_SMEM_MAX - extra) : R_SMEM_TILES;
     p.stage_bytes = RM * RK * 2 + p.Np * RK * 2;
-    p.stages = ring / p.stage_bytes;
-    if (p.stages > R_MAX_STAGES) p.stages = R_MAX_STAGES;
+    auto stages_for = [&](int groups) {
+        const int extra = R_SMEM_FIXED + 128 * groups * p.stash_pitch * 4;
+        const int ring = (R_SMEM_MAX - extra) < R_SMEM_TILES ? (R_SMEM_MAX - extra) : R_SMEM_TILES;
+        const int st = ring / p.stage_bytes;
+        return st < R_MAX_STAGES ? st : R_MAX_STAGES;
+    };
+    // A second epilogue group overlaps the epilogues of a CTA's tiles.  It pays
+    // off once CTAs average two tiles; with fewer, only if its stash leaves the
+    // TMA ring at least 4 stages deep (small E: stages are small).
+    p.epi_groups = (p.max_ranks == 0 && (p.m_tiles >= 2 * grid ||
+                                         (p.m_tiles > grid && stages_for(2) >= 4)))
+                       ? 2 : 1;
+    const int extra = R_SMEM_FIXED + 128 * p.epi_groups * p.stash_pitch * 4;
+    p.stages = stages_for(p.epi_groups);
     CUtensorMap tmX, tmW;
     if (!make_tmap_bf16(&tmX, a.x, (uint64_t)a.d, (uint64_t)a.T, 1, RM, 2) ||
         !make_tmap_bf16(&tmW, a.w, (uint64_t)a.d, (uint64_t)a.E, 1, (uint32_t)p.Np, 2))
