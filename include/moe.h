@@ -49,7 +49,7 @@ typedef struct CUstream_st* moe_stream_t;
 typedef enum moe_status {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or limit */
-    MOE_ERR_UNSUPPORTED = 2,  /* a valid combination this build does not run */
+    MOE_ERR_UNSUPPORTED = 2,  /* a valid combination this library does not run */
     MOE_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
     MOE_ERR_TIMEOUT = 4,      /* a bounded device wait gave up (status word) */
     MOE_ERR_NONFINITE = 5,    /* reserved: non-finite input detected */

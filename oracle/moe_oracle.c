@@ -27,7 +27,7 @@
  * Inputs on the dyadic grid (x multiples of 1/8, weights multiples of 1/512,
  * d <= 8192) make every partial sum exact, so L does not depend on the order.
  *
- * Readings taken where the pages are silent (all listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - ties in the selection key go to the lower expert index;
  *   - capacity C = ceil(cf * T * k / E) (Ultralytics "Load Balancing and
  *     Capacity": a fixed number of tokens per expert, e.g. 1.25x the even

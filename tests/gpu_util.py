@@ -1,7 +1,7 @@
 """Helpers shared by the GPU parity tests: run one step of the CUDA library
 through the C ABI, and compare with the oracle under the tolerances below.
 
-Tolerances (derived in DESIGN.md, "Parity bar"):
+Tolerances:
   * indices, counts, offsets, rows, drop decisions, xp bytes: exact;
   * gates (fp32): |g - g_ref| <= (4 + n_terms) * 2^-23 * |g_ref|, n_terms = k
     (renormalised) or E (full softmax);

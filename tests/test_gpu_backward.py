@@ -1,7 +1,7 @@
 """GPU parity of the backward of the two exchanges (moe_combine_backward,
 moe_dispatch_backward) against the oracle.
 
-Tolerances (derived in the design doc): d_yp = g*dy rounded once: relative
+Tolerances: d_yp = g*dy rounded once: relative
 2^-8 (bf16) or 2^-22 (fp32) per element; d_gate is an fp32 dot product of d
 terms: |err| <= 1e-5 * sum_c |dy_c * yp_c|; dx is a sum of <= k rows rounded
 once: per row 2^-7 (bf16) / 1e-6 (fp32) of max|ref row|."""
