@@ -162,3 +162,50 @@ def test_empty_batch_is_a_noop():
     c = _cfg(T=0)
     moe.moe_route(c, None, None, None, None, None, None, None, stream=0)
     moe.moe_combine(c, None, None, None, None, None, None, stream=0)
+
+
+def test_backward_scratch_size():
+    bf = _cfg(dtype="bf16", act="swiglu", d=512, d_ff=1024)
+    full = moe.moe_expert_ffn_backward_scratch_size(bf, True)
+    dgrad = moe.moe_expert_ffn_backward_scratch_size(bf, False)
+    assert full > dgrad > 0 and full % 256 == 0 and dgrad % 256 == 0
+    assert moe.moe_expert_ffn_backward_scratch_size(_cfg(k=0), True) == 0
+    assert moe.moe_expert_ffn_backward_scratch_size(_cfg(act="identity", d_ff=0), True) == 0
+    # more tokens, more scratch
+    assert moe.moe_expert_ffn_backward_scratch_size(_cfg(dtype="bf16", act="swiglu", T=8192), True) \
+        > moe.moe_expert_ffn_backward_scratch_size(_cfg(dtype="bf16", act="swiglu", T=4096), True)
+
+
+def test_backward_and_hooks_reject_bad_arguments_before_any_launch():
+    lib = moe.library()
+    c = _cfg(dtype="bf16", act="swiglu")
+    need = moe.moe_expert_ffn_backward_scratch_size(c, True)
+
+    def ffn_bwd(cfg, scratch, nbytes, d_w_up=0x7000, ws=0x9000):
+        return lib.moe_expert_ffn_backward(ctypes.byref(cfg), 0x1000, 0x2000, 0x3000, 0x4000,
+                                           0x5000, 0x6000, d_w_up, 0x8000, scratch,
+                                           ctypes.c_size_t(nbytes), ws, None)
+    assert ffn_bwd(c, 0x10000, need - 256) == moe.MOE_ERR_INVALID_ARG      # scratch too small
+    assert ffn_bwd(c, 0x10000 + 16, need) == moe.MOE_ERR_INVALID_ARG       # not 256-byte aligned
+    assert ffn_bwd(c, 0x10000, need, ws=None) == moe.MOE_ERR_INVALID_ARG   # no status word
+    assert ffn_bwd(c, 0x10000, need, d_w_up=0x7004) == moe.MOE_ERR_INVALID_ARG  # misaligned dW
+    ident = _cfg(act="identity", d_ff=0)
+    assert ffn_bwd(ident, 0, 0) == moe.MOE_ERR_INVALID_ARG   # identity experts have no weights
+    # failure-detection hook: K block in range, bounded limit, bf16 experts only
+    for kb, us in ((-1, 1000), (512 // 64, 1000), (0, 0), (0, 4000001)):
+        assert lib.moe_test_expert_ffn_stall(ctypes.byref(c), 0x1000, 0x2000, 0x3000, 0x4000, kb,
+                                             us, 0x9000, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_test_expert_ffn_stall(ctypes.byref(_cfg()), 0x1000, 0x2000, 0x3000, 0x4000, 0,
+                                         1000, 0x9000, None) == moe.MOE_ERR_UNSUPPORTED
+    # balancing step: the step size must be finite and non-negative
+    for gamma in (-1e-3, float("inf"), float("nan")):
+        assert lib.moe_update_sel_bias(ctypes.byref(c), 0x1000, 0x2000, ctypes.c_float(gamma),
+                                       None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_noalloc_dispatch_rejects_shapes_beyond_its_array():
+    lib = moe.library()
+    big = moe.make_config(131072, 7168, 256, 8, 8, 0, act="identity", score="sigmoid")
+    st = lib.moe_dispatch_noalloc(ctypes.byref(big), 0x1000, 0x2000, 0x3000, 0x4000, 0x5000,
+                                  0x6000, 0x7000, 0x8000, 0x9000, 0xa000, None, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
