@@ -93,8 +93,12 @@ moe_status check_ffn_config(const moe_config* c) {
     return MOE_OK;
 }
 
+// Each *_impl checks its arguments first and, unless check_only, enqueues its
+// kernels.  moe_layer_forward runs every step's checks before the first
+// launch, so an argument error never leaves part of the layer enqueued.
 moe_status route_impl(const moe_config* c, const void* x, const void* w, const float* lb,
-                      const float* sb, int32_t* idx, float* gate, void* ws, cudaStream_t s) {
+                      const float* sb, int32_t* idx, float* gate, void* ws, cudaStream_t s,
+                      bool check_only = false) {
     if (c->T == 0) return MOE_OK;
     if (!x || !w || !idx || !gate || !ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w) || !aligned4(idx) || !aligned4(gate) || !aligned4(lb) ||
@@ -103,6 +107,7 @@ moe_status route_impl(const moe_config* c, const void* x, const void* w, const f
     if (sb && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_UNSUPPORTED;
     const bool limited = c->max_ranks > 0 && c->max_ranks < c->R;
     if (limited && c->act_dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (check_only) return MOE_OK;
     RouteArgs a;
     a.x = x;
     a.w = w;
@@ -126,7 +131,7 @@ moe_status route_impl(const moe_config* c, const void* x, const void* w, const f
 moe_status dispatch_impl(const moe_config* c, const void* x, const int32_t* idx, void* xp,
                          int32_t* row_token, int32_t* slot_row, int32_t* counts, int32_t* offsets,
                          int32_t* rank_counts, int32_t* rank_splits, int32_t* n_dropped, void* ws,
-                         cudaStream_t s) {
+                         cudaStream_t s, bool check_only = false) {
     if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
     if (!counts || !offsets || !rank_counts || !n_dropped) return MOE_ERR_INVALID_ARG;
     if (c->T > 0 && (!x || !idx || !xp || !row_token || !slot_row)) return MOE_ERR_INVALID_ARG;
@@ -134,6 +139,7 @@ moe_status dispatch_impl(const moe_config* c, const void* x, const int32_t* idx,
         !aligned4(slot_row) || !aligned4(counts) || !aligned4(offsets) || !aligned4(rank_counts) ||
         !aligned4(rank_splits) || !aligned4(n_dropped))
         return MOE_ERR_INVALID_ARG;
+    if (check_only) return MOE_OK;
     const Layout L = layout_of(c);
     DispatchArgs a;
     a.x = x;
@@ -164,13 +170,13 @@ moe_status dispatch_impl(const moe_config* c, const void* x, const int32_t* idx,
 moe_status ffn_impl(const moe_config* c, const void* xp, const int32_t* offsets, const void* w_up,
                     const void* w_down, void* h, void* yp, const void* shared_x,
                     const void* shared_up, const void* shared_down, void* shared_h,
-                    void* shared_out, void* ws, cudaStream_t s) {
+                    void* shared_out, void* ws, cudaStream_t s, bool check_only = false) {
     if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
     const int64_t rows = max_rows_of(c);
     const int eb = elem_bytes(c);
     if (c->act == MOE_ACT_IDENTITY) {
         if (!xp || !yp) return rows == 0 ? MOE_OK : MOE_ERR_INVALID_ARG;
-        if (xp == yp || rows == 0) return MOE_OK;
+        if (xp == yp || rows == 0 || check_only) return MOE_OK;
         return cuda_status(cudaMemcpyAsync(yp, xp, (size_t)rows * c->d * eb,
                                            cudaMemcpyDeviceToDevice, s));
     }
@@ -187,39 +193,43 @@ moe_status ffn_impl(const moe_config* c, const void* xp, const int32_t* offsets,
     const Layout L = layout_of(c);
     uint32_t* status = at<uint32_t>(ws, L.status);
     const bool tc = c->act_dtype == MOE_DTYPE_BF16;
-    auto run = [&](const GemmArgs& g) -> cudaError_t {
-        return tc ? launch_gemm_tc(g, s) : launch_gemm_simt(g, s);
-    };
-    // One pass per expert group set: routed experts (device offsets), then the
-    // shared expert over all T rows of shared_x.
-    for (int pass = 0; pass < 1 + (c->n_shared == 1 ? 1 : 0); ++pass) {
+    // One up/down pair per expert set: routed experts (device offsets), then the
+    // shared expert over all T rows of shared_x.  Every pair is checked before
+    // the first launch.
+    const int npass = 1 + (c->n_shared == 1 ? 1 : 0);
+    GemmArgs up[2], down[2];
+    for (int pass = 0; pass < npass; ++pass) {
         const bool shared = pass == 1;
-        GemmArgs up;
-        up.A = shared ? shared_x : xp;
-        up.B = shared ? shared_up : w_up;
-        up.out = shared ? shared_h : h;
-        up.offsets = shared ? nullptr : offsets;
-        up.rows_cap = shared ? c->T : rows;
-        up.m_rows = shared ? c->T : 0;
-        up.G = shared ? 1 : c->E;
-        up.N = c->d_ff;
-        up.K = c->d;
-        up.epi = c->act == MOE_ACT_SWIGLU ? EPI_SWIGLU : EPI_GELU;
-        up.dtype = c->act_dtype;
-        up.status = status;
-        GemmArgs down = up;
-        down.A = shared ? shared_h : h;
-        down.B = shared ? shared_down : w_down;
-        down.out = shared ? shared_out : yp;
-        down.N = c->d;
-        down.K = c->d_ff;
-        down.epi = EPI_NONE;
-        if (up.rows_cap == 0) continue;
-        if (tc && (gemm_tc_supported(up) != 0 || gemm_tc_supported(down) != 0))
+        GemmArgs& u = up[pass];
+        u.A = shared ? shared_x : xp;
+        u.B = shared ? shared_up : w_up;
+        u.out = shared ? shared_h : h;
+        u.offsets = shared ? nullptr : offsets;
+        u.rows_cap = shared ? c->T : rows;
+        u.m_rows = shared ? c->T : 0;
+        u.G = shared ? 1 : c->E;
+        u.N = c->d_ff;
+        u.K = c->d;
+        u.epi = c->act == MOE_ACT_SWIGLU ? EPI_SWIGLU : EPI_GELU;
+        u.dtype = c->act_dtype;
+        u.status = status;
+        GemmArgs& dn = down[pass];
+        dn = u;
+        dn.A = shared ? shared_h : h;
+        dn.B = shared ? shared_down : w_down;
+        dn.out = shared ? shared_out : yp;
+        dn.N = c->d;
+        dn.K = c->d_ff;
+        dn.epi = EPI_NONE;
+        if (u.rows_cap > 0 && tc && (gemm_tc_supported(u) != 0 || gemm_tc_supported(dn) != 0))
             return MOE_ERR_UNSUPPORTED;
-        cudaError_t e = run(up);
+    }
+    if (check_only) return MOE_OK;
+    for (int pass = 0; pass < npass; ++pass) {
+        if (up[pass].rows_cap == 0) continue;
+        cudaError_t e = tc ? launch_gemm_tc(up[pass], s) : launch_gemm_simt(up[pass], s);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
-        e = run(down);
+        e = tc ? launch_gemm_tc(down[pass], s) : launch_gemm_simt(down[pass], s);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     return MOE_OK;
@@ -227,7 +237,7 @@ moe_status ffn_impl(const moe_config* c, const void* xp, const int32_t* offsets,
 
 moe_status combine_impl(const moe_config* c, const void* yp, const int32_t* slot_row,
                         const float* gate, const void* shared_out, const void* resid, void* y,
-                        cudaStream_t s) {
+                        cudaStream_t s, bool check_only = false) {
     if (c->T == 0) return MOE_OK;
     if (!yp || !slot_row || !gate || !y) return MOE_ERR_INVALID_ARG;
     if (c->add_residual && !resid) return MOE_ERR_INVALID_ARG;
@@ -235,6 +245,7 @@ moe_status combine_impl(const moe_config* c, const void* yp, const int32_t* slot
     if (!aligned16(yp) || !aligned16(y) || !aligned16(shared_out) || !aligned16(resid) ||
         !aligned4(slot_row) || !aligned4(gate))
         return MOE_ERR_INVALID_ARG;
+    if (check_only) return MOE_OK;
     CombineArgs a;
     a.yp = yp;
     a.slot_row = slot_row;
@@ -401,19 +412,24 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w
         return MOE_ERR_INVALID_ARG;
     if (!y || (cfg->T > 0 && !x)) return MOE_ERR_INVALID_ARG;
 
-    st = route_impl(cfg, x, w_router, logit_bias, sel_bias, idx, gate, ws, s);
-    if (st != MOE_OK) return st;
-    st = dispatch_impl(cfg, x, idx, buf->xp, row_token, slot_row, counts, offsets, rank_counts,
-                       rank_splits, n_dropped, ws, s);
-    if (st != MOE_OK) return st;
-    const void* yp = buf->xp;
-    if (!identity) {
-        st = ffn_impl(cfg, buf->xp, offsets, w_up, w_down, buf->h, buf->yp, x, shared_up, shared_down,
-                      buf->shared_h, buf->shared_out, ws, s);
+    // Every step's checks first: an argument error returns before any launch.
+    const void* yp = identity ? buf->xp : buf->yp;
+    for (int pass = 0; pass < 2; ++pass) {
+        const bool check = pass == 0;
+        st = route_impl(cfg, x, w_router, logit_bias, sel_bias, idx, gate, ws, s, check);
         if (st != MOE_OK) return st;
-        yp = buf->yp;
+        st = dispatch_impl(cfg, x, idx, buf->xp, row_token, slot_row, counts, offsets, rank_counts,
+                           rank_splits, n_dropped, ws, s, check);
+        if (st != MOE_OK) return st;
+        if (!identity) {
+            st = ffn_impl(cfg, buf->xp, offsets, w_up, w_down, buf->h, buf->yp, x, shared_up,
+                          shared_down, buf->shared_h, buf->shared_out, ws, s, check);
+            if (st != MOE_OK) return st;
+        }
+        st = combine_impl(cfg, yp, slot_row, gate, buf->shared_out, x, y, s, check);
+        if (st != MOE_OK) return st;
     }
-    return combine_impl(cfg, yp, slot_row, gate, buf->shared_out, x, y, s);
+    return MOE_OK;
 }
 
 moe_status moe_combine_backward(const moe_config* cfg, const void* dy, const void* yp,

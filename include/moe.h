@@ -30,8 +30,11 @@
  *    moe_read_device_status.  No entry point traps, aborts or throws.
  *  - Calls on different streams need separate workspaces.
  *
- * Limits: 1 <= T, T*k < 2^30; 1 <= k <= min(E, 8); 1 <= E <= 256; R >= 1 and
- * E % R == 0; d and d_ff multiples of 64 for bf16 (4 for fp32); d <= 16384.
+ * Limits: 0 <= T, T*k < 2^30; 1 <= k <= min(E, 8); 1 <= E <= 256; 1 <= R <= 32
+ * and E % R == 0; d <= 16384; d a multiple of 8 for bf16 (4 for fp32), and
+ * with bf16 GELU or SwiGLU experts d and d_ff multiples of 64
+ * (MOE_ERR_UNSUPPORTED otherwise).  moe_layer_forward checks the arguments of
+ * all four steps before it enqueues the first one.
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H

@@ -209,3 +209,50 @@ def test_noalloc_dispatch_rejects_shapes_beyond_its_array():
     st = lib.moe_dispatch_noalloc(ctypes.byref(big), 0x1000, 0x2000, 0x3000, 0x4000, 0x5000,
                                   0x6000, 0x7000, 0x8000, 0x9000, 0xa000, None, None)
     assert st == moe.MOE_ERR_INVALID_ARG
+
+
+def _layer_args(cfg, **over):
+    """Aligned stand-in device addresses for every moe_layer_forward argument
+    (never dereferenced: each case below must fail its checks first)."""
+    a = dict(x=0x10000, w_router=0x20000, logit_bias=None, sel_bias=None, w_up=0x30000,
+             w_down=0x40000, shared_up=None, shared_down=None, y=0x50000, ws=0x60000)
+    b = dict(xp=0x70000, h=0x80000, yp=0x90000, shared_h=None, shared_out=None)
+    if cfg.n_shared:
+        a.update(shared_up=0xa0000, shared_down=0xb0000)
+        b.update(shared_h=0xc0000, shared_out=0xd0000)
+    for key, v in over.items():
+        (a if key in a else b)[key] = v
+    buf = moe.moe_buffers(**b)
+    lib = moe.library()
+    return lib.moe_layer_forward(ctypes.byref(cfg), a["x"], a["w_router"], a["logit_bias"],
+                                 a["sel_bias"], a["w_up"], a["w_down"], a["shared_up"],
+                                 a["shared_down"], ctypes.byref(buf), a["y"], a["ws"], None)
+
+
+@pytest.mark.parametrize("dtype,act,n_shared", [("bf16", "swiglu", 1), ("bf16", "gelu", 0),
+                                                ("f32", "gelu", 0)])
+def test_layer_forward_rejects_every_argument_error_before_any_launch(dtype, act, n_shared):
+    """moe_layer_forward checks the arguments of all four steps before its
+    first launch.  On this GPU-less host a launch that went out would fail as
+    MOE_ERR_CUDA; each bad argument must instead come back as
+    MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED."""
+    import torch
+    c = _cfg(dtype=dtype, act=act, n_shared=n_shared, score="sigmoid" if n_shared else "softmax")
+    bad = [dict(w_up=None), dict(w_down=None), dict(w_up=0x30008), dict(yp=0x90008),
+           dict(h=0x80004), dict(y=0x50008), dict(xp=None), dict(ws=0x60008),
+           dict(w_router=None), dict(logit_bias=0x1002)]
+    if n_shared:
+        bad += [dict(shared_up=None), dict(shared_out=0xd0008), dict(shared_h=None)]
+    for over in bad:
+        assert _layer_args(c, **over) == moe.MOE_ERR_INVALID_ARG, over
+    # a selection-only bias with softmax scores is a valid call this library does not run
+    if not n_shared:
+        assert _layer_args(c, sel_bias=0x1000) == moe.MOE_ERR_UNSUPPORTED
+    # bf16 expert GEMMs take d and d_ff in multiples of 64
+    if dtype == "bf16":
+        assert _layer_args(_cfg(dtype=dtype, act=act, d=72)) == moe.MOE_ERR_UNSUPPORTED
+        assert _layer_args(_cfg(dtype=dtype, act=act, d_ff=1000)) == moe.MOE_ERR_UNSUPPORTED
+    if not torch.cuda.is_available():
+        # control: with every argument valid the call gets as far as a launch,
+        # which fails here for want of a device
+        assert _layer_args(c) == moe.MOE_ERR_CUDA

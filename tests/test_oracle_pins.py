@@ -407,6 +407,64 @@ def test_layer_matches_dense_mixture_definition():
         assert torch.allclose(out["y"][t], ref, rtol=1e-13, atol=1e-9)
 
 
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_layer_with_shared_expert_matches_dense_mixture_definition(act):
+    """One always-on shared expert (the DeepSeek-V3-shaped layer): y = sum_j
+    g_j FFN_{e_j}(x) + FFN_shared(x), token by token, from library matmuls.
+    The shared term has gate 1, is evaluated on the token's own x (not on a
+    row of the permuted buffer) and is added once.  Every pre-activation is
+    >= 48, where GELU(v) = v and silu(v) = v exactly in fp64, so each FFN is
+    plain matmuls (SwiGLU: the elementwise product of the gate and up
+    projections); all values are dyadic, so the fp64 sums are exact."""
+    T, d, E, k, f = 12, 24, 4, 2, 20
+    up = 2 * f if act == "swiglu" else f
+    g = torch.Generator().manual_seed(18)
+    x = 2 + torch.randint(0, 9, (T, d), generator=g).float() / 8
+    wr = torch.randint(-8, 9, (E, d), generator=g).float() / 64
+    w1 = 1 + torch.randint(0, 9, (E, up, d), generator=g).float() / 8
+    w2 = torch.randint(-8, 9, (E, d, f), generator=g).float() / 8
+    s1 = 1 + torch.randint(0, 9, (1, up, d), generator=g).float() / 8
+    s2 = torch.randint(-8, 9, (1, d, f), generator=g).float() / 8
+    out = oracle.layer_forward(x, wr, k=k, E=E, R=2, d_ff=f, act=act, w_up=w1, w_down=w2,
+                               shared_up=s1, shared_down=s2)
+    idx, gate = out["topk_idx"], out["topk_gate"]
+    assert (gate < 1).all()  # a shared term weighted by a routed gate would show
+
+    def ffn(xt, wu, wd):
+        pre = xt.double() @ wu.double().T
+        h = pre[:f] * pre[f:] if act == "swiglu" else pre
+        return h @ wd.double().T
+
+    for t in range(T):
+        ref = torch.zeros(d, dtype=torch.float64)
+        for j in range(k):
+            e = int(idx[t, j])
+            ref += float(gate[t, j]) * ffn(x[t], w1[e], w2[e])
+        ref += ffn(x[t], s1[0], s2[0])
+        assert torch.allclose(out["y"][t], ref, rtol=1e-13, atol=0), t
+
+
+def test_layer_shared_identity_expert_closed_form():
+    """Identity experts plus a shared identity expert: y = (sum_j g_j + 1) x.
+    Gates are full-softmax probabilities (no renormalisation), so sum_j g_j
+    differs from 1 and from every single gate."""
+    T, E, d, k = 40, 8, 16, 2
+    g = W._gen(33, "cpu")
+    x = W._grid_int((T, d), -8, 8, 8.0, g, "cpu")
+    wr = W._grid_int((E, d), -8, 8, 16.0, g, "cpu")
+    dummy = torch.zeros((1, 1, d))
+    out = oracle.layer_forward(x, wr, k=k, E=E, R=4, d_ff=0, act="identity", score="softmax",
+                               renorm=False, shared_up=dummy, shared_down=dummy)
+    gsum = out["topk_gate"].double().sum(1, keepdim=True)
+    assert (gsum < 0.99).any()
+    ref = (gsum + 1) * x.double()
+    assert torch.allclose(out["y"], ref, rtol=1e-14, atol=0)
+    # the same tokens through the residual path instead of the shared expert
+    res = oracle.layer_forward(x, wr, k=k, E=E, R=4, d_ff=0, act="identity", score="softmax",
+                               renorm=False, add_residual=True)
+    assert torch.allclose(res["y"], ref, rtol=1e-14, atol=0)
+
+
 def test_switch_workload_drop_fraction_in_band():
     """The Switch-shaped workload's Zipf(1.1) logit skew drops 5-20% of tokens
     at capacity factor 1.25 (its stated target band)."""
