@@ -7,14 +7,21 @@ Default workload: the Mixtral-8x7B-shaped layer (T=16384 tokens, d=4096, 8
 experts top-2, SwiGLU d_ff=14336, bf16, no dropping) on seeded synthetic
 inputs.  One JSON line is printed by rank 0.
 
-`value` is tokens/s of the whole layer with inputs resident in HBM (CUDA
-events around K back-to-back moe_layer_forward calls).  Inputs are larger
-than L2 (x 134 MB, weights 2.8 GB), so no explicit L2 flush is needed.
-`e2e` adds, every step, the pinned host->device copy of x and the
-device->host copy of y (double-buffered on a copy stream, as a serving loop
-would run them).  `roofline` is for the dominant kernel (the tcgen05
-grouped GEMM): algorithmic FLOPs / its measured time, against the measured
-sustained bf16 peak.  `cpu_baseline` is the CPU oracle timed on a bounded
+`value` is tokens/s of the whole layer with inputs resident in HBM: K
+back-to-back steps, each the four C-ABI calls that moe_layer_forward makes
+(moe_route, moe_dispatch, moe_expert_ffn, moe_combine) with CUDA events
+between them, so the per-kernel times in `kernels` come from the same timed
+pass and add up to the step.  Inputs are larger than L2 (x 134 MB, weights
+2.8 GB), so no explicit L2 flush is needed.  `layer_forward` repeats the K
+steps through the single moe_layer_forward call as a cross-check, with its
+own clock record.  `e2e` adds, every step, the pinned host->device copy of x
+and the device->host copy of y (double-buffered on a copy stream, as a
+serving loop would run them).  `roofline` is for the dominant kernel (the
+tcgen05 grouped GEMM): algorithmic FLOPs / its measured time, against the
+measured bf16 burst peak.  `configs` holds one record per other workload
+(the toy, Switch- and DeepSeek-shaped layers and the sweep's end points),
+each with its own timed steps, L2 flushed before every step, per-kernel
+rates and clock record.  `cpu_baseline` is the CPU oracle timed on a bounded
 sample of the same workload on this host's cores (N=1, rank 0).
 
 With --impl reference the CPU oracle itself is timed (on the host cores,
@@ -163,126 +170,90 @@ def layer_work(w, n_kept):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline and --impl reference)
 # ---------------------------------------------------------------------------
-def oracle_step(w, inp, rng_seed, route_tokens, ffn_experts, disp_tokens=None, comb_tokens=256):
-    """Time the oracle on a bounded sample and extrapolate to the workload:
-    route `route_tokens` tokens; dispatch and permute `disp_tokens` tokens
-    (all T by default); the expert FFN of `ffn_experts` experts with as many of
-    their rows as the oracle has threads (it parallelises one call over its
-    rows, and every expert of the full workload has far more rows than
-    threads); combine `comb_tokens` tokens.  Each phase is scaled linearly to
-    the full workload (the FFN by rows).  Returns (seconds for the whole
-    workload, description, per-phase seconds)."""
+def oracle_layer_sample(w, inp, n_tokens, seed):
+    """One oracle step: the whole layer (route, dispatch, expert FFN, combine)
+    with the workload's weights on `n_tokens` seeded tokens of its batch.
+    Every step of the oracle costs time in proportion to the tokens it
+    processes (capacity, if any, is computed for the sample's own size), so
+    tokens / seconds is its measured throughput on this workload.  Returns
+    seconds."""
     import torch
 
-    import moe_workloads as W
     import oracle
-    T = w.T
-    g = torch.Generator().manual_seed(rng_seed)
-    rs = torch.randperm(T, generator=g)[:route_tokens]
+    g = torch.Generator().manual_seed(seed)
+    toks = torch.sort(torch.randperm(w.T, generator=g)[:max(1, min(w.T, n_tokens))]).values
+    x = inp["x"][toks]
     t0 = time.perf_counter()
-    oracle.route(inp["x"][rs], inp["w_router"], w.k, w.score, w.renorm, inp["logit_bias"],
-                 inp["sel_bias"])
-    t_route = (time.perf_counter() - t0) * T / len(rs)
-    # dispatch needs every sampled token's choice: take seeded choices of the same shape
-    nd = T if disp_tokens is None else max(1, min(T, disp_tokens))
-    ds = torch.sort(torch.randperm(T, generator=g)[:nd]).values
-    idx = W.random_topk(nd, w.E, w.k, seed=rng_seed)
-    C = oracle.capacity(nd, w.k, w.E, w.capacity_factor)
-    xs = inp["x"] if nd == T else inp["x"][ds]
-    t0 = time.perf_counter()
-    disp = oracle.dispatch(idx, w.E, w.R, C)
-    xp = oracle.permute(xs, disp["slot_row"], disp["rows"])
-    t_disp = (time.perf_counter() - t0) * T / nd
-    full_rows = disp["rows"] * T / nd  # kept rows of the whole workload, estimated
-    t_ffn = 0.0
-    n_rows_s = 0
-    n_exp = 0
-    off = disp["expert_offsets"]
-    rows_per_call = oracle.num_threads()
-    yp = torch.zeros((max(disp["rows"], 1), w.d), dtype=torch.float64)
-    if w.act != "identity":
-        order = torch.randperm(w.E, generator=g).tolist()
-        t0 = time.perf_counter()
-        for e in order:
-            lo, hi = int(off[e]), int(off[e + 1])
-            if hi == lo:
-                continue
-            n = min(rows_per_call, hi - lo)
-            yp[lo:lo + n] = oracle.expert_ffn(xp[lo:lo + n], inp["w_up"][e], inp["w_down"][e],
-                                              w.act, w.d_ff)
-            n_rows_s += n
-            n_exp += 1
-            if n_exp == ffn_experts:
-                break
-        t_ffn = (time.perf_counter() - t0) * full_rows / max(n_rows_s, 1)
-    else:
-        yp = xp.double()
-    row_map = torch.arange(max(disp["rows"], 1), dtype=torch.int32)
-    fs = torch.randperm(nd, generator=g)[:max(1, min(nd, comb_tokens))]
-    t0 = time.perf_counter()
-    oracle.combine(fs, yp, row_map, disp["slot_row"], torch.rand((nd, w.k), generator=g))
-    t_comb = (time.perf_counter() - t0) * T / len(fs)
-    total = t_route + t_disp + t_ffn + t_comb
-    desc = (f"route {len(rs)} of {T} tokens, dispatch+permute {nd} of {T}, expert FFN on "
-            f"{n_rows_s} rows ({n_exp} experts x up to {rows_per_call} rows, one row per oracle "
-            f"thread), combine {len(fs)} tokens; each phase extrapolated linearly to the full "
-            f"workload")
-    return total, desc, dict(route=t_route, dispatch=t_disp, ffn=t_ffn, combine=t_comb)
+    oracle.layer_forward(x, inp["w_router"], k=w.k, E=w.E, R=w.R, d_ff=w.d_ff, act=w.act,
+                         score=w.score, renorm=w.renorm, capacity_factor=w.capacity_factor,
+                         logit_bias=inp.get("logit_bias"), sel_bias=inp.get("sel_bias"),
+                         w_up=inp.get("w_up"), w_down=inp.get("w_down"),
+                         shared_up=inp.get("shared_up"), shared_down=inp.get("shared_down"),
+                         add_residual=w.add_residual, max_ranks=w.max_ranks)
+    return time.perf_counter() - t0
 
 
-def cpu_inputs(w, dev_inp=None):
-    import torch
+def oracle_tokens_for(w, inp, seconds):
+    """Tokens per oracle step so that one step takes about `seconds` (from a
+    calibration step on one token per oracle thread)."""
+    import oracle
+    n0 = max(1, min(w.T, oracle.num_threads()))
+    t = oracle_layer_sample(w, inp, n0, 12345)
+    return int(max(1, min(w.T, seconds * n0 / max(t, 1e-6))))
 
+
+def oracle_sample_desc(w, n):
+    return (f"the whole layer (route, dispatch, expert FFN, combine) on {n} seeded tokens of "
+            f"the {w.T}-token batch per step, with the workload's full weights; measured, not "
+            f"extrapolated (the oracle's work is linear in tokens)")
+
+
+def cpu_inputs(w):
     import moe_workloads as W
-    if dev_inp is not None:
-        return {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in dev_inp.items()}
     return W.make_inputs(w, device="cpu")
 
 
 def run_reference(args, w):
-    """The oracle as it stands, on the host cores, one bounded sample per step,
-    sized so that all warm-up and timed steps together take about
-    --ref-budget-s seconds (or one minimal sample per step, if even that is
-    over budget)."""
+    """The oracle as it stands, on the host cores: each step is the whole layer
+    on a seeded token sample, sized so that all warm-up and timed steps take
+    about --ref-budget-s seconds together."""
     import oracle
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     inp = cpu_inputs(w)
-    # Calibration step (one of the warm-up steps) with one expert's FFN sample;
-    # the FFN is nearly all of the oracle's time, so only the number of sampled
-    # experts grows to fill the per-step budget.
-    rt, dt, fe = min(w.T, 256), min(w.T, 2048), 1
-    t0 = time.perf_counter()
-    oracle_step(w, inp, 99, rt, fe, dt)
-    cal = time.perf_counter() - t0
     per_step = args.ref_budget_s / max(1, args.steps + args.warmup)
-    if cal < per_step:
-        fe = int(max(1, min(args.ref_ffn_experts, w.E, per_step / cal)))
-    for i in range(max(0, args.warmup - 1)):
-        oracle_step(w, inp, 100 + i, rt, fe, dt)
+    n = oracle_tokens_for(w, inp, per_step)
+    for i in range(max(0, args.warmup - 1)):  # the calibration step was the first warm-up
+        oracle_layer_sample(w, inp, n, 100 + i)
     times = []
-    desc = ""
     t_wall = time.perf_counter()
     for i in range(args.steps):
-        t, desc, _ = oracle_step(w, inp, 1000 + i, rt, fe, dt)
-        times.append(t)
+        times.append(oracle_layer_sample(w, inp, n, 1000 + i))
     wall = time.perf_counter() - t_wall
-    per_step = statistics.mean(times)
-    value = w.T / per_step
+    ms = statistics.mean(times) * 1e3
+    value = n / (ms / 1e3)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded dyadic grid)",
-        "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.d_ff,
-                   "act": w.act},
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded dyadic grid; no dataset)",
+        "config": workload_config(w, None, 1),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
-                         "kind": "oracle", "sample": desc},
+                         "kind": "oracle", "sample": oracle_sample_desc(w, n),
+                         "tokens_per_step": n},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "sample_wall_s": wall,
     }
     print(json.dumps(line), flush=True)
+
+
+def workload_config(w, n_kept, world):
+    return {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "R": w.R,
+            "d_ff": w.d_ff, "act": w.act, "score": w.score, "max_ranks": w.max_ranks,
+            "capacity_factor": w.capacity_factor, "n_shared": w.n_shared,
+            "parallelism": f"replicas x{world}" if world > 1 else "none",
+            "l2": "inputs larger than L2 (x and expert weights); no flush"}
 
 
 # ---------------------------------------------------------------------------
@@ -335,6 +306,152 @@ def time_ffn_backward(args, w, cfg, b, inp, stream, peaks):
     return out
 
 
+def _phase_calls(moe, cfg, w, inp, b, x):
+    """The layer step as its four C-ABI calls (what moe_layer_forward enqueues),
+    so that events can sit between them."""
+    ident = w.act == "identity"
+
+    def route():
+        moe.moe_route(cfg, x, inp["w_router"], inp.get("logit_bias"), inp.get("sel_bias"),
+                      b.topk_idx, b.topk_gate, b.ws)
+
+    def dispatch():
+        moe.moe_dispatch(cfg, x, b.topk_idx, b.xp, b.row_token, b.slot_row, b.expert_counts,
+                         b.expert_offsets, b.rank_counts, b.rank_splits, b.n_dropped, b.ws)
+
+    def ffn():
+        if not ident:
+            moe.moe_expert_ffn(cfg, b.xp, b.expert_offsets, inp["w_up"], inp["w_down"], b.h, b.yp,
+                               x if w.n_shared else None, inp.get("shared_up"),
+                               inp.get("shared_down"), b.shared_h, b.shared_out, b.ws)
+
+    def combine():
+        moe.moe_combine(cfg, b.xp if ident else b.yp, b.slot_row, b.topk_gate, b.shared_out,
+                        x if w.add_residual else None, b.y)
+
+    return [("route", route), ("dispatch", dispatch), ("ffn", ffn), ("combine", combine)]
+
+
+def timed_steps(steps, phases, stream, flush=None, barrier=lambda: None):
+    """K steps of the layer, each its four calls with a CUDA event before the
+    first and after each one, on the launching stream.  With `flush`, a
+    buffer larger than L2 is written before every step (outside the step's
+    events).  Returns (bracket ms over all K steps, per-step ms, per-phase
+    mean ms)."""
+    import torch
+    n = len(phases)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for s in range(steps):
+        if flush is not None:
+            flush()
+        e = evs[s]
+        e[0].record(stream)
+        for i, (_, f) in enumerate(phases):
+            f()
+            e[i + 1].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    per_step = [evs[s][0].elapsed_time(evs[s][n]) for s in range(steps)]
+    phase = {name: statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps))
+             for i, (name, _) in enumerate(phases)}
+    return ev0.elapsed_time(ev1), per_step, phase
+
+
+def kernel_report(w, work, phase, peaks, sms):
+    """Per-kernel times of one timed pass, with rates against their bounds."""
+    ident = w.act == "identity"
+    k = {
+        "route": {"ms": phase["route"],
+                  "GB/s": work["route_bytes"] / (phase["route"] * 1e-3) / 1e9,
+                  "TFLOP/s": work["route_flops"] / (phase["route"] * 1e-3) / 1e12},
+        "dispatch": {"ms": phase["dispatch"],
+                     "GB/s": work["permute_bytes"] / (phase["dispatch"] * 1e-3) / 1e9},
+        "combine": {"ms": phase["combine"],
+                    "GB/s": work["combine_bytes"] / (phase["combine"] * 1e-3) / 1e9},
+    }
+    for name in ("route", "dispatch", "combine"):
+        k[name]["frac_hbm"] = k[name]["GB/s"] / peaks["hbm"]
+    # bf16 routers run on the tensor cores (a short kernel: burst peak), fp32 ones on FFMA
+    if w.dtype == "bf16":
+        k["route"]["pipe"] = "tensor (bf16)"
+        k["route"]["frac_tensor"] = k["route"]["TFLOP/s"] / peaks["bf16"]
+    else:
+        k["route"]["pipe"] = "FFMA (fp32)"
+        k["route"]["frac_fp32_ffma"] = k["route"]["TFLOP/s"] / \
+            fp32_ffma_peak_tflops(sms, peaks["sm_mhz"])
+    if not ident:
+        tf = work["ffn_flops"] / (phase["ffn"] * 1e-3) / 1e12
+        k["ffn"] = {"ms": phase["ffn"], "TFLOP/s": tf, "launches_per_step": 2 * (1 + w.n_shared)}
+        if w.dtype == "bf16":
+            k["ffn"]["frac_bf16_burst"] = tf / peaks["bf16"]
+            k["ffn"]["frac_bf16_sustained"] = tf / peaks["bf16_sus"]
+        else:
+            k["ffn"]["frac_fp32_ffma"] = tf / fp32_ffma_peak_tflops(sms, peaks["sm_mhz"])
+    else:
+        moved = work["route_bytes"] + work["permute_bytes"] + work["combine_bytes"]
+        ms = phase["route"] + phase["dispatch"] + phase["combine"]
+        k["route_permute_unpermute"] = {"ms": ms, "GB/s": moved / (ms * 1e-3) / 1e9,
+                                        "frac_hbm": moved / (ms * 1e-3) / 1e9 / peaks["hbm"]}
+    return k
+
+
+class L2Flush:
+    """Writes a 512 MiB buffer (over 4x the 126 MB L2) before each timed step."""
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.v = 0
+
+    def __call__(self):
+        self.v ^= 1
+        self.buf.fill_(self.v)
+
+
+def measure_config(moe, W, w, dev, stream, peaks, sms, uuid, target_ms=400.0):
+    """One per-config record for the bench line: inputs drawn on the device,
+    3 warm-up steps, then K steps (K sized to ~target_ms of step time, 20..200)
+    with L2 flushed before each step; the four calls timed with events, clocks
+    sampled during the timed steps."""
+    import torch
+    inp = W.make_inputs(w, device=dev)
+    cfg = moe.config_from_workload(w)
+    b = moe.alloc_buffers(cfg, dev)
+    x = inp["x"]
+    phases = _phase_calls(moe, cfg, w, inp, b, x)
+    flush = L2Flush(dev)
+    _, per, _ = timed_steps(3, phases, stream, flush)
+    assert moe.moe_read_device_status(b.ws) == 0
+    steps = int(max(20, min(200, target_ms / max(statistics.median(per), 1e-3))))
+    with ClockSampler(uuid) as clk:
+        _, per, phase = timed_steps(steps, phases, stream, flush)
+    assert moe.moe_read_device_status(b.ws) == 0
+    n_kept = int(b.expert_offsets[-1].item())
+    ms = statistics.mean(per)
+    work = layer_work(w, n_kept)
+    rec = {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.d_ff,
+           "act": w.act, "dtype": w.dtype, "score": w.score, "n_shared": w.n_shared,
+           "capacity_factor": w.capacity_factor, "kept_rows": n_kept,
+           "dropped_frac": 1.0 - n_kept / (w.T * w.k), "steps": steps, "warmup": 3,
+           "ms_per_step": ms, "value": w.T / (ms * 1e-3), "unit": UNIT,
+           "l2": "flushed before every step (512 MiB write, outside the step's events)",
+           "kernels": kernel_report(w, work, phase, peaks, sms), "clocks": clk.summary(),
+           "gpu_launches": (5 + (0 if w.act == "identity" else 2 * (1 + w.n_shared))) * steps}
+    del inp, b, phases, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
+DEFAULT_CONFIGS = ["toy", "switch", "deepseek", "sweep_T4096_s0", "sweep_T4096_s1.5",
+                   "sweep_T131072_s0", "sweep_T131072_s1.5"]
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -350,6 +467,7 @@ def run_ours(args, w):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     peaks = _peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     inp = W.make_inputs(w, device=dev)
     cfg = moe.config_from_workload(w)
@@ -382,9 +500,21 @@ def run_ours(args, w):
     except Exception:
         pass
 
-    # ---- timed region: K whole-layer calls, inputs resident in HBM ----
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # ---- timed region: K layer steps, inputs resident in HBM.  Each step is
+    # the four C-ABI calls moe_layer_forward makes, with events between them,
+    # so the per-kernel times come from this same pass and add up to the step.
+    b = layer.buf
+    phases = _phase_calls(moe, cfg, w, inp, b, x)
     with ClockSampler(uuid if rank == 0 else None) as clk:
+        total_ms, per_step, phase = timed_steps(args.steps, phases, stream, None, barrier)
+    ms = max_over_ranks(total_ms) / args.steps
+    clocks = clk.summary() if rank == 0 else None
+    value = world * w.T / (ms / 1e3)
+    assert layer.device_status() == 0
+
+    # ---- cross-check: the same K steps through moe_layer_forward (one call) ----
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(uuid if rank == 0 else None) as clk2:
         barrier()
         torch.cuda.synchronize()
         ev0.record(stream)
@@ -393,36 +523,8 @@ def run_ours(args, w):
         ev1.record(stream)
         torch.cuda.synchronize()
         barrier()
-    ms = max_over_ranks(ev0.elapsed_time(ev1)) / args.steps
-    clocks = clk.summary() if rank == 0 else None
-    value = world * w.T / (ms / 1e3)
-
-    # ---- per-step breakdown: the same four C-ABI calls with events between ----
-    b = layer.buf
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for s in range(args.steps):
-        e = evs[s]
-        e[0].record(stream)
-        moe.moe_route(cfg, x, inp["w_router"], inp.get("logit_bias"), inp.get("sel_bias"),
-                      b.topk_idx, b.topk_gate, b.ws)
-        e[1].record(stream)
-        moe.moe_dispatch(cfg, x, b.topk_idx, b.xp, b.row_token, b.slot_row, b.expert_counts,
-                         b.expert_offsets, b.rank_counts, b.rank_splits, b.n_dropped, b.ws)
-        e[2].record(stream)
-        if not ident:
-            moe.moe_expert_ffn(cfg, b.xp, b.expert_offsets, inp["w_up"], inp["w_down"], b.h, b.yp,
-                               x if w.n_shared else None, inp.get("shared_up"),
-                               inp.get("shared_down"), b.shared_h, b.shared_out, b.ws)
-        e[3].record(stream)
-        moe.moe_combine(cfg, b.xp if ident else b.yp, b.slot_row, b.topk_gate, b.shared_out,
-                        x if w.add_residual else None, b.y)
-        e[4].record(stream)
-    torch.cuda.synchronize()
-    phase = {}
-    for i, name in enumerate(["route", "dispatch", "ffn", "combine"]):
-        phase[name] = statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1])
-                                      for s in range(args.steps))
+    lf_ms = max_over_ranks(ev0.elapsed_time(ev1)) / args.steps
+    lf_clocks = clk2.summary() if rank == 0 else None
     assert layer.device_status() == 0
 
     # ---- e2e: pinned host x in, y out, every step ----
@@ -481,22 +583,9 @@ def run_ours(args, w):
             dist.destroy_process_group()
         return
 
-    ffn_ms = phase["ffn"]
-    kernels = {
-        "route": {"ms": phase["route"],
-                  "GB/s": work["route_bytes"] / (phase["route"] * 1e-3) / 1e9,
-                  "TFLOP/s": work["route_flops"] / (phase["route"] * 1e-3) / 1e12},
-        "dispatch": {"ms": phase["dispatch"],
-                     "GB/s": work["permute_bytes"] / (phase["dispatch"] * 1e-3) / 1e9},
-        "combine": {"ms": phase["combine"],
-                    "GB/s": work["combine_bytes"] / (phase["combine"] * 1e-3) / 1e9},
-    }
-    for kname in ("dispatch", "combine"):
-        kernels[kname]["frac_hbm"] = kernels[kname]["GB/s"] / peaks["hbm"]
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    kernels = kernel_report(w, work, phase, peaks, sms)
+    phase_sum = sum(phase.values())
     if not ident:
-        kernels["ffn"] = {"ms": ffn_ms, "TFLOP/s": work["ffn_flops"] / (ffn_ms * 1e-3) / 1e12,
-                          "launches_per_step": 2 * (1 + w.n_shared)}
         achieved = kernels["ffn"]["TFLOP/s"]
         if w.dtype == "bf16":
             tr = TRAFFIC.get(w.name)
@@ -504,11 +593,12 @@ def run_ours(args, w):
             if tr and tr["src_hash"] == _src_hash(os.path.join(ROOT, "expert_dispatch_top_b300",
                                                                "csrc", "ffn_tc.cu")):
                 traffic = tr["bytes"]
+            # the FFN runs in ms-long windows between the other kernels: burst peak
             roofline = {"kernel": "tc_gemm_kernel (expert FFN, up+down per step)",
-                        "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sus"],
-                        "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sus"],
-                        "traffic": traffic, "peak_kind": f"bf16 sustained ({peaks['src']})",
-                        "frac_of_burst": achieved / peaks["bf16"],
+                        "bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
+                        "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
+                        "traffic": traffic, "peak_kind": f"bf16 burst ({peaks['src']})",
+                        "frac_of_sustained": achieved / peaks["bf16_sus"],
                         "algorithmic_flops_per_step": work["ffn_flops"]}
         else:
             pk = fp32_ffma_peak_tflops(sms, peaks["sm_mhz"])
@@ -525,40 +615,46 @@ def run_ours(args, w):
                     "algorithmic_bytes_per_step": work["permute_bytes"]}
     if args.backward and not ident:
         kernels["ffn_backward"] = time_ffn_backward(args, w, cfg, b, inp, stream, peaks)
-    # bf16 routers run on the tensor cores (a short kernel: burst peak), fp32 ones on FFMA
-    if w.dtype == "bf16":
-        kernels["route"]["pipe"] = "tensor (bf16)"
-        kernels["route"]["frac_tensor"] = kernels["route"]["TFLOP/s"] / peaks["bf16"]
-    else:
-        kernels["route"]["pipe"] = "FFMA (fp32)"
-        kernels["route"]["frac_fp32_ffma"] = kernels["route"]["TFLOP/s"] / \
-            fp32_ffma_peak_tflops(sms, peaks["sm_mhz"])
-    kernels["route"]["frac_hbm"] = kernels["route"]["GB/s"] / peaks["hbm"]
+
+    configs = None
+    if world == 1 and args.configs:
+        del layer, phases, xd, yd
+        inp = {kk: v for kk, v in inp.items() if kk == "x"}
+        torch.cuda.empty_cache()
+        configs = []
+        for name in [c for c in args.configs.split(",") if c]:
+            configs.append(measure_config(moe, W, W.get(name), dev, stream, peaks, sms, uuid))
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         import oracle
-        inp_cpu = cpu_inputs(w, inp)
-        t, desc, parts = oracle_step(w, inp_cpu, 7, args.ref_route_tokens, args.ref_ffn_experts)
-        cpu = {"value": w.T / t, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-               "sample": desc, "phase_s": parts}
+        inp_cpu = cpu_inputs(w)
+        n = oracle_tokens_for(w, inp_cpu, args.cpu_step_s)
+        ts = [oracle_layer_sample(w, inp_cpu, n, 7 + i) for i in range(2)]
+        cpu = {"value": n / statistics.mean(ts), "unit": UNIT, "cores": oracle.num_threads(),
+               "kind": "oracle", "sample": oracle_sample_desc(w, n) + "; 2 steps",
+               "tokens_per_step": n, "s_per_step": statistics.mean(ts)}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded dyadic grid; no dataset)",
-        "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "R": w.R,
-                   "d_ff": w.d_ff, "act": w.act, "score": w.score, "max_ranks": w.max_ranks,
-                   "capacity_factor": w.capacity_factor, "n_shared": w.n_shared,
-                   "kept_rows": n_kept, "parallelism": f"replicas x{world}" if world > 1 else "none",
-                   "l2": "inputs larger than L2 (x and expert weights); no flush"},
+        "config": dict(workload_config(w, n_kept, world), kept_rows=n_kept,
+                       timed_step="moe_route, moe_dispatch, moe_expert_ffn, moe_combine with CUDA "
+                                  "events between them (the calls moe_layer_forward makes)"),
         "e2e": {"value": world * w.T / (e2e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": bytes_in, "d2h_bytes_per_step": bytes_out,
+                "via": "MoeLayer -> moe_layer_forward",
                 "overlap": "double-buffered: H2D(i+1) and D2H(i-1) on a copy stream during step i"},
         "gpu_launches": per_step_launches * args.steps,
         "roofline": roofline,
         "kernels": kernels,
+        "phase_sum_ms": phase_sum,
+        "layer_forward": {"ms_per_step": lf_ms, "value": world * w.T / (lf_ms / 1e3),
+                          "unit": UNIT, "clocks": lf_clocks,
+                          "note": "same K steps through the single moe_layer_forward call"},
+        "configs": configs,
         "cpu_baseline": cpu,
         "clocks": clocks,
     }
@@ -579,11 +675,13 @@ def main():
     ap.add_argument("--max-ranks", type=int, default=-1, help="rank-limited routing (0: off)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", default=",".join(DEFAULT_CONFIGS),
+                    help="comma-separated workloads measured after the main line, each with its "
+                         "own timed steps and clocks ('' to skip)")
     ap.add_argument("--backward", action="store_true",
                     help="also time the expert-FFN backward (kernels.ffn_backward)")
-    ap.add_argument("--ref-route-tokens", type=int, default=256)
-    ap.add_argument("--ref-ffn-experts", type=int, default=8,
-                    help="experts whose FFN the oracle sample runs (rows: one per oracle thread)")
+    ap.add_argument("--cpu-step-s", type=float, default=8.0,
+                    help="host seconds per cpu_baseline step (the token sample is sized to fit)")
     ap.add_argument("--ref-budget-s", type=float, default=150.0,
                     help="host seconds for all --impl reference steps (samples are sized to fit)")
     args = ap.parse_args()

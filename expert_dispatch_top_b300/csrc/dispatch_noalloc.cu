@@ -12,13 +12,20 @@
 // The array is a static __device__ object: every GPU that loads the library
 // holds kScratchBytes of it until the process exits.  Host code cannot use
 // the array's name as a device address (in host code it names a host-side
-// stand-in), so the first call on each device, with that device current,
-// looks the address up with cudaGetSymbolAddress and caches it.  Every call
-// shares the one array and finds the previous call's contents in it; the
-// kernels write every part they read before reading it.
+// stand-in), so the first call in each CUDA context (with that context
+// current) looks the address up with cudaGetSymbolAddress and caches it under
+// the context's unique ID.  A context that is destroyed and created again
+// (cudaDeviceReset, or an engine that manages its own contexts through the
+// driver API) gets a new ID, and with it a fresh lookup: the library's module
+// may load at another address in the new context.  Every call shares the one
+// array and finds the previous call's contents in it; the kernels write every
+// part they read before reading it.
 // Calls that overlap on the GPU (different streams, or several host threads
 // without ordering) race on the array.
 #include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -33,24 +40,67 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_dispatch_scratch[kScratchBytes];
 
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void* addr;
+};
+ScratchEntry g_scratch_cache[kMaxDevices] = {};
+int g_scratch_next = 0;  // next entry to reuse once the cache is full
 
 inline size_t up256(size_t v) { return (v + kAlignNA - 1) / kAlignNA * kAlignNA; }
 
-// Device address of the scratch array on the current device (set up once).
-cudaError_t scratch_address(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+// Unique ID of the current CUDA context (driver entry points through the
+// runtime, so the library needs no -lcuda).  False if there is no current
+// context or the driver cannot say.
+bool current_context_id(unsigned long long* id) {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    if (!get_current || !get_id) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
+        void* q = nullptr;
+        cudaDriverEntryPointQueryResult r1, r2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &r1) !=
+                cudaSuccess ||
+            r1 != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) !=
+                cudaSuccess ||
+            r2 != cudaDriverEntryPointSuccess)
+            return false;
+        get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(q);
     }
-    *out = g_scratch_addr[dev];
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current context (looked up once
+// per context).
+cudaError_t scratch_address(void** out) {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    unsigned long long id = 0;
+    if (!current_context_id(&id)) {
+        // no current context yet: the runtime call below makes the device's
+        // primary context current, and the cache is keyed by that context
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+        if (e != cudaSuccess) return e;
+        if (!current_context_id(&id)) {
+            *out = p;
+            return cudaSuccess;
+        }
+    }
+    for (int i = 0; i < kMaxDevices; ++i)
+        if (g_scratch_cache[i].addr != nullptr && g_scratch_cache[i].ctx_id == id) {
+            *out = g_scratch_cache[i].addr;
+            return cudaSuccess;
+        }
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_cache[g_scratch_next] = ScratchEntry{id, p};
+    g_scratch_next = (g_scratch_next + 1) % kMaxDevices;
+    *out = p;
     return cudaSuccess;
 }
 

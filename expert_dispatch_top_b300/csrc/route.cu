@@ -349,12 +349,16 @@ cudaError_t launch_typed(const RouteArgs& a, cudaStream_t s) {
             route_big_kernel<T, 128><<<blocks, 256, B, s>>>(a);
         } else {
             constexpr int B = big_smem_bytes<256>();
-            static bool attr = false;
-            if (!attr) {
+            // the shared-memory limit is a per-device function attribute
+            constexpr int kDevs = 64;
+            static bool attr[kDevs] = {};
+            int dev = 0;
+            cudaGetDevice(&dev);
+            if (dev < 0 || dev >= kDevs || !attr[dev]) {
                 cudaError_t e = cudaFuncSetAttribute(route_big_kernel<T, 256>,
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, B);
                 if (e != cudaSuccess) return e;
-                attr = true;
+                if (dev >= 0 && dev < kDevs) attr[dev] = true;
             }
             route_big_kernel<T, 256><<<blocks, 256, B, s>>>(a);
         }

@@ -208,8 +208,11 @@ moe_status moe_test_expert_ffn_stall(const moe_config* cfg, const void* xp,
  *   each term rounded up to 256, must fit in 4 MiB (T*E <= ~16.7 million, e.g.
  *   T = 65536 with E = 128); larger shapes return MOE_ERR_INVALID_ARG before
  *   anything is enqueued.
- *   The first call on a device (with that device current) looks up the
- *   array's device address; make that first call before any stream capture.
+ *   The first call in each CUDA context (with that context current) looks up
+ *   the array's device address and caches it under the context's unique ID,
+ *   so a context created anew (after cudaDeviceReset, or by an engine that
+ *   manages its own contexts) is looked up again; make the first call in a
+ *   context before any stream capture.
  *   Every call shares the array and writes each part of it before reading
  *   it; calls that overlap on the GPU (other streams, unordered host threads)
  *   race on it.  Allocates nothing: no cudaMalloc, no cudaFree.

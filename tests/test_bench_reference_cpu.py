@@ -20,7 +20,13 @@ def test_reference_arm_prints_contract_line():
     assert line["config"]["workload"] == "toy"
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
-    assert "extrapolated" in cb["sample"]
+    assert "measured" in cb["sample"] and cb["tokens_per_step"] >= 1
+    # the reported per-step time is the time a step took (it fits in the run)
+    assert line["ms_per_step"] * line["steps"] <= line["sample_wall_s"] * 1e3 * 1.05 + 1.0
+    assert abs(line["value"] - cb["tokens_per_step"] / (line["ms_per_step"] / 1e3)) \
+        <= 1e-6 * line["value"]
+    for key in ("T", "d", "E", "k", "R", "d_ff", "act", "score", "capacity_factor", "n_shared"):
+        assert key in line["config"], key
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0

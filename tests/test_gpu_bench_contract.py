@@ -14,7 +14,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def test_bench_json_line():
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "toy", "--steps", "3",
-           "--warmup", "3", "--no-cpu-baseline"]
+           "--warmup", "3", "--no-cpu-baseline",
+           "--configs", "sweep_T4096_s0"]
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=900, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.strip().splitlines() if l.startswith("{")]
@@ -38,3 +39,14 @@ def test_bench_json_line():
     assert rf["bound"] == "alu" and rf["achieved"] > 0 and rf["peak"] > 0
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
     assert set(line["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+    # per-kernel times come from the timed pass and add up to at most the step
+    ks = line["kernels"]
+    assert abs(sum(ks[n]["ms"] for n in ("route", "dispatch", "ffn", "combine"))
+               - line["phase_sum_ms"]) < 1e-9
+    assert line["phase_sum_ms"] <= line["ms_per_step"] * 1.0001
+    lf = line["layer_forward"]
+    assert lf["ms_per_step"] > 0 and set(lf["clocks"]) >= {"sm_mhz", "reasons"}
+    (rec,) = line["configs"]
+    assert rec["workload"] == "sweep_T4096_s0" and rec["value"] > 0 and rec["steps"] >= 20
+    assert "route_permute_unpermute" in rec["kernels"] and "flushed" in rec["l2"]
+    assert set(rec["clocks"]) >= {"sm_mhz", "reasons"}

@@ -2,8 +2,9 @@
 the five workloads: routing/dispatch outputs bit-exact, layer outputs within
 the per-row tolerance (2e-2 bf16, 1e-4 fp32).  Small-T versions are checked
 on every token; full-size versions route and dispatch every token on both
-sides and compare the layer output on a seeded token sample plus every
-fully dropped token."""
+sides and compare the layer output on at least 256 tokens: a seeded sample,
+the tokens at both ends of every expert's rows and at its 128-row tile
+boundaries, and every fully dropped token."""
 import pytest
 import torch
 
@@ -89,16 +90,41 @@ def test_layer_identity_sweep_small(s):
     _compare(w, layer, y, ref, torch.arange(2048))
 
 
+def _stratified_tokens(layer, w, n_random, seed=17):
+    """Tokens whose layer outputs are compared at full size: a seeded random
+    sample, plus for every expert the tokens of its first and last rows and
+    (up to 64 experts) of the rows on both sides of its 128-row tile
+    boundaries (every 4th boundary for long experts), where the grouped GEMM's
+    tiles change."""
+    g = torch.Generator().manual_seed(seed)
+    picked = [torch.randperm(w.T, generator=g)[:n_random], torch.tensor([0, w.T - 1])]
+    offs = layer.buf.expert_offsets.cpu().tolist()
+    rt = layer.buf.row_token.cpu()
+    rows = []
+    for e in range(w.E):
+        lo, hi = offs[e], offs[e + 1]
+        if hi <= lo:
+            continue
+        rows += [lo, hi - 1]
+        if w.E > 64:
+            continue  # 256 small experts: both ends of each already give ~500 tokens
+        bounds = list(range(lo + 128, hi, 128))
+        step = 4 if len(bounds) > 8 else 1
+        for b in bounds[::step]:
+            rows += [b - 1, b]
+    picked.append(rt[torch.tensor(rows, dtype=torch.long)].long())
+    return torch.unique(torch.cat(picked))
+
+
 @pytest.mark.parametrize("name", ["toy", "switch", "deepseek", "mixtral"])
 def test_layer_full_size_sampled(name):
     w = W.WORKLOADS[name]
     inp_dev = W.make_inputs(w, device=DEV)
     inp = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in inp_dev.items()}
     layer, y = _run_layer(w, inp_dev, w.T, False)
-    n_samp = {"toy": 512, "switch": 256, "deepseek": 24, "mixtral": 12}[name]
-    g = torch.Generator().manual_seed(17)
-    toks = torch.randperm(w.T, generator=g)[:n_samp]
-    toks = torch.unique(torch.cat([toks, torch.tensor([0, w.T - 1])]))
+    n_random = {"toy": 512, "switch": 256, "deepseek": 96, "mixtral": 128}[name]
+    toks = _stratified_tokens(layer, w, n_random)
+    assert toks.numel() >= 256
     slot = layer.buf.slot_row.cpu()
     dropped = (slot < 0).all(1).nonzero().flatten()
     if dropped.numel():
