@@ -20,14 +20,17 @@ from typing import Optional
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_lib", "libmoe_b300.so")
+# MOE_B300_CHECKED=1 loads the range-checked debugging build instead.
+LIB_PATH = os.path.join(_PKG, "_lib", "libmoe_b300_checked.so"
+                        if os.environ.get("MOE_B300_CHECKED") == "1" else "libmoe_b300.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, \
     MOE_ERR_NONFINITE, MOE_ERR_BOUNDS = range(7)
 MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_ACT_GELU, MOE_ACT_SWIGLU, MOE_ACT_IDENTITY = 0, 1, 2
-MOE_DEV_GEMM_TIMEOUT, MOE_DEV_BAD_INDEX = 0x2, 0x4
+MOE_DEV_GEMM_TIMEOUT, MOE_DEV_BAD_INDEX, MOE_DEV_COPY_TIMEOUT, MOE_DEV_NONFINITE, MOE_DEV_BOUNDS = \
+    0x2, 0x4, 0x8, 0x10, 0x20
 
 _ACTS = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU, "identity": MOE_ACT_IDENTITY}
 _SCORES = {"softmax": MOE_SCORE_SOFTMAX, "sigmoid": MOE_SCORE_SIGMOID}
@@ -107,6 +110,8 @@ def _load():
     lib.moe_update_sel_bias.restype = i32
     lib.moe_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.moe_read_device_status.restype = i32
+    lib.moe_build_checked.argtypes = []
+    lib.moe_build_checked.restype = i32
     _lib = lib
     return lib
 
@@ -271,6 +276,11 @@ def moe_update_sel_bias(cfg, expert_counts, sel_bias, gamma, stream=None):
     _check(_load().moe_update_sel_bias(ctypes.byref(cfg), _p(expert_counts), _p(sel_bias),
                                        ctypes.c_float(gamma), _stream(stream)),
            "moe_update_sel_bias")
+
+
+def moe_build_checked() -> bool:
+    """True if the loaded library is the range-checked debugging build."""
+    return bool(_load().moe_build_checked())
 
 
 def moe_read_device_status(ws, stream=None) -> int:

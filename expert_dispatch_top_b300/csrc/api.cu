@@ -38,7 +38,7 @@ int64_t max_rows_of(const moe_config* c) {
 // Byte offsets of every workspace section.
 struct Layout {
     size_t status = 0;
-    size_t totals, hist, prefix, splits_acc;
+    size_t totals, hist, prefix, splits_acc, route_part, safe_offsets;
     size_t topk_idx, topk_gate, slot_row, row_token, expert_counts, offsets, rank_counts,
         rank_splits, n_dropped;
     size_t total;
@@ -55,6 +55,12 @@ Layout layout_of(const moe_config* c) {
     o = align_up(o + (size_t)dispatch_blocks(c->T) * c->E * 4);
     L.splits_acc = o;
     o = align_up(o + (size_t)c->R * c->R * 4);
+    // partial top-k lists of a bf16 router that splits its experts (small T)
+    L.route_part = o;
+    if (c->act_dtype == MOE_DTYPE_BF16) o = align_up(o + (size_t)route_partial_bytes(c->T, c->E));
+    // checked build: the sanitised copy of expert_offsets the FFN kernels read
+    L.safe_offsets = o;
+    o = align_up(o + (size_t)(c->E + 1) * 4);
     const size_t tk = (size_t)c->T * c->k;
     L.topk_idx = o;
     o = align_up(o + tk * 4);
@@ -106,8 +112,8 @@ moe_status route_impl(const moe_config* c, const void* x, const void* w, const f
         return MOE_ERR_INVALID_ARG;
     if (sb && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_UNSUPPORTED;
     const bool limited = c->max_ranks > 0 && c->max_ranks < c->R;
-    if (limited && c->act_dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
     if (check_only) return MOE_OK;
+    const Layout L0 = layout_of(c);
     RouteArgs a;
     a.x = x;
     a.w = w;
@@ -115,7 +121,7 @@ moe_status route_impl(const moe_config* c, const void* x, const void* w, const f
     a.sel_bias = sb;
     a.idx = idx;
     a.gate = gate;
-    a.status = at<uint32_t>(ws, layout_of(c).status);
+    a.status = at<uint32_t>(ws, L0.status);
     a.T = c->T;
     a.d = c->d;
     a.E = c->E;
@@ -125,6 +131,8 @@ moe_status route_impl(const moe_config* c, const void* x, const void* w, const f
     a.dtype = c->act_dtype;
     a.R = c->R;
     a.max_ranks = limited ? c->max_ranks : 0;
+    if (c->act_dtype == MOE_DTYPE_BF16 && route_partial_bytes(c->T, c->E) > 0)
+        a.part = at<RoutePartial>(ws, L0.route_part);
     return cuda_status(launch_route(a, s));
 }
 
@@ -193,6 +201,13 @@ moe_status ffn_impl(const moe_config* c, const void* xp, const int32_t* offsets,
     const Layout L = layout_of(c);
     uint32_t* status = at<uint32_t>(ws, L.status);
     const bool tc = c->act_dtype == MOE_DTYPE_BF16;
+    if (kChecked && !check_only) {
+        // checked build: the kernels read a copy made non-decreasing within the rows
+        int32_t* safe = at<int32_t>(ws, L.safe_offsets);
+        if (launch_sanitize_offsets(offsets, safe, c->E, rows, status, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        offsets = safe;
+    }
     // One up/down pair per expert set: routed experts (device offsets), then the
     // shared expert over all T rows of shared_x.  Every pair is checked before
     // the first launch.
@@ -257,6 +272,7 @@ moe_status combine_impl(const moe_config* c, const void* yp, const int32_t* slot
     a.d = c->d;
     a.k = c->k;
     a.dtype = c->act_dtype;
+    a.rows_cap = max_rows_of(c);
     return cuda_status(launch_combine(a, s));
 }
 
@@ -319,6 +335,7 @@ int64_t moe_max_rows(const moe_config* cfg) {
 moe_status moe_route(const moe_config* cfg, const void* x, const void* w_router,
                      const float* logit_bias, const float* sel_bias, int32_t* topk_idx,
                      float* topk_gate, void* ws, moe_stream_t stream) {
+    NvtxRange range("moe_route");
     moe_status st = moe_check_config(cfg);
     if (st != MOE_OK) return st;
     return route_impl(cfg, x, w_router, logit_bias, sel_bias, topk_idx, topk_gate, ws,
@@ -329,6 +346,7 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
                         int32_t* row_token, int32_t* slot_row, int32_t* expert_counts,
                         int32_t* expert_offsets, int32_t* rank_counts, int32_t* rank_splits,
                         int32_t* n_dropped, void* ws, moe_stream_t stream) {
+    NvtxRange range("moe_dispatch");
     moe_status st = moe_check_config(cfg);
     if (st != MOE_OK) return st;
     return dispatch_impl(cfg, x, topk_idx, xp, row_token, slot_row, expert_counts, expert_offsets,
@@ -340,6 +358,7 @@ moe_status moe_test_expert_ffn_stall(const moe_config* cfg, const void* xp,
                                      const int32_t* expert_offsets, const void* w_up, void* h,
                                      int32_t stall_kb, uint32_t wait_limit_us, void* ws,
                                      moe_stream_t stream) {
+    NvtxRange range("moe_test_expert_ffn_stall");
     moe_status st = moe_check_config(cfg);
     if (st != MOE_OK) return st;
     if ((st = check_ffn_config(cfg)) != MOE_OK) return st;
@@ -373,6 +392,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* 
                           const void* w_up, const void* w_down, void* h, void* yp,
                           const void* shared_x, const void* shared_up, const void* shared_down,
                           void* shared_h, void* shared_out, void* ws, moe_stream_t stream) {
+    NvtxRange range("moe_expert_ffn");
     moe_status st = moe_check_config(cfg);
     if (st != MOE_OK) return st;
     return ffn_impl(cfg, xp, expert_offsets, w_up, w_down, h, yp, shared_x, shared_up, shared_down,
@@ -382,6 +402,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* 
 moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slot_row,
                        const float* topk_gate, const void* shared_out, const void* x_residual,
                        void* y, moe_stream_t stream) {
+    NvtxRange range("moe_combine");
     moe_status st = moe_check_config(cfg);
     if (st != MOE_OK) return st;
     return combine_impl(cfg, yp, slot_row, topk_gate, shared_out, x_residual, y,
@@ -392,6 +413,7 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w
                              const float* logit_bias, const float* sel_bias, const void* w_up,
                              const void* w_down, const void* shared_up, const void* shared_down,
                              const moe_buffers* buf, void* y, void* ws, moe_stream_t stream) {
+    NvtxRange range("moe_layer_forward");
     moe_status st = moe_check_config(cfg);
     if (st != MOE_OK) return st;
     if (!buf || !ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
@@ -435,6 +457,7 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w
 moe_status moe_combine_backward(const moe_config* cfg, const void* dy, const void* yp,
                                 const int32_t* slot_row, const float* topk_gate, void* d_yp,
                                 float* d_gate, moe_stream_t stream) {
+    NvtxRange range("moe_combine_backward");
     moe_status st = moe_check_config(cfg);
     if (st != MOE_OK) return st;
     if (cfg->T == 0) return MOE_OK;
@@ -453,11 +476,13 @@ moe_status moe_combine_backward(const moe_config* cfg, const void* dy, const voi
     a.d = cfg->d;
     a.k = cfg->k;
     a.dtype = cfg->act_dtype;
+    a.rows_cap = max_rows_of(cfg);
     return cuda_status(launch_combine_backward(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_dispatch_backward(const moe_config* cfg, const void* d_xp, const int32_t* slot_row,
                                  void* dx, moe_stream_t stream) {
+    NvtxRange range("moe_dispatch_backward");
     moe_status st = moe_check_config(cfg);
     if (st != MOE_OK) return st;
     if (cfg->T == 0) return MOE_OK;
@@ -474,6 +499,7 @@ moe_status moe_dispatch_backward(const moe_config* cfg, const void* d_xp, const 
     a.d = cfg->d;
     a.k = cfg->k;
     a.dtype = cfg->act_dtype;
+    a.rows_cap = max_rows_of(cfg);
     return cuda_status(launch_combine(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -489,6 +515,7 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* xp,
                                    const void* w_down, const void* d_yp, void* d_xp, void* d_w_up,
                                    void* d_w_down, void* scratch, size_t scratch_bytes, void* ws,
                                    moe_stream_t stream) {
+    NvtxRange range("moe_expert_ffn_backward");
     moe_status st = moe_check_config(cfg);
     if (st != MOE_OK) return st;
     if ((st = check_ffn_config(cfg)) != MOE_OK) return st;
@@ -524,6 +551,14 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* xp,
             return MOE_ERR_CUDA;
         return MOE_OK;
     }
+    uint32_t* status = at<uint32_t>(ws, layout_of(cfg).status);
+    if (kChecked) {
+        // checked build: the kernels read a copy made non-decreasing within the rows
+        int32_t* safe = at<int32_t>(ws, layout_of(cfg).safe_offsets);
+        if (launch_sanitize_offsets(expert_offsets, safe, cfg->E, rows, status, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        expert_offsets = safe;
+    }
     FfnBwdArgs a;
     a.xp = xp;
     a.offsets = expert_offsets;
@@ -534,7 +569,7 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* xp,
     a.d_w_up = d_w_up;
     a.d_w_down = d_w_down;
     a.scratch = scratch;
-    a.status = at<uint32_t>(ws, layout_of(cfg).status);
+    a.status = status;
     a.rows_cap = rows;
     a.E = cfg->E;
     a.d = cfg->d;
@@ -546,6 +581,7 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* xp,
 
 moe_status moe_update_sel_bias(const moe_config* cfg, const int32_t* expert_counts, float* sel_bias,
                                float gamma, moe_stream_t stream) {
+    NvtxRange range("moe_update_sel_bias");
     moe_status st = moe_check_config(cfg);
     if (st != MOE_OK) return st;
     if (!expert_counts || !sel_bias || !aligned4(expert_counts) || !aligned4(sel_bias))
@@ -556,6 +592,7 @@ moe_status moe_update_sel_bias(const moe_config* cfg, const int32_t* expert_coun
 }
 
 moe_status moe_read_device_status(const void* ws, uint32_t* out, moe_stream_t stream) {
+    NvtxRange range("moe_read_device_status");
     if (!ws || !out) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint32_t v = 0;
@@ -563,9 +600,12 @@ moe_status moe_read_device_status(const void* ws, uint32_t* out, moe_stream_t st
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e == cudaSuccess) e = cudaMemsetAsync(const_cast<void*>(ws), 0, 4, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = take_checked_status(&v, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     *out = v;
     return MOE_OK;
 }
+
+int moe_build_checked(void) { return kChecked ? 1 : 0; }
 
 }  // extern "C"

@@ -19,6 +19,41 @@
 namespace moe {
 namespace {
 
+#ifdef MOE_CHECKED
+// Bounds violations found by calls that have no workspace (checked build).
+__device__ uint32_t g_checked_status;
+#endif
+
+// Checked build: a kept row outside [0, rows_cap) is reported and dropped.
+__device__ __forceinline__ int checked_row(int r, int64_t rows_cap) {
+#ifdef MOE_CHECKED
+    if (r < -1 || (r >= 0 && r >= rows_cap)) {
+        atomicOr(&g_checked_status, MOE_DEV_BOUNDS);
+        return -1;
+    }
+#endif
+    return r;
+}
+
+// Checked build: the offsets the expert FFN kernels read, made non-decreasing
+// within [0, rows_cap] (one warp).
+__global__ void sanitize_offsets_kernel(const int32_t* in, int32_t* out, int G, int64_t rows_cap,
+                                        uint32_t* status) {
+    if (threadIdx.x != 0) return;
+    bool bad = false;
+    int64_t prev = 0;
+    for (int g = 0; g <= G; ++g) {
+        int64_t v = in[g];
+        if (v < prev || v > rows_cap) {
+            bad = true;
+            v = v < prev ? prev : rows_cap;
+        }
+        out[g] = (int32_t)v;
+        prev = v;
+    }
+    if (bad) atomicOr(status, MOE_DEV_BOUNDS);
+}
+
 // KMAX: compile-time bound on k; U: 16-byte column vectors per lane in flight.
 // U * KMAX = 8 keeps eight independent row loads in flight per lane.
 template <typename T, int KMAX, int U, bool PRE>
@@ -33,6 +68,8 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     const char* sh = static_cast<const char*>(a.shared);
     const char* rs = static_cast<const char*>(a.resid);
     char* y = static_cast<char*>(a.y);
+    pdl_wait();  // the expert FFN's (or dispatch's) rows
+    pdl_launch_dependents();
     for (int64_t t = warp0; t < a.T; t += nwarps) {
         int r_l = -1;
         float g_l = 0.f;
@@ -40,6 +77,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
             r_l = a.slot_row[t * a.k + lane];
             g_l = a.gate ? a.gate[t * a.k + lane] : 1.f;  // no gates: the plain sum of rows
         }
+        if (kChecked && lane < a.k) r_l = checked_row(r_l, a.rows_cap);
         int r[KMAX];
         float g[KMAX];
 #pragma unroll
@@ -95,15 +133,12 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
 }
 
 template <typename T>
-void launch_combine_typed(const CombineArgs& a, unsigned blocks, cudaStream_t s) {
-    if (a.k <= 2)
-        combine_kernel<T, 2, 4, false><<<blocks, 256, 0, s>>>(a);
-    else if (a.k <= 4)
-        combine_kernel<T, 4, 2, false><<<blocks, 256, 0, s>>>(a);
-    else if (a.shared || a.resid)
-        combine_kernel<T, 8, 1, true><<<blocks, 256, 0, s>>>(a);
-    else
-        combine_kernel<T, 8, 1, false><<<blocks, 256, 0, s>>>(a);
+cudaError_t launch_combine_typed(const CombineArgs& a, unsigned blocks, cudaStream_t s) {
+    const dim3 g(blocks);
+    if (a.k <= 2) return launch_pdl(combine_kernel<T, 2, 4, false>, g, 256, 0, s, a);
+    if (a.k <= 4) return launch_pdl(combine_kernel<T, 4, 2, false>, g, 256, 0, s, a);
+    if (a.shared || a.resid) return launch_pdl(combine_kernel<T, 8, 1, true>, g, 256, 0, s, a);
+    return launch_pdl(combine_kernel<T, 8, 1, false>, g, 256, 0, s, a);
 }
 
 // Backward of combine, one warp per token: for every kept slot j,
@@ -128,6 +163,7 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(CombineBwdArgs a) {
             r_l = a.slot_row[t * a.k + lane];
             g_l = a.gate[t * a.k + lane];
         }
+        if (kChecked && lane < a.k) r_l = checked_row(r_l, a.rows_cap);
         int r[KMAX];
         float g[KMAX], dot[KMAX];
 #pragma unroll
@@ -197,6 +233,30 @@ cudaError_t launch_combine_backward(const CombineBwdArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+cudaError_t launch_sanitize_offsets(const int32_t* in, int32_t* out, int G, int64_t rows_cap,
+                                    uint32_t* status, cudaStream_t s) {
+    sanitize_offsets_kernel<<<1, 32, 0, s>>>(in, out, G, rows_cap, status);
+    return cudaGetLastError();
+}
+
+cudaError_t take_checked_status(uint32_t* out, cudaStream_t s) {
+#ifdef MOE_CHECKED
+    uint32_t v = 0;
+    void* addr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&addr, g_checked_status);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&v, addr, 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(addr, 0, 4, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) *out |= v;
+    return e;
+#else
+    (void)out;
+    (void)s;
+    return cudaSuccess;
+#endif
+}
+
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
     if (a.T == 0) return cudaSuccess;
     int dev = 0, sms = 148;
@@ -205,11 +265,8 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
     int64_t blocks = (a.T + 7) / 8;  // 8 warps (tokens) per block
     const int64_t cap = (int64_t)sms * 16;
     if (blocks > cap) blocks = cap;
-    if (a.dtype == MOE_DTYPE_F32)
-        launch_combine_typed<float>(a, (unsigned)blocks, s);
-    else
-        launch_combine_typed<__nv_bfloat16>(a, (unsigned)blocks, s);
-    return cudaGetLastError();
+    if (a.dtype == MOE_DTYPE_F32) return launch_combine_typed<float>(a, (unsigned)blocks, s);
+    return launch_combine_typed<__nv_bfloat16>(a, (unsigned)blocks, s);
 }
 
 }  // namespace moe

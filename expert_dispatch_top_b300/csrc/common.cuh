@@ -6,8 +6,27 @@
 #include <stdint.h>
 
 #include "moe.h"
+#include "nvtx3/nvToolsExt.h"
 
 namespace moe {
+
+// An NVTX range named after a C-ABI entry point, for the duration of the call
+// (host-side enqueue time; a profiler that attaches through NVTX shows the
+// kernels each call launched inside it).  Without an attached tool the push
+// and pop return at once.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+// Debug build that range-checks indices read from callers' buffers.
+#ifdef MOE_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
 
 // Upper bound on any bounded device wait (nanoseconds of %globaltimer).
 constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s
@@ -101,6 +120,34 @@ __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
 
 __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start
+// while the kernel before it on the stream is still running; pdl_wait blocks
+// the calling thread until that kernel has completed and its memory writes
+// are visible, so each kernel calls it before its first global read or write.
+// pdl_launch_dependents lets the next kernel on the stream start early.  Both
+// are no-ops in a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch with programmatic stream serialization (see pdl_wait).
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kernel, dim3 grid, unsigned block, size_t smem, cudaStream_t s,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // Key order of the router's selection: larger key first, ties to the lower index.

@@ -24,15 +24,24 @@
 //                    decides keep/drop against C and the row; then the block
 //                    copies its tokens' rows with 16-byte vectors.
 // Nothing waits on another CTA: the order comes from the scan, not from a
-// look-back chain, so no kernel here spins.  scan_kernel and place_kernel are
-// programmatic dependents of the kernel before them: each starts while its
-// predecessor runs, does what does not need the predecessor's results (place:
-// the per-block bitmaps), and waits (griddepcontrol.wait) before reading them.
+// look-back chain, so no kernel here spins.  All three are programmatic
+// dependents of the kernel before them: each starts while its predecessor
+// runs, does what does not need the predecessor's results (place: the
+// per-block bitmaps from topk_idx), and waits (griddepcontrol.wait) before
+// reading them.  Every kernel releases its successor only after its own wait,
+// so when place_kernel starts, the router that wrote topk_idx has completed.
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace moe {
 namespace {
+
+using tc::mbar_expect_tx;
+using tc::mbar_fence_init;
+using tc::mbar_init;
+using tc::mbar_try_wait;
+using tc::smem_u32;
 
 constexpr int kPlaceTokens = 32;  // smallest token block: one warp's worth of tokens
 constexpr int kPlaceThreads = 256;
@@ -69,20 +78,18 @@ __device__ int block_exclusive_scan(int v, int* scratch /* >= 33 ints */, int* t
     return out;
 }
 
-// Programmatic dependent launch: let the next kernel on the stream start, and
-// (in that kernel) wait for this grid's completion and memory.
-__device__ __forceinline__ void pdl_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // Per-block, per-expert assignment counts: hist[e * nblk + b].
 __global__ void __launch_bounds__(256) count_kernel(DispatchArgs a, int tb, int nblk) {
     __shared__ int h[256];
     const int tid = threadIdx.x;
     const int b = blockIdx.x;
-    pdl_launch_dependents();
     for (int e = tid; e < a.E; e += blockDim.x) h[e] = 0;
+    // The router's topk_idx (or whatever kernel ran before).  Dependents are
+    // released only after this wait: place_kernel reads topk_idx before its own
+    // wait, which is safe because no kernel of the chain lets its successor
+    // start before its own predecessor has completed.
+    pdl_wait();
+    pdl_launch_dependents();
     if (b == 0) {
         int32_t* splits = a.rank_splits ? a.rank_splits : a.splits_acc;
         for (int i = tid; i < a.R * a.R; i += blockDim.x) splits[i] = 0;
@@ -110,8 +117,8 @@ __global__ void __launch_bounds__(256) count_kernel(DispatchArgs a, int tb, int 
 // j < b, and totals[e] = the sum over all blocks.
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(DispatchArgs a, int nblk) {
     __shared__ int scratch[33];
-    pdl_launch_dependents();
     pdl_wait();  // count_kernel's histograms
+    pdl_launch_dependents();
     const int e = blockIdx.x;
     const int32_t* in = a.hist + (int64_t)e * nblk;
     int32_t* out = a.prefix + (int64_t)e * nblk;
@@ -137,12 +144,53 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(DispatchArgs a, int 
     if (threadIdx.x == 0) a.totals[e] = carry;
 }
 
+// Bulk (TMA engine, untiled) copies between global and shared memory.  Both
+// addresses 16-byte aligned, sizes multiples of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's most recent store groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Bounded wait for phase `parity` of a shared-memory barrier.
+__device__ __forceinline__ bool bar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    return true;
+}
+
+constexpr int kBulkLag = 6;           // store groups allowed to still read their slot
+constexpr int kBulkMaxSlots = 16;
+constexpr int kBulkRingBytes = 48 * 1024;  // with ~18 KB of static shared memory: 3 CTAs per SM
+
 // SUB sub-tiles of 32 tokens per block (TB = 32*SUB tokens): warp s < SUB
 // ranks sub-tile s with per-expert lane bitmaps; larger blocks amortise the
 // block's fixed costs (offsets, barriers) over more row copies.
+// nslot > 0: the row copies go through a ring of nslot shared-memory slots
+// with bulk copies (dynamic shared memory: nslot * chunk bytes); 0: 16-byte
+// vector loads and stores.
 template <typename T, int SUB>
-__global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a, int nblk) {
+__global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a, int nblk, int nslot) {
     constexpr int TB = 32 * SUB;
+    extern __shared__ __align__(128) uint8_t ring[];
+    __shared__ __align__(8) uint64_t ring_bar[kBulkMaxSlots];
     __shared__ uint32_t bits[SUB][256];  // per sub-tile and expert: lanes (tokens) that chose it
     __shared__ int wpre[SUB][256];       // per sub-tile and expert: assignments in earlier sub-tiles
     __shared__ int prefix[256];          // per expert: assignments in earlier blocks
@@ -159,6 +207,10 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a, in
         for (int sb = 0; sb < SUB; ++sb) bits[sb][e] = 0u;
     }
     for (int i = tid; i < a.R * a.R; i += kPlaceThreads) split_acc[i] = 0;
+    if (tid == 0 && nslot > 0) {
+        for (int i = 0; i < nslot; ++i) mbar_init(smem_u32(&ring_bar[i]), 1);
+        mbar_fence_init();
+    }
     __syncthreads();
     const int64_t t0 = (int64_t)blk * TB;
     const int64_t t = t0 + warp * 32 + lane;  // meaningful for warps < SUB
@@ -189,6 +241,7 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a, in
     }
     // scan_kernel's prefixes and totals from here on
     pdl_wait();
+    pdl_launch_dependents();
     {
         const int e = tid;  // E <= 256 = blockDim.x
         int total = 0, kept = 0, pre = 0;
@@ -236,6 +289,13 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a, in
                 const int pos = prefix[e] + wpre[warp][e] + __popc(bits[warp][e] & lanemask_lt());
                 if (a.C < 0 || pos < a.C) {
                     row = offs[e] + pos;
+                    if (kChecked && (int64_t)row >= (a.C < 0 || a.T * a.k < (int64_t)a.E * a.C
+                                                        ? a.T * a.k : (int64_t)a.E * a.C)) {
+                        atomicOr(a.status, MOE_DEV_BOUNDS);  // cannot happen: counts are exact
+                        row = -1;
+                    }
+                }
+                if (row >= 0) {
                     if (chunk0) {
                         a.row_token[row] = (int32_t)t;
                         atomicAdd(&split_acc[src * a.R + e / per], 1);
@@ -269,6 +329,62 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a, in
     const char* x = static_cast<const char*>(a.x) + (int64_t)vlo * 16;
     char* xp = static_cast<char*>(a.xp) + (int64_t)vlo * 16;
     const int ntok = (int)((a.T - t0) < TB ? (a.T - t0) : TB);
+    if (nslot > 0) {
+        // One thread moves the rows: a bulk load of each token's chunk into a
+        // ring slot, then one bulk store per kept row.  A slot is reloaded once
+        // the store group that read it is done reading (kBulkLag groups behind).
+        if (tid != 0) return;
+        const uint32_t cb = (uint32_t)w * 16u;
+        const uint32_t ring0 = smem_u32(ring);
+        const uint32_t bar0 = smem_u32(ring_bar);
+        int lt = 0, st = 0, loads = 0, groups = 0;
+        auto kept = [&](int tok) {
+            bool any = false;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) any |= j < a.k && rows[tok][j] >= 0;
+            return any;
+        };
+        auto refill = [&]() {
+            while (loads < groups - kBulkLag + nslot) {
+                while (lt < ntok && !kept(lt)) ++lt;
+                if (lt >= ntok) return;
+                const int slot = loads % nslot;
+                mbar_expect_tx(bar0 + 8 * slot, cb);
+                bulk_load(ring0 + slot * cb, x + (t0 + lt) * row_bytes, cb, bar0 + 8 * slot);
+                ++loads;
+                ++lt;
+            }
+        };
+        refill();
+        bool ok = true;
+        while (groups < loads) {
+            while (!kept(st)) ++st;
+            const int slot = groups % nslot;
+            if (!bar_wait_bounded(bar0 + 8 * slot, (uint32_t)(groups / nslot) & 1u, kWaitTimeoutNs)) {
+                ok = false;
+                break;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int r = j < a.k ? rows[st][j] : -1;
+                if (r >= 0) bulk_store(xp + (int64_t)r * row_bytes, ring0 + slot * cb, cb);
+            }
+            bulk_commit();
+            ++groups;
+            ++st;
+            bulk_wait_read<kBulkLag>();
+            refill();
+        }
+        if (!ok) {
+            // a load never landed: report it, and wait (bounded) for the loads
+            // still in flight before the shared memory they target goes away
+            atomicOr(a.status, MOE_DEV_COPY_TIMEOUT);
+            for (int g = groups; g < loads; ++g)
+                bar_wait_bounded(bar0 + 8 * (g % nslot), (uint32_t)(g / nslot) & 1u, kWaitTimeoutNs / 16);
+        }
+        bulk_wait_all();
+        return;
+    }
     if (w >= kPlaceThreads) {
         for (int tok = warp; tok < ntok; tok += kPlaceThreads / 32) {
             int r[8];
@@ -341,23 +457,6 @@ int place_sub(int64_t T) {
     return 1;
 }
 
-// Launch with programmatic stream serialization: the kernel may start while
-// the previous kernel on the stream runs, and waits for it in device code.
-template <typename K, typename... Args>
-cudaError_t launch_pdl(K kernel, dim3 grid, unsigned block, cudaStream_t s, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
 // Column chunks per token block: enough CTAs for about four per SM, chunks of
 // at least 64 vectors (1 KB).
 int place_chunks(const DispatchArgs& a, int nblk, int elem_bytes) {
@@ -375,10 +474,38 @@ int place_chunks(const DispatchArgs& a, int nblk, int elem_bytes) {
 template <typename T>
 cudaError_t launch_place(const DispatchArgs& a, int sub, int nblk, cudaStream_t s) {
     // one CTA writes the metadata when T = 0
-    const dim3 grid(nblk > 0 ? (unsigned)nblk : 1u, (unsigned)place_chunks(a, nblk, (int)sizeof(T)));
-    if (sub == 4) return launch_pdl(place_kernel<T, 4>, grid, kPlaceThreads, s, a, nblk);
-    if (sub == 2) return launch_pdl(place_kernel<T, 2>, grid, kPlaceThreads, s, a, nblk);
-    return launch_pdl(place_kernel<T, 1>, grid, kPlaceThreads, s, a, nblk);
+    const int S = place_chunks(a, nblk, (int)sizeof(T));
+    const dim3 grid(nblk > 0 ? (unsigned)nblk : 1u, (unsigned)S);
+    // Bulk copies through a shared-memory ring (as many chunk-sized slots as fit
+    // kBulkRingBytes, more than kBulkLag) where they measured faster than the
+    // vector copies: many destination rows per token (k >= 4), chunks of at
+    // least 2 KB and batches of at most 16384 tokens (DeepSeek-shaped layer
+    // 204 -> 191 us, 7168-wide rows at T = 4096 114 -> 111 us).  With k <= 2 or
+    // short rows one issuing thread per CTA falls behind the vector copies
+    // (Mixtral-shaped 75 -> 89 us, Switch-shaped 36 -> 105 us), and at
+    // T = 131072 the two forms tie.
+    const int nvec = a.d * (int)sizeof(T) / 16;
+    const int64_t cb = (int64_t)((nvec + S - 1) / S) * 16;  // the widest chunk
+    int nslot = (int)(kBulkRingBytes / cb);
+    if (nslot > kBulkMaxSlots) nslot = kBulkMaxSlots;
+    if (nslot < kBulkLag + 1 || a.k < 4 || cb < 2048 || a.T > 16384) nslot = 0;
+    const size_t smem = (size_t)nslot * (size_t)cb;
+    auto kern = sub == 4 ? place_kernel<T, 4> : sub == 2 ? place_kernel<T, 2> : place_kernel<T, 1>;
+    if (smem > 0) {
+        // the dynamic shared-memory limit is a per-device function attribute
+        constexpr int kDevs = 64;
+        static bool attr_set[kDevs][3] = {};
+        const int form = sub == 4 ? 2 : sub == 2 ? 1 : 0;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev < 0 || dev >= kDevs || !attr_set[dev][form]) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kBulkRingBytes);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < kDevs) attr_set[dev][form] = true;
+        }
+    }
+    return launch_pdl(kern, grid, kPlaceThreads, smem, s, a, nblk, nslot);
 }
 }  // namespace
 
@@ -389,10 +516,10 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
     const int64_t nblk64 = (a.T + 32 * sub - 1) / (32 * sub);
     if (nblk64 > (1 << 30)) return cudaErrorInvalidValue;
     const int nblk = (int)nblk64;
-    count_kernel<<<nblk > 0 ? (unsigned)nblk : 1u, 256, 0, s>>>(a, 32 * sub, nblk);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(count_kernel, dim3(nblk > 0 ? (unsigned)nblk : 1u), 256, 0, s, a,
+                               32 * sub, nblk);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(scan_kernel, dim3((unsigned)a.E), kScanThreads, s, a, nblk);
+    e = launch_pdl(scan_kernel, dim3((unsigned)a.E), kScanThreads, 0, s, a, nblk);
     if (e != cudaSuccess) return e;
     if (a.dtype == MOE_DTYPE_F32) return launch_place<float>(a, sub, nblk, s);
     return launch_place<__nv_bfloat16>(a, sub, nblk, s);

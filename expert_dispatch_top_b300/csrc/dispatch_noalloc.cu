@@ -134,6 +134,7 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x,
                                            int32_t* expert_offsets, int32_t* rank_counts,
                                            int32_t* rank_splits, int32_t* n_dropped,
                                            uint32_t* device_status, moe_stream_t stream) {
+    NvtxRange range("moe_dispatch_noalloc");
     moe_status st = moe_check_config(cfg);
     if (st != MOE_OK) return st;
     if (!expert_counts || !expert_offsets || !rank_counts || !n_dropped) return MOE_ERR_INVALID_ARG;

@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a) {
     __shared__ __align__(16) float Bs[2][SBK][SBN];
     __shared__ int s_g, s_row0, s_rows;
     const int tid = threadIdx.x;
+    pdl_wait();  // programmatic dependent launch: the previous kernel's writes
+    pdl_launch_dependents();
     if (tid == 0) {
         int rem = blockIdx.x, g = -1, row0 = 0, rows = 0;
         for (int q = 0; q < a.G; ++q) {
@@ -175,11 +177,8 @@ cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t s) {
     const bool gated = a.epi == EPI_SWIGLU;
     const int ncol = gated ? SBN / 2 : SBN;
     dim3 grid((unsigned)mtiles, (unsigned)((a.N + ncol - 1) / ncol));
-    if (gated)
-        gemm_simt_kernel<true><<<grid, 256, 0, s>>>(a);
-    else
-        gemm_simt_kernel<false><<<grid, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    if (gated) return launch_pdl(gemm_simt_kernel<true>, grid, 256, 0, s, a);
+    return launch_pdl(gemm_simt_kernel<false>, grid, 256, 0, s, a);
 }
 
 }  // namespace moe

@@ -194,6 +194,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     }
+    // programmatic dependent launch: everything above touched no global data
+    pdl_wait();
+    pdl_launch_dependents();
     if (warp == 2) {
         // Per-group tile table: lane l covers groups [8l, 8l+8).
         int cnt[8], kbs[8];
@@ -506,8 +509,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kDevs) attr_set[dev][mode] = true;
     }
-    kern<<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), THREADS, (size_t)SMEM_BYTES, s, tmA, tmB, p);
 }
 
 }  // namespace moe

@@ -6,6 +6,19 @@
 
 namespace moe {
 
+// One entry of a partial top-k list (router split over expert slices).
+struct RoutePartial {
+    float key;  // selection key
+    float val;  // logit (softmax) or exact sigmoid score
+    int32_t idx;
+};
+// The tensor-core router splits a tile's experts over up to kRouteSplitMax
+// work units when T <= kRouteSplitMaxT and a partial-list buffer is given.
+constexpr int kRouteSplitMax = 4;
+constexpr int64_t kRouteSplitMaxT = 16384;
+// Bytes of that buffer for T tokens and E experts (0: the router never splits).
+int64_t route_partial_bytes(int64_t T, int E);
+
 struct RouteArgs {
     const void* x;
     const void* w;
@@ -17,6 +30,7 @@ struct RouteArgs {
     int64_t T;
     int d, E, k, score, renorm, dtype;
     int R, max_ranks;  // rank-limited routing when 0 < max_ranks < R (tensor-core router)
+    RoutePartial* part = nullptr;  // route_partial_bytes(T, E) bytes, or null: no split
 };
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 // Tensor-core router (bf16, E <= 256): 0 if supported.
@@ -57,6 +71,7 @@ struct CombineArgs {
     void* y;
     int64_t T;
     int d, k, dtype;
+    int64_t rows_cap = 0;  // rows of yp (the checked build's range of a kept slot_row)
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);  // gate == null: unit gates
 
@@ -69,8 +84,17 @@ struct CombineBwdArgs {
     float* d_gate;
     int64_t T;
     int d, k, dtype;
+    int64_t rows_cap = 0;  // rows of yp / d_yp (checked build)
 };
 cudaError_t launch_combine_backward(const CombineBwdArgs& a, cudaStream_t s);
+
+// Checked build: copies offsets [G+1] to out, clamped to be non-decreasing
+// within [0, rows_cap], and sets MOE_DEV_BOUNDS in *status if anything changed.
+cudaError_t launch_sanitize_offsets(const int32_t* in, int32_t* out, int G, int64_t rows_cap,
+                                    uint32_t* status, cudaStream_t s);
+// Checked build: the library-wide bounds word of calls without a workspace,
+// OR-ed into *out and cleared (after the stream's work); unchecked: nothing.
+cudaError_t take_checked_status(uint32_t* out, cudaStream_t s);
 
 // Epilogue of one grouped GEMM: out = epi(A . B^T).
 enum Epilogue { EPI_NONE = 0, EPI_GELU = 1, EPI_SWIGLU = 2 };

@@ -11,6 +11,7 @@
 // same fp32 value, so the selection is reproducible bit for bit.  The sigmoid
 // score is fp32(1/(1+exp(-L))) evaluated in double, i.e. the correctly
 // rounded fp32 sigmoid except in vanishingly rare double-rounding cases.
+#include <float.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -50,12 +51,20 @@ __device__ __forceinline__ float seg_sum(float v) {
 // Top-k and gates for one token whose E logits are spread over a group of W
 // lanes, lane e' of the group holding the values of experts e' + W*i
 // (i < NV).  L: logits (logit bias included); valid[i]: e < E.
+// Rank-limited routing (0 < max_ranks < R): a rank's score is the best key of
+// its E/R experts, the max_ranks best ranks are kept (ties to the lower rank)
+// and the top-k is taken among their experts.  The best remaining rank is the
+// rank of the best key among experts of ranks not yet kept: ranks are
+// contiguous blocks of experts, so the lower expert index that wins a tie of
+// keys also names the lower rank.
 template <int W, int NV>
 __device__ __forceinline__ void select_and_gate(const float (&L)[NV], int e_base, int E, int k,
                                                 int score, int renorm, const float* sel_bias,
-                                                int32_t* out_idx, float* out_gate) {
+                                                int R, int max_ranks, int32_t* out_idx,
+                                                float* out_gate, uint32_t* status) {
     float key[NV], s[NV];
     int slot[NV];
+    bool ok[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int e = e_base + W * i;
@@ -72,6 +81,31 @@ __device__ __forceinline__ void select_and_gate(const float (&L)[NV], int e_base
             s[i] = 0.f;
             key[i] = kNegInf;
         }
+        ok[i] = e < E;
+        if (status && e < E && !(fabsf(L[i]) <= FLT_MAX)) atomicOr(status, MOE_DEV_NONFINITE);
+    }
+    if (max_ranks > 0 && max_ranks < R) {
+        const int per = E / R;
+        uint32_t kept = 0;  // bit r: rank r kept
+        for (int m = 0; m < max_ranks; ++m) {
+            float bv = kNegInf;
+            int bi = kNoExpert;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int e = e_base + W * i;
+                if (e < E && !((kept >> (e / per)) & 1u) && key_better(key[i], e, bv, bi)) {
+                    bv = key[i];
+                    bi = e;
+                }
+            }
+            seg_argmax<W>(bv, bi);
+            if (bi != kNoExpert) kept |= 1u << (bi / per);
+        }
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int e = e_base + W * i;
+            ok[i] = e < E && ((kept >> (e / per)) & 1u);
+        }
     }
     float top_logit = 0.f;
     for (int j = 0; j < k; ++j) {
@@ -81,7 +115,7 @@ __device__ __forceinline__ void select_and_gate(const float (&L)[NV], int e_base
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             const int e = e_base + W * i;
-            if (e < E && slot[i] < 0 && key_better(key[i], e, bv, bi)) {
+            if (ok[i] && slot[i] < 0 && key_better(key[i], e, bv, bi)) {
                 bv = key[i];
                 bi = e;
             }
@@ -135,6 +169,8 @@ __device__ __forceinline__ void select_and_gate(const float (&L)[NV], int e_base
 // ---------------------------------------------------------------------------
 template <typename T, int EMAX>
 __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
+    pdl_wait();  // programmatic dependent launch: the previous kernel's writes
+    pdl_launch_dependents();
     constexpr int TPW = 32 / EMAX;
     constexpr int V = Elem<T>::kPerVec;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -197,7 +233,8 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
         idx_buf[j] = -1;
         gate_buf[j] = 0.f;
     }
-    select_and_gate<EMAX, 1>(L, e, a.E, a.k, a.score, a.renorm, a.sel_bias, idx_buf, gate_buf);
+    select_and_gate<EMAX, 1>(L, e, a.E, a.k, a.score, a.renorm, a.sel_bias, a.R, a.max_ranks,
+                             idx_buf, gate_buf, live ? a.status : nullptr);
     if (live) {
 #pragma unroll
         for (int j = 0; j < 8; ++j)
@@ -225,6 +262,8 @@ constexpr int big_smem_bytes() {
 template <typename T, int EP>
 __global__ void __launch_bounds__(256) route_big_kernel(RouteArgs a) {
     extern __shared__ __align__(16) float sm[];
+    pdl_wait();  // programmatic dependent launch: the previous kernel's writes
+    pdl_launch_dependents();
     float* xs = sm;                // [kKC][kTT]
     float* ws = sm + kKC * kTT;    // [kKC][EP]
     float* Ls = sm;                // [kTT][EP+1] after the GEMM
@@ -317,7 +356,8 @@ __global__ void __launch_bounds__(256) route_big_kernel(RouteArgs a) {
             idx_buf[j] = -1;
             gate_buf[j] = 0.f;
         }
-        select_and_gate<32, NV>(L, lane, a.E, a.k, a.score, a.renorm, a.sel_bias, idx_buf, gate_buf);
+        select_and_gate<32, NV>(L, lane, a.E, a.k, a.score, a.renorm, a.sel_bias, a.R, a.max_ranks,
+                                idx_buf, gate_buf, a.status);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             if (j < a.k && idx_buf[j] >= 0) {
@@ -332,21 +372,21 @@ cudaError_t launch_typed(const RouteArgs& a, cudaStream_t s) {
     if (a.T == 0) return cudaSuccess;
     if (a.E <= 8) {
         const int64_t blocks = (a.T + 8 * 4 - 1) / (8 * 4);
-        route_small_kernel<T, 8><<<(unsigned)blocks, 256, 0, s>>>(a);
+        return launch_pdl(route_small_kernel<T, 8>, dim3((unsigned)blocks), 256, 0, s, a);
     } else if (a.E <= 16) {
         const int64_t blocks = (a.T + 8 * 2 - 1) / (8 * 2);
-        route_small_kernel<T, 16><<<(unsigned)blocks, 256, 0, s>>>(a);
+        return launch_pdl(route_small_kernel<T, 16>, dim3((unsigned)blocks), 256, 0, s, a);
     } else if (a.E <= 32) {
         const int64_t blocks = (a.T + 8 - 1) / 8;
-        route_small_kernel<T, 32><<<(unsigned)blocks, 256, 0, s>>>(a);
+        return launch_pdl(route_small_kernel<T, 32>, dim3((unsigned)blocks), 256, 0, s, a);
     } else {
         const unsigned blocks = (unsigned)((a.T + kTT - 1) / kTT);
         if (a.E <= 64) {
             constexpr int B = big_smem_bytes<64>();
-            route_big_kernel<T, 64><<<blocks, 256, B, s>>>(a);
+            return launch_pdl(route_big_kernel<T, 64>, dim3(blocks), 256, (size_t)B, s, a);
         } else if (a.E <= 128) {
             constexpr int B = big_smem_bytes<128>();
-            route_big_kernel<T, 128><<<blocks, 256, B, s>>>(a);
+            return launch_pdl(route_big_kernel<T, 128>, dim3(blocks), 256, (size_t)B, s, a);
         } else {
             constexpr int B = big_smem_bytes<256>();
             // the shared-memory limit is a per-device function attribute
@@ -360,7 +400,7 @@ cudaError_t launch_typed(const RouteArgs& a, cudaStream_t s) {
                 if (e != cudaSuccess) return e;
                 if (dev >= 0 && dev < kDevs) attr[dev] = true;
             }
-            route_big_kernel<T, 256><<<blocks, 256, B, s>>>(a);
+            return launch_pdl(route_big_kernel<T, 256>, dim3(blocks), 256, (size_t)B, s, a);
         }
     }
     return cudaGetLastError();

@@ -39,6 +39,8 @@
 // mask of the values that beat the current k-th key; only those are inserted
 // (sorted insertion, ties to the lower index), so the insertion code exists
 // once and runs rarely.
+#include <float.h>
+
 #include "kernels.h"
 #include "tcgen05.cuh"
 
@@ -53,12 +55,13 @@ constexpr int RM = 128, RK = 64;
 constexpr int STASH_PITCH = 33;
 constexpr int STASH_PITCH_RANKS = 97;
 constexpr int R_THREADS_MAX = 64 + 2 * 128;  // producer, MMA, up to two epilogue warp groups
-constexpr int R_MAX_STAGES = 8;
+constexpr int R_MAX_STAGES = 12;  // deep rings for few experts (18 KB stages): more of x in flight
 constexpr uint32_t R_TMEM_COLS = 512;
-constexpr int R_SMEM_TILES = 196608;  // bytes of stage ring
+constexpr int R_SMEM_TILES = 221184;  // bytes of stage ring (at most)
 constexpr int R_SMEM_FIXED = 1024 /*align*/ + 256 /*barriers*/ + 2 * 256 * 4 /*biases*/;
 constexpr int R_SMEM_MAX = 232448;  // 227 KB per block
 constexpr float kApproxDelta = 1.0f / 256.0f;
+static_assert((2 * R_MAX_STAGES + 5) * 8 <= 240, "barriers overlap the flags");
 
 struct RtParams {
     int64_t T;
@@ -72,6 +75,16 @@ struct RtParams {
     float* gate;
     uint32_t* status;
     int num_kb, m_tiles, stages, stage_bytes;
+    int tile_rows;  // tokens per tile (multiple of 8, <= 128); the MMA always runs M = 128
+    int tx_bytes;   // bytes one stage's TMA loads deliver
+    // Expert split: each tile's experts are cut into `split` slices of Eh
+    // experts (one work unit each, units = m_tiles * split).  With split > 1
+    // every unit writes its exact partial top-k to `part` (and, for softmax
+    // gates without renormalisation, its partial softmax sum to `zpart`), and
+    // route_merge_kernel forms the final top-k and gates.
+    int split, Eh, units;
+    RoutePartial* part;
+    float2* zpart;
 };
 
 __device__ __forceinline__ float sigmoid_exact(float L) {
@@ -145,6 +158,10 @@ __device__ __forceinline__ uint32_t pick_ranks(const float* sc, int R, int m, fl
 // tiles; on inputs whose sums are exact in fp32 this changes nothing.)
 __device__ __forceinline__ int k_start(int tile, int num_kb) { return (int)(((unsigned)tile * 37u) % (unsigned)num_kb); }
 
+// SPLIT: the launch cuts each tile's experts into p.split slices (never with
+// rank-limited routing); a separate instantiation keeps the unsplit kernel's
+// register budget as it is.
+template <bool SPLIT>
 __global__ void __launch_bounds__(R_THREADS_MAX, 1)
     route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     const RtParams p) {
@@ -152,9 +169,10 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint8_t* extra = smem + p.stages * p.stage_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(extra);  // full[8] empty[8] accf[2] acce[2] drain
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(extra + 192);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(extra + 196);
+    // full[R_MAX_STAGES] empty[R_MAX_STAGES] accf[2] acce[2] drain: 232 bytes
+    uint64_t* bars = reinterpret_cast<uint64_t*>(extra);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(extra + 240);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(extra + 244);
     float* lb_s = reinterpret_cast<float*>(extra + 256);
     float* sb_s = lb_s + 256;
     float* stash_all = sb_s + 256;  // [128][p.stash_pitch]
@@ -183,6 +201,9 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
         prefetch_tmap(&tmW);
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), R_TMEM_COLS);
+    // programmatic dependent launch: everything above touched no global data
+    pdl_wait();
+    pdl_launch_dependents();
     if (warp >= 2) {
         for (int e = threadIdx.x - 64; e < 256; e += (int)blockDim.x - 64) {
             lb_s[e] = (p.logit_bias && e < p.E) ? p.logit_bias[e] : 0.f;
@@ -198,8 +219,10 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            for (int tile = blockIdx.x; tile < p.m_tiles && !*abort_flag; tile += gridDim.x) {
-                const int kb0 = k_start(tile, p.num_kb);
+            for (int unit = blockIdx.x; unit < p.units && !*abort_flag; unit += gridDim.x) {
+                const int tile = SPLIT ? unit / p.split : unit;
+                const int e0 = SPLIT ? (unit - tile * p.split) * p.Eh : 0;  // first expert of the slice
+                const int kb0 = k_start(unit, p.num_kb);
                 for (int i = 0; i < p.num_kb; ++i) {
                     int kb = kb0 + i;
                     if (kb >= p.num_kb) kb -= p.num_kb;
@@ -207,10 +230,10 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                                    MOE_DEV_GEMM_TIMEOUT))
                         break;
                     const uint32_t fb = full0 + 8 * stage;
-                    mbar_expect_tx(fb, p.stage_bytes);
+                    mbar_expect_tx(fb, p.tx_bytes);
                     const uint32_t sa = smem_u32(smem + stage * p.stage_bytes);
-                    tma_load_2d(sa, &tmX, kb * RK, tile * RM, fb);
-                    tma_load_2d(sa + RM * RK * 2, &tmW, kb * RK, 0, fb);
+                    tma_load_2d(sa, &tmX, kb * RK, tile * p.tile_rows, fb);
+                    tma_load_2d(sa + RM * RK * 2, &tmW, kb * RK, e0, fb);
                     if (++stage == p.stages) {
                         stage = 0;
                         phase ^= 1;
@@ -226,7 +249,7 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < p.m_tiles && ok; tile += gridDim.x) {
+            for (int unit = blockIdx.x; unit < p.units && ok; unit += gridDim.x) {
                 if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status,
                                MOE_DEV_GEMM_TIMEOUT)) {
                     ok = false;
@@ -272,18 +295,17 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
         // (they land in TMEM buffer g), so two tiles' epilogues run at once.
         const int q = warp & 3;
         const int egroup = (warp - 2) >> 2;
-        const int nchunks = (p.E + 31) / 32;
         const bool sigmoid = p.score == MOE_SCORE_SIGMOID;
         const bool has_lb = p.logit_bias != nullptr;
         const bool has_sb = p.sel_bias != nullptr;
         float* stash = stash_all + (threadIdx.x - 64) * p.stash_pitch;
         float* rank_a = stash + 33;  // rank scores (rank-limited routing only)
         float* rank_x = stash + 65;
-        const bool limited = p.max_ranks > 0;
+        const bool limited = !SPLIT && p.max_ranks > 0;
         const int per = p.E / p.R;
         const float inv_per = 1.0f / (float)per;  // (e + 1/2) * inv_per truncates to e / per exactly
         int local = -1;
-        for (int tile = blockIdx.x; tile < p.m_tiles; tile += gridDim.x) {
+        for (int unit = blockIdx.x; unit < p.units; unit += gridDim.x) {
             ++local;
             if (local % p.epi_groups != egroup) continue;
             const int acc = local & 1;                       // the MMA alternates buffers per tile
@@ -294,10 +316,18 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
             if (!ok) break;
             fence_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256);
-            const int64_t t = (int64_t)tile * RM + q * 32 + lane;
+            // rows past tile_rows hold whatever the stage held before: computed, never stored
+            const bool row_ok = q * 32 + lane < p.tile_rows;
+            const int tile = SPLIT ? unit / p.split : unit;
+            const int h = SPLIT ? unit - tile * p.split : 0;
+            const int e0 = SPLIT ? h * p.Eh : 0;  // this unit's experts: [e0, e_end)
+            const int e_end = SPLIT ? e0 + p.Eh : p.E;  // slices are whole 32-expert chunks
+            const int nchunks = SPLIT ? p.Eh / 32 : (p.E + 31) / 32;
+            const int64_t t = (int64_t)tile * p.tile_rows + q * 32 + lane;
             TopK top;
             top.init(p.k);
             float v[32];
+            bool nonfinite = false;  // a NaN or infinite logit among this token's
             // Rank-limited routing: rank score = best key among the rank's
             // experts; keep the max_ranks best ranks (ties to the lower rank).
             uint32_t allowed = 0xffffffffu;
@@ -307,8 +337,8 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                     tmem_ld32(tb + (uint32_t)(c * 32), v);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const int e = c * 32 + i;
-                        if (e < p.E) {
+                        const int e = e0 + c * 32 + i;
+                        if ((SPLIT || e < e_end)) {
                             const float L = has_lb ? __fadd_rn(v[i], lb_s[e]) : v[i];
                             const float key =
                                 sigmoid ? __fadd_rn(sigmoid_approx(L), sb_s[e]) : L;
@@ -333,10 +363,10 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                         uint32_t mask = 0;
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
-                            const int e = c * 32 + i;
+                            const int e = e0 + c * 32 + i;
                             const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
                             stash[i] = L;
-                            if (e < p.E) {
+                            if ((SPLIT || e < e_end)) {
                                 const float a = __fadd_rn(sigmoid_approx(L), sb_s[e]);
                                 const float ra = rank_a[(int)(((float)e + 0.5f) * inv_per)];
                                 if (ra >= rthr && a >= ra - 2.f * kApproxDelta) mask |= 1u << i;
@@ -345,7 +375,7 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                         while (mask) {
                             const int i = __ffs(mask) - 1;
                             mask &= mask - 1;
-                            const int e = c * 32 + i;
+                            const int e = e0 + c * 32 + i;
                             const float key = __fadd_rn(sigmoid_exact(stash[i]), sb_s[e]);
                             const int r = (int)(((float)e + 0.5f) * inv_per);
                             if (key > rank_x[r]) rank_x[r] = key;
@@ -364,16 +394,17 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                     uint32_t mask = 0;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const int e = c * 32 + i;
+                        const int e = e0 + c * 32 + i;
                         const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
                         stash[i] = L;
-                        if (e < p.E && L > thr && rank_ok(e)) mask |= 1u << i;
+                        nonfinite |= (SPLIT || e < e_end) && !(fabsf(L) <= FLT_MAX);
+                        if ((SPLIT || e < e_end) && L > thr && rank_ok(e)) mask |= 1u << i;
                     }
                     while (mask) {
                         const int i = __ffs(mask) - 1;
                         mask &= mask - 1;
                         const float L = stash[i];
-                        top.insert(L, L, c * 32 + i);
+                        top.insert(L, L, e0 + c * 32 + i);
                     }
                 }
             } else {
@@ -385,16 +416,17 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                     uint32_t mask = 0;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const int e = c * 32 + i;
+                        const int e = e0 + c * 32 + i;
                         const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
                         stash[i] = L;
+                        nonfinite |= (SPLIT || e < e_end) && !(fabsf(L) <= FLT_MAX);
                         const float a = __fadd_rn(sigmoid_approx(L), sb_s[e & 255]);
-                        if (e < p.E && a > thr && rank_ok(e)) mask |= 1u << i;
+                        if ((SPLIT || e < e_end) && a > thr && rank_ok(e)) mask |= 1u << i;
                     }
                     while (mask) {
                         const int i = __ffs(mask) - 1;
                         mask &= mask - 1;
-                        const int e = c * 32 + i;
+                        const int e = e0 + c * 32 + i;
                         const float a = __fadd_rn(sigmoid_approx(stash[i]), sb_s[e]);
                         approx.insert(a, 0.f, e);
                     }
@@ -405,63 +437,79 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                     uint32_t mask = 0;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const int e = c * 32 + i;
+                        const int e = e0 + c * 32 + i;
                         const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
                         stash[i] = L;
                         const float a = __fadd_rn(sigmoid_approx(L), sb_s[e & 255]);
-                        if (e < p.E && a >= thresh && rank_ok(e)) mask |= 1u << i;
+                        if ((SPLIT || e < e_end) && a >= thresh && rank_ok(e)) mask |= 1u << i;
                     }
                     while (mask) {
                         const int i = __ffs(mask) - 1;
                         mask &= mask - 1;
-                        const int e = c * 32 + i;
+                        const int e = e0 + c * 32 + i;
                         const float s = sigmoid_exact(stash[i]);
                         const float key = has_sb ? __fadd_rn(s, sb_s[e]) : s;
                         top.insert(key, s, e);
                     }
                 }
             }
-            // gates
-            // the k chosen experts are entries 8-k .. 7, best first
+            // gates; the k chosen experts are entries 8-k .. 7, best first
             const int j0 = 8 - p.k;
             float g[8];
+            float m = -INFINITY;  // softmax: the best logit (of this unit's experts)
+            float z = 0.f;        // softmax: the gate denominator
             if (!sigmoid) {
-                float m = -INFINITY;  // the best logit
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     if (j == j0) m = top.val[j];
-                float z = 0.f;
+            }
+            if (!sigmoid && !p.renorm) {
+                // full softmax: the sum over every expert (of this unit)
+                for (int c = 0; c < nchunks; ++c) {
+                    tmem_ld32(tb + (uint32_t)(c * 32), v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = e0 + c * 32 + i;
+                        if ((SPLIT || e < e_end)) {
+                            const float L = has_lb ? __fadd_rn(v[i], lb_s[e]) : v[i];
+                            z += expf(L - m);
+                        }
+                    }
+                }
+            }
+            if (SPLIT) {
+                // this slice's exact top-k (and partial softmax sum) for the merge
+                if (row_ok && t < p.T) {
+                    RoutePartial* pp = p.part + ((int64_t)t * p.split + h) * p.k;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (j >= j0) {
+                            pp[j - j0].key = top.key[j];
+                            pp[j - j0].val = top.val[j];
+                            pp[j - j0].idx = top.idx[j];
+                        }
+                    if (!sigmoid && !p.renorm) p.zpart[t * p.split + h] = make_float2(m, z);
+                }
+            } else if (!sigmoid) {
                 if (p.renorm) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         if (j >= j0) z += expf(top.val[j] - m);
-                } else {
-                    for (int c = 0; c < nchunks; ++c) {
-                        tmem_ld32(tb + (uint32_t)(c * 32), v);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int e = c * 32 + i;
-                            if (e < p.E) {
-                                const float L = has_lb ? __fadd_rn(v[i], lb_s[e]) : v[i];
-                                z += expf(L - m);
-                            }
-                        }
-                    }
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) g[j] = expf(top.val[j] - m) / z;
             } else {
-                float z = 0.f;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     if (j >= j0) z += top.val[j];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) g[j] = p.renorm ? top.val[j] / z : top.val[j];
             }
+            if (nonfinite && row_ok && t < p.T) atomicOr(p.status, MOE_DEV_NONFINITE);
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce0 + 8 * acc);
-            if (t < p.T) {
+            if (!SPLIT && row_ok && t < p.T) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     if (j >= j0) {
@@ -480,7 +528,105 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
     }
 }
 
+// The final top-k of a router whose experts were split across work units:
+// one thread per token inserts every slice's exact partial top-k into one
+// list (the same key order and tie rule, so the result is the top-k over all
+// experts), then computes the gates as the unsplit epilogue does.  Softmax
+// gates without renormalisation rescale the slices' partial sums to the
+// common maximum.
+__global__ void __launch_bounds__(256) route_merge_kernel(const RtParams p) {
+    pdl_wait();  // the router's partial lists
+    pdl_launch_dependents();
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= p.T) return;
+    TopK top;
+    top.init(p.k);
+    for (int h = 0; h < p.split; ++h) {
+        const RoutePartial* pp = p.part + (t * p.split + h) * p.k;
+        for (int jj = 0; jj < p.k; ++jj) top.insert(pp[jj].key, pp[jj].val, pp[jj].idx);
+    }
+    const int j0 = 8 - p.k;
+    float g[8];
+    if (p.score != MOE_SCORE_SIGMOID) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j == j0) m = top.val[j];
+        float z = 0.f;
+        if (p.renorm) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j >= j0) z += expf(top.val[j] - m);
+        } else {
+            for (int h = 0; h < p.split; ++h) {
+                const float2 mz = p.zpart[t * p.split + h];
+                z += mz.y * expf(mz.x - m);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = expf(top.val[j] - m) / z;
+    } else {
+        float z = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j >= j0) z += top.val[j];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = p.renorm ? top.val[j] / z : top.val[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (j >= j0) {
+            p.idx[t * p.k + (j - j0)] = top.idx[j];
+            p.gate[t * p.k + (j - j0)] = g[j];
+        }
+}
+
 }  // namespace
+
+// Expert slices per router tile.  A unit's time is about proportional to its
+// experts (tensor work and the epilogue's passes over the logits) plus a fixed
+// part (streaming x, the exact scores of the candidates), counted here as 32
+// experts; split when fewer waves of smaller units finish sooner.  Slices are
+// multiples of 32 experts.  Only unlimited routing with a partial-list buffer.
+int route_split(int64_t T, int E, int sms, bool allowed) {
+    if (!allowed || T <= 0 || T > kRouteSplitMaxT) return 1;
+    const int64_t m = (T + RM - 1) / RM;
+    int best = 1;
+    int64_t best_cost = (m + sms - 1) / sms * (32 + E);
+    for (int S = 2; S <= kRouteSplitMax; S *= 2) {
+        if (E % (32 * S) != 0) continue;
+        const int64_t cost = (m * S + sms - 1) / sms * (32 + E / S);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = S;
+        }
+    }
+    return best;
+}
+
+int64_t route_partial_bytes(int64_t T, int E) {
+    if (T <= 0 || T > kRouteSplitMaxT || E < 64 || E % 64 != 0) return 0;
+    return T * kRouteSplitMax * (8 * (int64_t)sizeof(RoutePartial) + (int64_t)sizeof(float2));
+}
+
+// Tokens per router tile.  With few experts (Np <= 64) the K loop is bound by
+// reading x, so what matters is the most rows any CTA streams: the tile height
+// (a multiple of 8, the swizzle atom's row count) that minimises
+// ceil(tiles / SMs) * height, the larger height on a tie.  With more experts
+// the M = 128 MMA (whatever the height) sets the tile's time: 128.
+int route_tile_rows(int64_t T, int Np, int sms) {
+    if (Np > 64 || T <= 0) return RM;
+    int best = RM;
+    int64_t best_cost = ((T + RM - 1) / RM + sms - 1) / sms * RM;
+    for (int tr = RM - 8; tr >= 8; tr -= 8) {
+        const int64_t cost = ((T + tr - 1) / tr + sms - 1) / sms * tr;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = tr;
+        }
+    }
+    return best;
+}
 
 int route_tc_supported(const RouteArgs& a) {
     if (a.dtype != MOE_DTYPE_BF16) return 1;
@@ -507,15 +653,23 @@ cudaError_t launch_route_tc(const RouteArgs& a, cudaStream_t s) {
     p.gate = a.gate;
     p.status = a.status;
     p.num_kb = (a.d + RK - 1) / RK;
-    p.m_tiles = (int)((a.T + RM - 1) / RM);
     p.R = a.R > 0 ? a.R : 1;
     p.max_ranks = (a.max_ranks > 0 && a.max_ranks < p.R && p.R <= 32) ? a.max_ranks : 0;
+    p.part = a.part;
+    p.zpart = a.part ? reinterpret_cast<float2*>(a.part + a.T * kRouteSplitMax * 8) : nullptr;
     p.stash_pitch = p.max_ranks > 0 ? STASH_PITCH_RANKS : STASH_PITCH;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int grid = p.m_tiles < sms ? p.m_tiles : sms;
-    p.stage_bytes = RM * RK * 2 + p.Np * RK * 2;
+    p.split = route_split(a.T, a.E, sms, p.max_ranks == 0 && a.part != nullptr);
+    p.Eh = p.E / p.split;
+    if (p.split > 1) p.Np = p.Eh;  // a multiple of 32
+    p.tile_rows = p.split > 1 ? RM : route_tile_rows(a.T, p.Np, sms);
+    p.m_tiles = (int)((a.T + p.tile_rows - 1) / p.tile_rows);
+    p.units = p.m_tiles * p.split;
+    const int grid = p.units < sms ? p.units : sms;
+    p.stage_bytes = RM * RK * 2 + p.Np * RK * 2;  // stage stride: a full 128-row A tile
+    p.tx_bytes = p.tile_rows * RK * 2 + p.Np * RK * 2;
     auto stages_for = [&](int groups) {
         const int extra = R_SMEM_FIXED + 128 * groups * p.stash_pitch * 4;
         const int ring = (R_SMEM_MAX - extra) < R_SMEM_TILES ? (R_SMEM_MAX - extra) : R_SMEM_TILES;
@@ -525,28 +679,31 @@ cudaError_t launch_route_tc(const RouteArgs& a, cudaStream_t s) {
     // A second epilogue group overlaps the epilogues of a CTA's tiles.  It pays
     // off once CTAs average two tiles; with fewer, only if its stash leaves the
     // TMA ring at least 4 stages deep (small E: stages are small).
-    p.epi_groups = (p.max_ranks == 0 && (p.m_tiles >= 2 * grid ||
-                                         (p.m_tiles > grid && stages_for(2) >= 4)))
+    p.epi_groups = (p.max_ranks == 0 && (p.units >= 2 * grid ||
+                                         (p.units > grid && stages_for(2) >= 4)))
                        ? 2 : 1;
     const int extra = R_SMEM_FIXED + 128 * p.epi_groups * p.stash_pitch * 4;
     p.stages = stages_for(p.epi_groups);
     CUtensorMap tmX, tmW;
-    if (!make_tmap_bf16(&tmX, a.x, (uint64_t)a.d, (uint64_t)a.T, 1, RM, 2) ||
+    if (!make_tmap_bf16(&tmX, a.x, (uint64_t)a.d, (uint64_t)a.T, 1, (uint32_t)p.tile_rows, 2) ||
         !make_tmap_bf16(&tmW, a.w, (uint64_t)a.d, (uint64_t)a.E, 1, (uint32_t)p.Np, 2))
         return cudaErrorInvalidValue;
     const int smem = p.stages * p.stage_bytes + extra;
     // the shared-memory limit is a per-device function attribute: raise it once per
     // device to the largest size used so far
     constexpr int kDevs = 64;
-    static int attr_bytes[kDevs] = {};
-    if (dev < 0 || dev >= kDevs || attr_bytes[dev] < smem) {
-        cudaError_t e =
-            cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static int attr_bytes[kDevs][2] = {};
+    const int form = p.split > 1 ? 1 : 0;
+    auto kern = p.split > 1 ? route_tc_kernel<true> : route_tc_kernel<false>;
+    if (dev < 0 || dev >= kDevs || attr_bytes[dev][form] < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kDevs) attr_bytes[dev] = smem;
+        if (dev >= 0 && dev < kDevs) attr_bytes[dev][form] = smem;
     }
-    route_tc_kernel<<<grid, 64 + 128 * p.epi_groups, smem, s>>>(tmX, tmW, p);
-    return cudaGetLastError();
+    cudaError_t e =
+        launch_pdl(kern, dim3(grid), 64 + 128 * p.epi_groups, (size_t)smem, s, tmX, tmW, p);
+    if (e != cudaSuccess || p.split == 1) return e;
+    return launch_pdl(route_merge_kernel, dim3((unsigned)((a.T + 255) / 256)), 256, 0, s, p);
 }
 
 }  // namespace moe

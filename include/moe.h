@@ -55,7 +55,7 @@ typedef enum moe_status {
     MOE_ERR_UNSUPPORTED = 2,  /* a valid combination this library does not run */
     MOE_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
     MOE_ERR_TIMEOUT = 4,      /* a bounded device wait gave up (status word) */
-    MOE_ERR_NONFINITE = 5,    /* reserved: non-finite input detected */
+    MOE_ERR_NONFINITE = 5,    /* a non-finite router logit was seen (status word) */
     MOE_ERR_BOUNDS = 6        /* an index left its range (status word) */
 } moe_status;
 
@@ -67,6 +67,10 @@ enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1, MOE_ACT_IDENTITY = 2 };
 /* 0x1u: unused */
 #define MOE_DEV_GEMM_TIMEOUT 0x2u     /* a tensor-core pipeline wait (expert GEMM or router) gave up */
 #define MOE_DEV_BAD_INDEX 0x4u        /* an expert index outside [0, E) reached dispatch */
+#define MOE_DEV_COPY_TIMEOUT 0x8u     /* a bulk row copy of dispatch did not land in time */
+#define MOE_DEV_NONFINITE 0x10u       /* a router logit was NaN or +-inf (x or w_router holds one) */
+#define MOE_DEV_BOUNDS 0x20u          /* checked build only: an index read from a caller's buffer
+                                         (slot_row, expert_offsets) was out of range */
 
 /*
  * Layer shape and method switches.
@@ -90,8 +94,7 @@ enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1, MOE_ACT_IDENTITY = 2 };
  *   Capacity": DeepSeek-V3 sends each token to experts on at most 4 nodes).
  *   A rank's score is the best selection key among its E/R experts; the
  *   max_ranks best ranks are kept (ties to the lower rank) and the top-k is
- *   taken among their experts.  Needs max_ranks <= R and max_ranks*(E/R) >= k;
- *   bf16 routers only (MOE_ERR_UNSUPPORTED for fp32).
+ *   taken among their experts.  Needs max_ranks <= R and max_ranks*(E/R) >= k.
  */
 typedef struct moe_config {
     int32_t T;
@@ -144,6 +147,10 @@ int64_t moe_max_rows(const moe_config* cfg);
  *   Selection key: L (softmax) or fp32(1/(1+exp(-L))) (+ sel_bias) (sigmoid).
  * Outputs: topk_idx [T,k] int32, experts in descending key order with ties
  * to the lower expert index; topk_gate [T,k] fp32.  ws: workspace.
+ * Device-side: every logit is checked; a NaN or infinite one (from a
+ * non-finite element of x or w_router, or an overflowing sum) sets
+ * MOE_DEV_NONFINITE in the status word, and that token's choices are then
+ * unspecified (other tokens are unaffected).
  */
 moe_status moe_route(const moe_config* cfg, const void* x, const void* w_router,
                      const float* logit_bias, const float* sel_bias, int32_t* topk_idx,
@@ -356,8 +363,25 @@ moe_status moe_update_sel_bias(const moe_config* cfg, const int32_t* expert_coun
                                float gamma, moe_stream_t stream);
 
 /* Copies the device status word of `ws` to *out (HOST pointer), waiting for
-   `stream`, then clears it.  MOE_OK with *out == 0 means no device error. */
+   `stream`, then clears it.  MOE_OK with *out == 0 means no device error.
+   In a checked build (below) it also reports, and clears, the bounds bit that
+   calls without a workspace (moe_combine, moe_combine_backward,
+   moe_dispatch_backward) record in a library-wide word. */
 moe_status moe_read_device_status(const void* ws, uint32_t* out, moe_stream_t stream);
+
+/*
+ * 1 if this library was built with MOE_CHECKED (libmoe_b300_checked.so), else
+ * 0.  A checked build is a debugging aid standing in for a memory checker: it
+ * range-checks every index the kernels read from a caller's buffer --
+ * slot_row entries in combine and in the two exchange backwards (kept rows
+ * must lie in [0, moe_max_rows)), the rows dispatch computes, and
+ * expert_offsets in the expert FFN and its backward (non-decreasing, within
+ * [0, moe_max_rows]; a sanitised copy in the workspace is what the kernels
+ * then read).  A violation sets MOE_DEV_BOUNDS and the access is skipped (a
+ * bad slot counts as dropped, a bad expert range as empty).  The release
+ * build performs none of these checks: such inputs are undefined there.
+ */
+int moe_build_checked(void);
 
 #ifdef __cplusplus
 }

@@ -151,13 +151,6 @@ def test_invalid_calls_fail_before_any_launch():
     assert e.value.status == moe.MOE_ERR_INVALID_ARG
 
 
-def test_rank_limited_fp32_router_is_unsupported():
-    c = _cfg(max_ranks=2)   # fp32 router: the rank limit runs on the tensor-core router only
-    with pytest.raises(moe.MoeError) as e:
-        moe.moe_route(c, 0x1000, 0x2000, None, None, 0x3000, 0x4000, 0x6000, stream=0)
-    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
-
-
 def test_empty_batch_is_a_noop():
     c = _cfg(T=0)
     moe.moe_route(c, None, None, None, None, None, None, None, stream=0)
@@ -256,3 +249,14 @@ def test_layer_forward_rejects_every_argument_error_before_any_launch(dtype, act
         # control: with every argument valid the call gets as far as a launch,
         # which fails here for want of a device
         assert _layer_args(c) == moe.MOE_ERR_CUDA
+
+
+def test_release_and_checked_builds_say_which_they_are():
+    assert moe.library().moe_build_checked() == 0
+    child = ("import sys; sys.path.insert(0, sys.argv[1]); import expert_dispatch_top_b300 as m; "
+             "print(m.LIB_PATH); print(m.moe_build_checked())")
+    r = subprocess.run(["python", "-c", child, ROOT], capture_output=True, text=True,
+                       env=dict(os.environ, MOE_B300_CHECKED="1"), timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    path, flag = r.stdout.strip().splitlines()[-2:]
+    assert path.endswith("libmoe_b300_checked.so") and flag == "True"

@@ -5,7 +5,7 @@ import torch
 import expert_dispatch_top_b300 as moe
 import moe_workloads as W
 import oracle
-from gpu_util import DEV, assert_rows_close
+from gpu_util import Guarded, DEV, assert_rows_close
 
 pytestmark = pytest.mark.gpu
 
@@ -36,10 +36,12 @@ def test_combine_matches_oracle(dtype, tol, T, d, E, k, cap, resid, shared):
     cfg = moe.make_config(T, d, E, k, 4, 64, 1 if shared else 0,
                           "bf16" if dtype == torch.bfloat16 else "f32", "softmax", True, 0.0, cap,
                           "gelu", resid)
-    y = torch.empty((T, d), dtype=dtype, device=DEV)
+    yg = Guarded((T, d), dtype, 0)
+    y = yg.t
     moe.moe_combine(cfg, yp.to(DEV), disp["slot_row"].to(DEV), gate.to(DEV),
                     sh.to(DEV) if shared else None, x.to(DEV) if resid else None, y)
     torch.cuda.synchronize()
+    yg.check("y")
     toks = torch.arange(T)
     ref = oracle.combine(toks, yp, torch.arange(yp.shape[0], dtype=torch.int32), disp["slot_row"],
                          gate, sh.double() if shared else None, x if resid else None)

@@ -70,3 +70,37 @@ def test_stall_hook_rejects_bad_arguments():
     cfg32 = moe.make_config(128, 128, 2, 1, 1, 128, 0, "f32", "softmax", True, 0.0, 0, "gelu")
     with pytest.raises(moe.MoeError):
         moe.moe_test_expert_ffn_stall(cfg32, *args, stall_kb=0, wait_limit_us=1000, ws=ws)
+
+
+@pytest.mark.parametrize("name,T", [("mixtral", 96), ("deepseek", 200), ("toy", 96),
+                                    ("switch", 150)])
+def test_nonfinite_router_input_is_reported(name, T):
+    """A NaN and an infinity planted in x on the host (plain data: nothing
+    faults) make those tokens' logits non-finite: the router sets
+    MOE_DEV_NONFINITE in the status word, and every other token is routed
+    exactly as the oracle routes it.  Clean inputs leave the bit clear."""
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w, ffn=False, T=T)
+    cfg = moe.config_from_workload(w, T=T)
+    dev = {k: (v.to(DEV) if torch.is_tensor(v) else v) for k, v in inp.items()}
+
+    def route(x):
+        idx = torch.zeros((T, w.k), dtype=torch.int32, device=DEV)
+        gate = torch.zeros((T, w.k), dtype=torch.float32, device=DEV)
+        ws = moe.alloc_workspace(cfg)
+        moe.moe_route(cfg, x, dev["w_router"], dev.get("logit_bias"), dev.get("sel_bias"), idx,
+                      gate, ws)
+        return idx.cpu(), moe.moe_read_device_status(ws)
+
+    _, clean = route(dev["x"])
+    assert clean == 0
+    x = inp["x"].clone()
+    x[5, 3] = float("nan")
+    x[T - 7, 0] = float("inf")
+    idx, status = route(x.to(DEV))
+    assert status == moe.MOE_DEV_NONFINITE
+    ridx, _ = oracle.route(inp["x"], inp["w_router"], w.k, w.score, w.renorm, inp["logit_bias"],
+                           inp["sel_bias"])
+    ok = torch.ones(T, dtype=torch.bool)
+    ok[5] = ok[T - 7] = False
+    assert torch.equal(idx[ok], ridx[ok])

@@ -7,7 +7,7 @@ import torch
 import expert_dispatch_top_b300 as moe
 import moe_workloads as W
 import oracle
-from gpu_util import DEV, assert_rows_close
+from gpu_util import Guarded, DEV, assert_rows_close
 
 pytestmark = pytest.mark.gpu
 
@@ -33,8 +33,9 @@ def _run_ffn(counts, d, f, act, dtype, seed, rows_cap=None, shared=False):
     cfg = moe.make_config(T, d, E, 1, 1, f, 1 if shared else 0,
                           "bf16" if dtype == torch.bfloat16 else "f32", "softmax", True, 0.0,
                           0, act)
-    h = torch.zeros((rows_cap, f), dtype=dtype, device=DEV)
-    yp = torch.full((rows_cap, d), 7.0, dtype=dtype, device=DEV)
+    hg = Guarded((rows_cap, f), dtype, 0)
+    ypg = Guarded((rows_cap, d), dtype, 7.0)
+    h, yp = hg.t, ypg.t
     ws = moe.alloc_workspace(cfg)
     sh_args = {}
     if shared:
@@ -48,6 +49,8 @@ def _run_ffn(counts, d, f, act, dtype, seed, rows_cap=None, shared=False):
                        **sh_args)
     torch.cuda.synchronize()
     assert moe.moe_read_device_status(ws) == 0
+    hg.check("h")
+    ypg.check("yp")
     tol = 2e-2 if dtype == torch.bfloat16 else 1e-4
     worst = 0.0
     for e in range(E):

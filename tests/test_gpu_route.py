@@ -41,9 +41,13 @@ def test_route_sweep_skew(s):
                                                (16, 3, "softmax", False), (32, 4, "sigmoid", True),
                                                (48, 5, "softmax", True), (64, 1, "softmax", False),
                                                (128, 6, "sigmoid", True), (256, 8, "sigmoid", True),
-                                               (200, 7, "softmax", True)])
+                                               (200, 7, "softmax", True), (192, 8, "softmax", False),
+                                               (64, 8, "sigmoid", False), (256, 2, "softmax", True)])
 def test_route_ties_and_shapes(E, k, score, renorm):
-    """A coarse weight grid makes exact ties common: the lower index must win."""
+    """A coarse weight grid makes exact ties common: the lower index must win.
+    At this T the tensor-core router cuts E = 64 ... 256 into expert slices
+    merged by a second kernel (96-expert slices for E = 192, with softmax
+    gates over all experts); E = 200 is not cut."""
     T = 257
     d = 8 if E <= 8 else 64       # short rows keep exact ties frequent for small E
     g = W._gen(E * 100 + k, "cpu")
@@ -140,18 +144,22 @@ def test_route_deterministic():
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("E,R,M,k,score", [(8, 4, 2, 2, "softmax"), (16, 4, 1, 3, "sigmoid"),
+                                            (32, 8, 2, 4, "sigmoid"), (32, 32, 3, 2, "softmax"),
                                             (64, 8, 3, 6, "softmax"), (96, 8, 2, 8, "sigmoid"),
                                             (256, 8, 4, 8, "sigmoid"), (256, 32, 5, 8, "softmax")])
-def test_route_rank_limited_ties(E, R, M, k, score):
+def test_route_rank_limited_ties(E, R, M, k, score, dtype):
     """Rank-limited routing (at most M of R ranks per token) on a coarse grid
-    with many exact ties, bit for bit against the oracle."""
+    with many exact ties, bit for bit against the oracle: the bf16 router on
+    the tensor cores and the fp32 FFMA routers (E <= 32 and E > 32 forms)."""
     T, d = 300, 64
     g = W._gen(E * 7 + M, "cpu")
-    x = W._grid_int((T, d), -8, 8, 8.0, g, "cpu").to(torch.bfloat16)
-    wr = W._grid_int((E, d), -1, 1, 512.0, g, "cpu").to(torch.bfloat16)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    x = W._grid_int((T, d), -8, 8, 8.0, g, "cpu").to(dt)
+    wr = W._grid_int((E, d), -1, 1, 512.0, g, "cpu").to(dt)
     sel = W._grid_int((E,), -1, 1, 4096.0, g, "cpu") if score == "sigmoid" else None
-    w = W.Workload("rl", T, d, E, R, k, 64, "identity", "bf16", score, True, 0.0, 0, 0,
+    w = W.Workload("rl", T, d, E, R, k, 64, "identity", dtype, score, True, 0.0, 0, 0,
                    "normal512", max_ranks=M)
     cfg = cfg_for(w)
     idx, gate = run_route(cfg, to_dev(dict(x=x, w_router=wr, logit_bias=None, sel_bias=sel)))
