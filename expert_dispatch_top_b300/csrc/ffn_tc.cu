@@ -26,7 +26,9 @@
 // by group, n-tile by n-tile, m-tile fastest (the 148 concurrent tiles share
 // one group's A rows and a few of its weight tiles through L2).  A tile that
 // runs past its group's last row reads the next group's rows (or TMA's zero
-// fill past the buffer); those output rows are computed and never stored.
+// fill past the buffer); those output rows are computed and never stored.  A
+// group's last tile with at most 64 rows issues M = 64 MMAs instead of M = 128
+// (row-offset and MN-major modes).
 // SwiGLU weights are [G, 2N, K] with the gate rows first: one B stage holds
 // 128 gate rows and the matching 128 up rows, so the accumulator holds gate
 // and up side by side and the epilogue writes 128 output columns per tile.
@@ -71,6 +73,12 @@ constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
 constexpr uint32_t kIdescBmn = idesc_bf16_bmn(BM, BN);
+// Tail tiles with at most 64 of their group's rows run M = 64 MMAs (half the
+// tensor work).  Their accumulator rows land in TMEM lanes 32*(r/16) + r%16:
+// lanes 0-15 of each warp's 32-lane quarter.
+constexpr int HALF_M = 64;
+constexpr uint32_t kIdesc64 = idesc_bf16(HALF_M, BN);
+constexpr uint32_t kIdescBmn64 = idesc_bf16_bmn(HALF_M, BN);
 constexpr uint32_t kIdescMn = idesc_bf16_bmn(BM, BN) | (1u << 15);  // A and B MN-major
 constexpr int MN_CHUNK = 64 * BK * 2;  // one 64-column x 64-row box of an MN-major B: 8 KB
 
@@ -308,8 +316,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                const int nkb = KG ? decode_tile<KG>(tile, p.G, tstart, mt, rowoff, grows, p).nkb
-                                   : p.num_kb;
+                const TileInfo ti = decode_tile<KG>(tile, p.G, tstart, mt, rowoff, grows, p);
+                const int nkb = KG ? ti.nkb : p.num_kb;
+                const bool half = !KG && ti.rows <= HALF_M;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT, p.wait_ns)) {
                         ok = false;
@@ -326,11 +335,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                                      (kb | kk) != 0 ? 1u : 0u);
                         else if (BMN)  // 16 K rows of 128 B per MMA
                             mma_bf16(d_tmem, sw128_desc(sa + kk * 32),
-                                     sw128_mn_desc(sb + kk * 2048, MN_CHUNK), kIdescBmn,
-                                     (kb | kk) != 0 ? 1u : 0u);
+                                     sw128_mn_desc(sb + kk * 2048, MN_CHUNK),
+                                     half ? kIdescBmn64 : kIdescBmn, (kb | kk) != 0 ? 1u : 0u);
                         else
-                            mma_bf16(d_tmem, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), kIdesc,
-                                     (kb | kk) != 0 ? 1u : 0u);
+                            mma_bf16(d_tmem, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32),
+                                     half ? kIdesc64 : kIdesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     commit(empty0 + 8 * stage);
                     if (++stage == STAGES) {
@@ -367,6 +376,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             const int col0 = ti.n_tile * p.out_cols;
+            const bool half = !KG && ti.rows <= HALF_M;  // M = 64: rows 16q + lane, lane < 16
             for (int c64 = 0; c64 < p.out_cols / 64; ++c64) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -404,11 +414,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int it = 0; it < 8; ++it) {
                     const int r = it * 4 + (lane >> 3);
-                    const int lr = q * 32 + r;  // row inside the tile
+                    // row inside the tile of staged row r (TMEM lane q*32 + r)
+                    const int lr = half ? (r < 16 ? q * 16 + r : BM) : q * 32 + r;
                     if (lr < ti.rows && gc < p.N) {
                         const uint4 w = *reinterpret_cast<const uint4*>(my_stg + r * STG_PITCH +
                                                                         (lane & 7) * 16);
-                        st_v4(obase + (int64_t)(ti.row0 + q * 32 + r) * p.N + gc, w);
+                        st_v4(obase + (int64_t)(ti.row0 + lr) * p.N + gc, w);
                     }
                 }
                 __syncwarp();
