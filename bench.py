@@ -55,8 +55,9 @@ UNIT = "tokens/s"
 # unchanged.  See profiles/ for the commands.
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the full
-    # Mixtral-shaped step: up 2.18 GB read + 0.928 GB written, down 5.20 GB + 0.265 GB.
-    "mixtral": {"bytes": 2.18e9 + 0.92834e9 + 5.20e9 + 0.2649e9, "src_hash": "aaa35b3fa1d43b50",
+    # Mixtral-shaped step: up 2.181 GB read + 0.929 GB written, down (banded tile
+    # order) 4.449 GB + 0.261 GB.
+    "mixtral": {"bytes": 2.1808e9 + 0.9288e9 + 4.4492e9 + 0.2615e9, "src_hash": "ada51b3f0ba79d98",
                 "per": "step (up + down launches)"},
 }
 

@@ -24,7 +24,9 @@
 //
 // Ragged groups: tiles are enumerated from the device-side row offsets, group
 // by group, n-tile by n-tile, m-tile fastest (the 148 concurrent tiles share
-// one group's A rows and a few of its weight tiles through L2).  A tile that
+// one group's A rows and a few of its weight tiles through L2); when a group's
+// rows of A are too large for that (the Mixtral-shaped down projection: 117 MB
+// of h per expert), in bands of 8 n-tiles with the m-tile fastest in a band.  A tile that
 // runs past its group's last row reads the next group's rows (or TMA's zero
 // fill past the buffer); those output rows are computed and never stored.  A
 // group's last tile with at most 64 rows issues M = 64 MMAs instead of M = 128
@@ -81,6 +83,8 @@ constexpr uint32_t kIdesc64 = idesc_bf16(HALF_M, BN);
 constexpr uint32_t kIdescBmn64 = idesc_bf16_bmn(HALF_M, BN);
 constexpr uint32_t kIdescMn = idesc_bf16_bmn(BM, BN) | (1u << 15);  // A and B MN-major
 constexpr int MN_CHUNK = 64 * BK * 2;  // one 64-column x 64-row box of an MN-major B: 8 KB
+constexpr int kBandTiles = 8;                      // n-tiles per band of the banded tile order
+constexpr int64_t kBandMinABytes = 64ll << 20;     // banded when a group's A exceeds this
 
 struct TcParams {
     const int32_t* offsets;
@@ -91,6 +95,7 @@ struct TcParams {
     int out_cols;  // output columns per tile (128 SwiGLU, 256 otherwise)
     int kg_M;      // K-grouped mode: rows of each group's output matrix
     int stall_kb;  // failure-detection hook (-1: off)
+    int band;      // > 0: tiles run in bands of `band` n-tiles, m-tile fastest inside a band
     uint64_t wait_ns;
     __nv_bfloat16* out;
     uint32_t* status;
@@ -138,6 +143,14 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, int G, const int* tsta
         ti.kb0 = rowoff[lo];
         ti.nkb = grows[lo];
     } else {
+        if (p.band > 0) {
+            // band b holds n-tiles [b*band, b*band + wb); its tiles run m-fastest
+            const int b = local / (mt[lo] * p.band);
+            const int wb = min(p.band, p.n_tiles - b * p.band);
+            const int lb = local - b * mt[lo] * p.band;
+            ti.m_tile = lb / wb;
+            ti.n_tile = b * p.band + (lb - ti.m_tile * wb);
+        }
         ti.row0 = rowoff[lo] + ti.m_tile * BM;
         ti.rows = grows[lo] - ti.m_tile * BM;
         ti.kb0 = 0;
@@ -497,6 +510,15 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
     p.status = a.status;
     p.kg_M = kg ? (int)rows_cap : 0;
     p.stall_kb = a.stall_kb;
+    // When one group's rows of A (the down projection's h) would not share L2 with
+    // its weights, the concurrent tiles should form a near-square block of the
+    // output so that both operands are re-read as little as possible: bands of
+    // kBandTiles n-tiles, m-tile fastest inside each band (a wave of 148 tiles
+    // then covers ~18 m-tiles x 8 n-tiles instead of every m-tile x ~4.6 n-tiles).
+    p.band = 0;
+    if (!kg && !bmn && a.offsets && a.G > 0 &&
+        rows_cap / a.G * (int64_t)a.K * 2 > kBandMinABytes && p.n_tiles > kBandTiles)
+        p.band = kBandTiles;
     p.wait_ns = a.wait_ns ? a.wait_ns : kWaitTimeoutNs;
 
     int dev = 0, sms = 148;
