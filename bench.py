@@ -14,9 +14,10 @@ between them, so the per-kernel times in `kernels` come from the same timed
 pass and add up to the step.  Inputs are larger than L2 (x 134 MB, weights
 2.8 GB), so no explicit L2 flush is needed.  `layer_forward` repeats the K
 steps through the single moe_layer_forward call as a cross-check, with its
-own clock record.  `e2e` adds, every step, the pinned host->device copy of x
-and the device->host copy of y (double-buffered on a copy stream, as a
-serving loop would run them).  `roofline` is for the dominant kernel (the
+own clock record.  `e2e` is the same metric through the C-ABI call with HOST
+buffers (moe_layer_forward_host: the pinned host->device copy of x, the
+layer and the device->host copy of y, every step; two layer instances
+alternate on two streams, as a serving loop would run them).  `roofline` is for the dominant kernel (the
 tcgen05 grouped GEMM): algorithmic FLOPs / its measured time, against the
 measured bf16 burst peak.  `configs` holds one record per other workload
 (the toy, Switch- and DeepSeek-shaped layers and the sweep's end points),
@@ -453,6 +454,38 @@ DEFAULT_CONFIGS = ["toy", "switch", "deepseek", "sweep_T4096_s0", "sweep_T4096_s
                    "sweep_T131072_s0", "sweep_T131072_s1.5"]
 
 
+def time_route_backward(args, w, cfg, b, inp, stream):
+    """Opt-in (--backward): time moe_route_backward (logit, input, weight and
+    logit-bias gradients) on the forward's choices with a seeded d_gate."""
+    import torch
+
+    import expert_dispatch_top_b300 as moe
+    import moe_workloads as W
+
+    g = W._gen(w.seed + 200, b.xp.device)
+    d_gate = torch.randn(tuple(b.topk_gate.shape), generator=g, device=b.xp.device)
+    d_logits = torch.empty((w.T, w.E), dtype=torch.float32, device=b.xp.device)
+    dx = torch.empty_like(inp["x"])
+    dw = torch.empty_like(inp["w_router"])
+    dlb = torch.empty(w.E, dtype=torch.float32, device=b.xp.device)
+
+    def call():
+        moe.moe_route_backward(cfg, inp["x"], inp["w_router"], inp.get("logit_bias"), b.topk_idx,
+                               d_gate, d_logits, dx, dw, dlb)
+
+    for _ in range(max(args.warmup, 1)):
+        call()
+    torch.cuda.synchronize()
+    n = max(args.steps // 4, 3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return {"ms": e0.elapsed_time(e1) / n, "calls": n}
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -528,44 +561,30 @@ def run_ours(args, w):
     lf_clocks = clk2.summary() if rank == 0 else None
     assert layer.device_status() == 0
 
-    # ---- e2e: pinned host x in, y out, every step ----
-    # Double-buffered like a serving loop: the H2D copy of step i+1 and the
-    # D2H copy of step i-1 run on a copy stream while step i computes.  Each
-    # step still moves its own x in and its own y out.
+    # ---- e2e: the C-ABI call with HOST buffers, every step ----
+    # moe_layer_forward_host copies the step's x in from pinned host memory, runs
+    # the layer and copies its y back out, all enqueued by the library.  Two
+    # layer instances (separate buffers, workspaces and staging) alternate on
+    # two streams, so one step's copies overlap the other step's kernels, as a
+    # serving loop would run them; each step still moves its own x and y.
+    layers = [layer, moe.MoeLayer(cfg, inp["w_router"], inp.get("w_up"), inp.get("w_down"),
+                                  inp.get("shared_up"), inp.get("shared_down"),
+                                  inp.get("logit_bias"), inp.get("sel_bias"), device=dev)]
+    e2e_streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
     xh = x.cpu().pin_memory()
     yh = [torch.empty(b.y.shape, dtype=b.y.dtype, pin_memory=True) for _ in range(2)]
     xd = [torch.empty_like(x) for _ in range(2)]
-    yd = [torch.empty_like(b.y) for _ in range(2)]
-    copy_s = torch.cuda.Stream(device=dev)
-    h2d_done = [torch.cuda.Event() for _ in range(2)]
-    y_ready = [torch.cuda.Event() for _ in range(2)]
-    d2h_done = [torch.cuda.Event() for _ in range(2)]
-    in_free = [torch.cuda.Event() for _ in range(2)]
 
     def e2e_run(n):
-        with torch.cuda.stream(copy_s):
-            xd[0].copy_(xh, non_blocking=True)
-            h2d_done[0].record(copy_s)
+        start = torch.cuda.Event()
+        start.record(stream)
+        for st in e2e_streams:
+            st.wait_event(start)
         for i in range(n):
-            cur, nxt = i % 2, (i + 1) % 2
-            if i + 1 < n:
-                with torch.cuda.stream(copy_s):
-                    if i >= 1:
-                        copy_s.wait_event(in_free[nxt])  # step i-1 finished reading xd[nxt]
-                    xd[nxt].copy_(xh, non_blocking=True)
-                    h2d_done[nxt].record(copy_s)
-            stream.wait_event(h2d_done[cur])
-            if i >= 2:
-                stream.wait_event(d2h_done[cur])       # yd[cur] drained by step i-2's D2H
-            y = layer(xd[cur])
-            yd[cur].copy_(y, non_blocking=True)
-            in_free[cur].record(stream)
-            y_ready[cur].record(stream)
-            with torch.cuda.stream(copy_s):
-                copy_s.wait_event(y_ready[cur])
-                yh[cur].copy_(yd[cur], non_blocking=True)
-                d2h_done[cur].record(copy_s)
-        stream.wait_stream(copy_s)
+            j = i % 2
+            layers[j].forward_host(xh, yh[j], xd[j], e2e_streams[j])
+        for st in e2e_streams:
+            stream.wait_stream(st)
 
     e2e_run(2)
     torch.cuda.synchronize()
@@ -576,6 +595,7 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     barrier()
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1)) / args.steps
+    assert all(lay.device_status() == 0 for lay in layers)
     bytes_in = x.numel() * x.element_size()
     bytes_out = b.y.numel() * b.y.element_size()
 
@@ -616,10 +636,12 @@ def run_ours(args, w):
                     "algorithmic_bytes_per_step": work["permute_bytes"]}
     if args.backward and not ident:
         kernels["ffn_backward"] = time_ffn_backward(args, w, cfg, b, inp, stream, peaks)
+    if args.backward:
+        kernels["route_backward"] = time_route_backward(args, w, cfg, b, inp, stream)
 
     configs = None
     if world == 1 and args.configs:
-        del layer, phases, xd, yd
+        del layer, layers, phases, xd
         inp = {kk: v for kk, v in inp.items() if kk == "x"}
         torch.cuda.empty_cache()
         configs = []
@@ -646,8 +668,9 @@ def run_ours(args, w):
                                   "events between them (the calls moe_layer_forward makes)"),
         "e2e": {"value": world * w.T / (e2e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": bytes_in, "d2h_bytes_per_step": bytes_out,
-                "via": "MoeLayer -> moe_layer_forward",
-                "overlap": "double-buffered: H2D(i+1) and D2H(i-1) on a copy stream during step i"},
+                "via": "moe_layer_forward_host (host x in, host y out; copies enqueued by the library)",
+                "overlap": "two layer instances alternate on two streams: one step's copies "
+                           "overlap the other's kernels"},
         "gpu_launches": per_step_launches * args.steps,
         "roofline": roofline,
         "kernels": kernels,
@@ -680,7 +703,8 @@ def main():
                     help="comma-separated workloads measured after the main line, each with its "
                          "own timed steps and clocks ('' to skip)")
     ap.add_argument("--backward", action="store_true",
-                    help="also time the expert-FFN backward (kernels.ffn_backward)")
+                    help="also time the expert-FFN and router backwards (kernels.ffn_backward, "
+                         "kernels.route_backward)")
     ap.add_argument("--cpu-step-s", type=float, default=8.0,
                     help="host seconds per cpu_baseline step (the token sample is sized to fit)")
     ap.add_argument("--ref-budget-s", type=float, default=150.0,

@@ -98,6 +98,11 @@ def _load():
     lib.moe_combine.restype = i32
     lib.moe_layer_forward.argtypes = [cfgp] + [vp] * 8 + [ctypes.POINTER(moe_buffers), vp, vp, vp]
     lib.moe_layer_forward.restype = i32
+    lib.moe_layer_forward_host.argtypes = [cfgp] + [vp] * 9 + [ctypes.POINTER(moe_buffers), vp, vp,
+                                                              vp, vp]
+    lib.moe_layer_forward_host.restype = i32
+    lib.moe_route_backward.argtypes = [cfgp] + [vp] * 10
+    lib.moe_route_backward.restype = i32
     lib.moe_combine_backward.argtypes = [cfgp] + [vp] * 7
     lib.moe_combine_backward.restype = i32
     lib.moe_dispatch_backward.argtypes = [cfgp] + [vp] * 4
@@ -241,6 +246,28 @@ def moe_layer_forward(cfg, x, w_router, logit_bias, sel_bias, w_up, w_down, shar
                                      _stream(stream)), "moe_layer_forward")
 
 
+def moe_route_backward(cfg, x, w_router, logit_bias, topk_idx, d_gate, d_logits, dx=None,
+                       d_w_router=None, d_logit_bias=None, stream=None):
+    """Backward of the router through its gates: d_logits [T,E] fp32 and, when
+    given, dx [T,d], d_w_router [E,d] and d_logit_bias [E]."""
+    _check(_load().moe_route_backward(ctypes.byref(cfg), _p(x), _p(w_router), _p(logit_bias),
+                                      _p(topk_idx), _p(d_gate), _p(d_logits), _p(dx),
+                                      _p(d_w_router), _p(d_logit_bias), _stream(stream)),
+           "moe_route_backward")
+
+
+def moe_layer_forward_host(cfg, x_host, x_dev, w_router, logit_bias, sel_bias, w_up, w_down,
+                           shared_up, shared_down, buffers: moe_buffers, y_dev, y_host, ws,
+                           stream=None):
+    """The layer with host input and output (x_host, y_host: CPU tensors, pinned for
+    asynchronous copies); x_dev, y_dev: device staging tensors [T, d]."""
+    _check(_load().moe_layer_forward_host(ctypes.byref(cfg), _p(x_host), _p(x_dev), _p(w_router),
+                                          _p(logit_bias), _p(sel_bias), _p(w_up), _p(w_down),
+                                          _p(shared_up), _p(shared_down), ctypes.byref(buffers),
+                                          _p(y_dev), _p(y_host), _p(ws), _stream(stream)),
+           "moe_layer_forward_host")
+
+
 def moe_combine_backward(cfg, dy, yp, slot_row, topk_gate, d_yp, d_gate, stream=None):
     """Reverse of the combine exchange: d_yp rows and gate gradients."""
     _check(_load().moe_combine_backward(ctypes.byref(cfg), _p(dy), _p(yp), _p(slot_row),
@@ -356,6 +383,20 @@ class MoeLayer:
         return self.buf.y
 
     __call__ = forward
+
+    def forward_host(self, x_host, y_host, x_dev=None, stream=None):
+        """Host x in, host y out through moe_layer_forward_host (x_dev: an optional
+        device staging tensor; the layer's own y buffer receives the result on the
+        device).  Returns y_host."""
+        if x_dev is None:
+            if getattr(self, "_x_dev", None) is None:
+                self._x_dev = torch.empty_like(self.buf.y)
+            x_dev = self._x_dev
+        moe_layer_forward_host(self.cfg, x_host, x_dev, self.w_router, self.logit_bias,
+                               self.sel_bias, self.w_up, self.w_down, self.shared_up,
+                               self.shared_down, self._cbuf, self.buf.y, y_host, self.buf.ws,
+                               stream)
+        return y_host
 
     def device_status(self) -> int:
         return moe_read_device_status(self.buf.ws)

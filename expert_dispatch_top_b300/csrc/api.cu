@@ -409,15 +409,20 @@ moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slo
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
-moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router,
-                             const float* logit_bias, const float* sel_bias, const void* w_up,
-                             const void* w_down, const void* shared_up, const void* shared_down,
-                             const moe_buffers* buf, void* y, void* ws, moe_stream_t stream) {
-    NvtxRange range("moe_layer_forward");
+}  // extern "C"
+
+namespace moe {
+namespace {
+
+// The layer's four steps; with check_only, every step's argument checks and
+// nothing else (so a caller can check before enqueueing anything of its own).
+moe_status layer_impl(const moe_config* cfg, const void* x, const void* w_router,
+                      const float* logit_bias, const float* sel_bias, const void* w_up,
+                      const void* w_down, const void* shared_up, const void* shared_down,
+                      const moe_buffers* buf, void* y, void* ws, cudaStream_t s, bool check_only) {
     moe_status st = moe_check_config(cfg);
     if (st != MOE_OK) return st;
     if (!buf || !ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const Layout L = layout_of(cfg);
     int32_t* idx = buf->topk_idx ? buf->topk_idx : at<int32_t>(ws, L.topk_idx);
     float* gate = buf->topk_gate ? buf->topk_gate : at<float>(ws, L.topk_gate);
@@ -436,7 +441,7 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w
 
     // Every step's checks first: an argument error returns before any launch.
     const void* yp = identity ? buf->xp : buf->yp;
-    for (int pass = 0; pass < 2; ++pass) {
+    for (int pass = 0; pass < (check_only ? 1 : 2); ++pass) {
         const bool check = pass == 0;
         st = route_impl(cfg, x, w_router, logit_bias, sel_bias, idx, gate, ws, s, check);
         if (st != MOE_OK) return st;
@@ -452,6 +457,89 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w
         if (st != MOE_OK) return st;
     }
     return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router,
+                             const float* logit_bias, const float* sel_bias, const void* w_up,
+                             const void* w_down, const void* shared_up, const void* shared_down,
+                             const moe_buffers* buf, void* y, void* ws, moe_stream_t stream) {
+    NvtxRange range("moe_layer_forward");
+    return layer_impl(cfg, x, w_router, logit_bias, sel_bias, w_up, w_down, shared_up, shared_down,
+                      buf, y, ws, reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+moe_status moe_layer_forward_host(const moe_config* cfg, const void* x_host, void* x_dev,
+                                  const void* w_router, const float* logit_bias,
+                                  const float* sel_bias, const void* w_up, const void* w_down,
+                                  const void* shared_up, const void* shared_down,
+                                  const moe_buffers* buf, void* y_dev, void* y_host, void* ws,
+                                  moe_stream_t stream) {
+    NvtxRange range("moe_layer_forward_host");
+    moe_status st = moe_check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (cfg->T > 0 && (!x_host || !y_host || !x_dev || !y_dev)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the layer's checks before the input copy is enqueued
+    st = layer_impl(cfg, x_dev, w_router, logit_bias, sel_bias, w_up, w_down, shared_up,
+                    shared_down, buf, y_dev, ws, s, true);
+    if (st != MOE_OK) return st;
+    const size_t bytes = (size_t)cfg->T * cfg->d * elem_bytes(cfg);
+    if (bytes && cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    st = layer_impl(cfg, x_dev, w_router, logit_bias, sel_bias, w_up, w_down, shared_up,
+                    shared_down, buf, y_dev, ws, s, false);
+    if (st != MOE_OK) return st;
+    if (bytes && cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_route_backward(const moe_config* cfg, const void* x, const void* w_router,
+                              const float* logit_bias, const int32_t* topk_idx,
+                              const float* d_gate, float* d_logits, void* dx, void* d_w_router,
+                              float* d_logit_bias, moe_stream_t stream) {
+    NvtxRange range("moe_route_backward");
+    moe_status st = moe_check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (cfg->T == 0) {
+        // no tokens: the weight and bias gradients are zero
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        if (d_w_router && !aligned16(d_w_router)) return MOE_ERR_INVALID_ARG;
+        if (d_w_router && cudaMemsetAsync(d_w_router, 0, (size_t)cfg->E * cfg->d * elem_bytes(cfg),
+                                          s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (d_logit_bias && cudaMemsetAsync(d_logit_bias, 0, (size_t)cfg->E * 4, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    if (!x || !w_router || !topk_idx || !d_gate || !d_logits) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_router) || !aligned16(dx) || !aligned16(d_w_router) ||
+        !aligned4(logit_bias) || !aligned4(topk_idx) || !aligned4(d_gate) || !aligned4(d_logits) ||
+        !aligned4(d_logit_bias))
+        return MOE_ERR_INVALID_ARG;
+    RouteBwdArgs a;
+    a.x = x;
+    a.w = w_router;
+    a.logit_bias = logit_bias;
+    a.idx = topk_idx;
+    a.d_gate = d_gate;
+    a.d_logits = d_logits;
+    a.dx = dx;
+    a.d_w = d_w_router;
+    a.d_logit_bias = d_logit_bias;
+    a.T = cfg->T;
+    a.d = cfg->d;
+    a.E = cfg->E;
+    a.k = cfg->k;
+    a.score = cfg->score;
+    a.renorm = cfg->renorm;
+    a.dtype = cfg->act_dtype;
+    return cuda_status(launch_route_backward(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_combine_backward(const moe_config* cfg, const void* dy, const void* yp,

@@ -55,7 +55,8 @@ __global__ void sanitize_offsets_kernel(const int32_t* in, int32_t* out, int G, 
 }
 
 // KMAX: compile-time bound on k; U: 16-byte column vectors per lane in flight.
-// U * KMAX = 8 keeps eight independent row loads in flight per lane.
+// U * KMAX = 8 keeps eight independent row loads in flight per lane (k = 1 has
+// its own variant, so that top-1 layers also keep eight).
 template <typename T, int KMAX, int U, bool PRE>
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     constexpr int V = Elem<T>::kPerVec;
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
 template <typename T>
 cudaError_t launch_combine_typed(const CombineArgs& a, unsigned blocks, cudaStream_t s) {
     const dim3 g(blocks);
+    if (a.k == 1) return launch_pdl(combine_kernel<T, 1, 8, false>, g, 256, 0, s, a);
     if (a.k <= 2) return launch_pdl(combine_kernel<T, 2, 4, false>, g, 256, 0, s, a);
     if (a.k <= 4) return launch_pdl(combine_kernel<T, 4, 2, false>, g, 256, 0, s, a);
     if (a.shared || a.resid) return launch_pdl(combine_kernel<T, 8, 1, true>, g, 256, 0, s, a);

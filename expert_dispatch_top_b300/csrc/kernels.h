@@ -144,6 +144,22 @@ size_t ffn_backward_scratch_bytes(int64_t rows_cap, int E, int d, int f, int gat
                                   int weight_grads);
 cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s);
 
+// Backward of the router through its gates (route_bwd.cu).
+struct RouteBwdArgs {
+    const void* x;          // [T, d]
+    const void* w;          // [E, d]
+    const float* logit_bias;
+    const int32_t* idx;     // [T, k]
+    const float* d_gate;    // [T, k]
+    float* d_logits;        // [T, E]
+    void* dx;               // [T, d] or null
+    void* d_w;              // [E, d] or null
+    float* d_logit_bias;    // [E] or null
+    int64_t T;
+    int d, E, k, score, renorm, dtype;
+};
+cudaError_t launch_route_backward(const RouteBwdArgs& a, cudaStream_t s);
+
 cudaError_t launch_update_sel_bias(const int32_t* counts, float* bias, int E, int64_t T, int k,
                                    float gamma, cudaStream_t s);
 

@@ -61,6 +61,7 @@ constexpr int R_SMEM_TILES = 221184;  // bytes of stage ring (at most)
 constexpr int R_SMEM_FIXED = 1024 /*align*/ + 256 /*barriers*/ + 2 * 256 * 4 /*biases*/;
 constexpr int R_SMEM_MAX = 232448;  // 227 KB per block
 constexpr float kApproxDelta = 1.0f / 256.0f;
+constexpr int kRouteKbs = 1;  // K blocks per ring stage with <= 64 experts
 static_assert((2 * R_MAX_STAGES + 5) * 8 <= 240, "barriers overlap the flags");
 
 struct RtParams {
@@ -75,6 +76,8 @@ struct RtParams {
     float* gate;
     uint32_t* status;
     int num_kb, m_tiles, stages, stage_bytes;
+    int kbs;        // K blocks per ring stage (their x boxes are issued back to back)
+    int num_st;     // ring stages per tile: num_kb / kbs
     int tile_rows;  // tokens per tile (multiple of 8, <= 128); the MMA always runs M = 128
     int tx_bytes;   // bytes one stage's TMA loads deliver
     // Expert split: each tile's experts are cut into `split` slices of Eh
@@ -222,18 +225,22 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
             for (int unit = blockIdx.x; unit < p.units && !*abort_flag; unit += gridDim.x) {
                 const int tile = SPLIT ? unit / p.split : unit;
                 const int e0 = SPLIT ? (unit - tile * p.split) * p.Eh : 0;  // first expert of the slice
-                const int kb0 = k_start(unit, p.num_kb);
-                for (int i = 0; i < p.num_kb; ++i) {
-                    int kb = kb0 + i;
-                    if (kb >= p.num_kb) kb -= p.num_kb;
+                const int ks0 = k_start(unit, p.num_st);
+                for (int i = 0; i < p.num_st; ++i) {
+                    int ks = ks0 + i;
+                    if (ks >= p.num_st) ks -= p.num_st;
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status,
                                    MOE_DEV_GEMM_TIMEOUT))
                         break;
                     const uint32_t fb = full0 + 8 * stage;
                     mbar_expect_tx(fb, p.tx_bytes);
                     const uint32_t sa = smem_u32(smem + stage * p.stage_bytes);
-                    tma_load_2d(sa, &tmX, kb * RK, tile * p.tile_rows, fb);
-                    tma_load_2d(sa + RM * RK * 2, &tmW, kb * RK, e0, fb);
+                    const uint32_t sw = sa + p.kbs * (RM * RK * 2);
+                    for (int j = 0; j < p.kbs; ++j)
+                        tma_load_2d(sa + j * (RM * RK * 2), &tmX, (ks * p.kbs + j) * RK,
+                                    tile * p.tile_rows, fb);
+                    for (int j = 0; j < p.kbs; ++j)
+                        tma_load_2d(sw + j * (p.Np * RK * 2), &tmW, (ks * p.kbs + j) * RK, e0, fb);
                     if (++stage == p.stages) {
                         stage = 0;
                         phase ^= 1;
@@ -257,7 +264,7 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                 }
                 fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
-                for (int i = 0; i < p.num_kb; ++i) {
+                for (int i = 0; i < p.num_st; ++i) {
                     if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status,
                                    MOE_DEV_GEMM_TIMEOUT)) {
                         ok = false;
@@ -265,11 +272,14 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                     }
                     fence_after();
                     const uint32_t sa = smem_u32(smem + stage * p.stage_bytes);
-                    const uint32_t sb = sa + RM * RK * 2;
+                    const uint32_t sw = sa + p.kbs * (RM * RK * 2);
+                    for (int j = 0; j < p.kbs; ++j) {
 #pragma unroll
-                    for (int kk = 0; kk < RK / 16; ++kk)
-                        mma_bf16(d_tmem, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), idesc,
-                                 (i | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < RK / 16; ++kk)
+                            mma_bf16(d_tmem, sw128_desc(sa + j * (RM * RK * 2) + kk * 32),
+                                     sw128_desc(sw + j * (p.Np * RK * 2) + kk * 32), idesc,
+                                     (i | j | kk) != 0 ? 1u : 0u);
+                    }
                     commit(empty0 + 8 * stage);
                     if (++stage == p.stages) {
                         stage = 0;
@@ -668,8 +678,13 @@ cudaError_t launch_route_tc(const RouteArgs& a, cudaStream_t s) {
     p.m_tiles = (int)((a.T + p.tile_rows - 1) / p.tile_rows);
     p.units = p.m_tiles * p.split;
     const int grid = p.units < sms ? p.units : sms;
-    p.stage_bytes = RM * RK * 2 + p.Np * RK * 2;  // stage stride: a full 128-row A tile
-    p.tx_bytes = p.tile_rows * RK * 2 + p.Np * RK * 2;
+    // Few experts: the K loop only streams x; a stage of kRouteKbs K blocks reads
+    // kRouteKbs * 128 contiguous bytes of each row at once.
+    p.kbs = (p.Np <= 64 && p.num_kb % kRouteKbs == 0) ? kRouteKbs : 1;
+    p.num_st = p.num_kb / p.kbs;
+    // stage stride: full 128-row A tiles
+    p.stage_bytes = p.kbs * (RM * RK * 2 + p.Np * RK * 2);
+    p.tx_bytes = p.kbs * (p.tile_rows * RK * 2 + p.Np * RK * 2);
     auto stages_for = [&](int groups) {
         const int extra = R_SMEM_FIXED + 128 * groups * p.stash_pitch * 4;
         const int ring = (R_SMEM_MAX - extra) < R_SMEM_TILES ? (R_SMEM_MAX - extra) : R_SMEM_TILES;

@@ -266,6 +266,34 @@ moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slo
                        void* y, moe_stream_t stream);
 
 /*
+ * Backward of Step 1 (training: topicspectrum "Training teaches both experts
+ * and router").  Which experts a token picks is piecewise constant in the
+ * logits, so no gradient flows through the selection (nor into the
+ * selection-only bias, nor through rank limiting); it flows through the gates.
+ * For a token with chosen experts e_j, gates g_j and dg_j = dL/dtopk_gate:
+ *   softmax, renorm:  dlogit[e_j] = g_j (dg_j - sum_i g_i dg_i), 0 elsewhere;
+ *   softmax, full:    dlogit[e] = p_e (dg_e - sum_j p_(e_j) dg_j) for every e
+ *                     (p: softmax over all experts; dg_e = 0 off the choice);
+ *   sigmoid, renorm:  dlogit[e_j] = (dg_j - sum_i g_i dg_i) / (sum_i s_i)
+ *                     * s_j (1 - s_j), s = sigmoid(logit);
+ *   sigmoid:          dlogit[e_j] = dg_j s_j (1 - s_j).
+ * Then dx[t] = sum_e dlogit[t,e] w_router[e], d_w_router[e] = sum_t
+ * dlogit[t,e] x[t], d_logit_bias[e] = sum_t dlogit[t,e].
+ *   x [T,d], w_router [E,d], logit_bias [E] or NULL: the forward's inputs (the
+ *   needed logits are recomputed); topk_idx [T,k]: the forward's choices
+ *   (an index outside [0,E) is read as expert 0 with no gradient);
+ *   d_gate [T,k] fp32, e.g. from moe_combine_backward.
+ * Outputs (overwritten): d_logits [T,E] fp32, required; dx [T,d] and
+ * d_w_router [E,d] (act dtype, one rounding of fp32 sums) and d_logit_bias
+ * [E] fp32, each NULL to skip.  The weight gradient sums the tokens in order
+ * (deterministic).
+ */
+moe_status moe_route_backward(const moe_config* cfg, const void* x, const void* w_router,
+                              const float* logit_bias, const int32_t* topk_idx,
+                              const float* d_gate, float* d_logits, void* dx, void* d_w_router,
+                              float* d_logit_bias, moe_stream_t stream);
+
+/*
  * Backward of Step 4 (the reverse of the combine exchange).  Combine is
  * linear in the expert outputs and in the gates, so for dy = dL/dy [T,d]:
  *   d_yp[slot_row[t,j]] = topk_gate[t,j] * dy[t] for every kept slot (one
@@ -348,6 +376,25 @@ moe_status moe_layer_forward(const moe_config* cfg, const void* x, const void* w
                              const float* logit_bias, const float* sel_bias, const void* w_up,
                              const void* w_down, const void* shared_up, const void* shared_down,
                              const moe_buffers* buf, void* y, void* ws, moe_stream_t stream);
+
+/*
+ * The whole layer with HOST input and output, for a caller that holds x and
+ * wants y in host memory: enqueues on `stream` the copy of x_host [T,d] into
+ * x_dev, moe_layer_forward on x_dev (y into y_dev), and the copy of y_dev
+ * into y_host [T,d].  x_host and y_host are HOST pointers (page-locked memory
+ * keeps the copies asynchronous; pageable memory makes them synchronous);
+ * x_dev and y_dev are caller-owned device buffers of T*d elements.  Nothing is
+ * allocated.  All of moe_layer_forward's argument checks run before the first
+ * copy is enqueued; y_host holds the result once the stream has reached the
+ * end of the call.  Two calls may overlap on two streams only with separate
+ * buffers, workspaces and staging buffers.
+ */
+moe_status moe_layer_forward_host(const moe_config* cfg, const void* x_host, void* x_dev,
+                                  const void* w_router, const float* logit_bias,
+                                  const float* sel_bias, const void* w_up, const void* w_down,
+                                  const void* shared_up, const void* shared_down,
+                                  const moe_buffers* buf, void* y_dev, void* y_host, void* ws,
+                                  moe_stream_t stream);
 
 /*
  * Bias-based balancing (Ultralytics "Load Balancing and Capacity": DeepSeek-V3

@@ -78,6 +78,9 @@ def _load():
         lib.oracle_update_sel_bias.restype = None
         lib.oracle_expert_ffn_backward.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                                    vp]
+        lib.oracle_route_backward.argtypes = [i64, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                              vp, vp, vp, vp]
+        lib.oracle_route_backward.restype = None
         lib.oracle_expert_ffn_backward.restype = None
         lib.oracle_combine_backward.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         lib.oracle_combine_backward.restype = None
@@ -267,6 +270,27 @@ def dispatch_backward(d_xp, slot_row, T):
     _load().oracle_dispatch_backward(T, d, sr.shape[1], _dtype_code(d_xp), _ptr(d_xp), _ptr(sr),
                                      _ptr(dx))
     return dx
+
+
+def route_backward(x, w_router, topk_idx, d_gate, score="softmax", renorm=True, logit_bias=None):
+    """Backward of the router through its gates: (d_logits fp64 [T,E], dx fp64 [T,d],
+    dw fp64 [E,d], d_logit_bias fp64 [E]).  The selection itself carries no gradient."""
+    x = _cpu(x)
+    w = _cpu(w_router, x.dtype)
+    T, d = x.shape
+    E = w.shape[0]
+    idx = _cpu(topk_idx, torch.int32)
+    k = idx.shape[1]
+    dg = _cpu(d_gate, torch.float32)
+    lb = _cpu(logit_bias, torch.float32)
+    dL = torch.zeros((T, E), dtype=torch.float64)
+    dx = torch.zeros((T, d), dtype=torch.float64)
+    dw = torch.zeros((E, d), dtype=torch.float64)
+    dlb = torch.zeros(E, dtype=torch.float64)
+    _load().oracle_route_backward(T, d, E, k, _dtype_code(x), _SCORES[score], int(bool(renorm)),
+                                  _ptr(x), _ptr(w), _ptr(lb), _ptr(idx), _ptr(dg), _ptr(dL),
+                                  _ptr(dx), _ptr(dw), _ptr(dlb))
+    return dL, dx, dw, dlb
 
 
 def layer_forward(x, w_router, *, k, E, R, d_ff, act, score="softmax", renorm=True,

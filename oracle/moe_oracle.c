@@ -529,3 +529,98 @@ void oracle_expert_ffn_backward(int64_t n_rows, int d, int f, int act, int dtype
     free(dpre);
     free(dy);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Backward of Step 1, Route: the router is trained through its gates       */
+/* (topicspectrum, Training teaches both experts and router).  Which        */
+/* experts a token picks is piecewise constant in the logits, so no         */
+/* gradient flows through the selection (nor into the selection-only bias); */
+/* it flows through the gates, each a function of the logits L = x W^T + b: */
+/*   softmax, renormalised: g_j = exp(L_j) / sum over chosen i of exp(L_i)  */
+/*     dL_j = g_j (dg_j - sum_i g_i dg_i) for chosen j, 0 for the others;    */
+/*   softmax, full: g_j = p_(e_j), p the softmax over all E experts          */
+/*     dL_e = p_e (dg_e - sum_j p_(e_j) dg_j) for every e (dg_e = 0 unless   */
+/*     e was chosen);                                                        */
+/*   sigmoid, renormalised: g_j = s_j / sum over chosen i of s_i, s = sig(L) */
+/*     ds_j = (dg_j - sum_i g_i dg_i) / sum_i s_i, dL_j = ds_j s_j (1 - s_j);*/
+/*   sigmoid: g_j = s_j, dL_j = dg_j s_j (1 - s_j).                          */
+/* Then d_logit_bias[e] = sum_t dL[t,e], dx[t] = sum_e dL[t,e] W[e] and      */
+/* dW[e] = sum_t dL[t,e] x[t].  Everything in fp64 from the inputs (the      */
+/* logits recomputed in fp64; exact on the dyadic test grid).               */
+/* ------------------------------------------------------------------------ */
+void oracle_route_backward(int64_t T, int d, int E, int k, int dtype, int score, int renorm,
+                           const void* x, const void* w_router, const float* logit_bias,
+                           const int32_t* topk_idx, const float* d_gate, double* d_logits,
+                           double* dx, double* dw, double* d_logit_bias) {
+#pragma omp parallel
+    {
+        double* L = (double*)malloc(sizeof(double) * E);
+        double* g = (double*)malloc(sizeof(double) * k);
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < T; ++t) {
+            for (int e = 0; e < E; ++e) {
+                double acc = 0.0;
+                for (int i = 0; i < d; ++i)
+                    acc += elem(x, dtype, t * (int64_t)d + i) * elem(w_router, dtype, (int64_t)e * d + i);
+                L[e] = acc + (logit_bias ? (double)logit_bias[e] : 0.0);
+            }
+            const int32_t* idx = topk_idx + t * k;
+            const float* dg = d_gate + t * k;
+            double* dL = d_logits + t * E;
+            for (int e = 0; e < E; ++e) dL[e] = 0.0;
+            if (score == OR_SOFTMAX && renorm) {
+                double m = -INFINITY, z = 0.0, dot = 0.0;
+                for (int j = 0; j < k; ++j) m = fmax(m, L[idx[j]]);
+                for (int j = 0; j < k; ++j) z += exp(L[idx[j]] - m);
+                for (int j = 0; j < k; ++j) {
+                    g[j] = exp(L[idx[j]] - m) / z;
+                    dot += g[j] * (double)dg[j];
+                }
+                for (int j = 0; j < k; ++j) dL[idx[j]] = g[j] * ((double)dg[j] - dot);
+            } else if (score == OR_SOFTMAX) {
+                double m = -INFINITY, z = 0.0, dot = 0.0;
+                for (int e = 0; e < E; ++e) m = fmax(m, L[e]);
+                for (int e = 0; e < E; ++e) z += exp(L[e] - m);
+                for (int j = 0; j < k; ++j) dot += exp(L[idx[j]] - m) / z * (double)dg[j];
+                for (int e = 0; e < E; ++e) dL[e] = -exp(L[e] - m) / z * dot;
+                for (int j = 0; j < k; ++j) dL[idx[j]] += exp(L[idx[j]] - m) / z * (double)dg[j];
+            } else {
+                double sum = 0.0, dot = 0.0;
+                for (int j = 0; j < k; ++j) sum += 1.0 / (1.0 + exp(-L[idx[j]]));
+                for (int j = 0; j < k; ++j) {
+                    g[j] = (1.0 / (1.0 + exp(-L[idx[j]]))) / sum;
+                    dot += g[j] * (double)dg[j];
+                }
+                for (int j = 0; j < k; ++j) {
+                    const double s = 1.0 / (1.0 + exp(-L[idx[j]]));
+                    const double ds = renorm ? ((double)dg[j] - dot) / sum : (double)dg[j];
+                    dL[idx[j]] = ds * s * (1.0 - s);
+                }
+            }
+            if (dx)
+                for (int i = 0; i < d; ++i) {
+                    double acc = 0.0;
+                    for (int e = 0; e < E; ++e)
+                        acc += dL[e] * elem(w_router, dtype, (int64_t)e * d + i);
+                    dx[t * d + i] = acc;
+                }
+        }
+        free(L);
+        free(g);
+    }
+    if (dw)
+#pragma omp parallel for schedule(static)
+        for (int e = 0; e < E; ++e)
+            for (int i = 0; i < d; ++i) {
+                double acc = 0.0;
+                for (int64_t t = 0; t < T; ++t)
+                    acc += d_logits[t * E + e] * elem(x, dtype, t * (int64_t)d + i);
+                dw[(int64_t)e * d + i] = acc;
+            }
+    if (d_logit_bias)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < T; ++t) acc += d_logits[t * E + e];
+            d_logit_bias[e] = acc;
+        }
+}

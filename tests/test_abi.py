@@ -260,3 +260,41 @@ def test_release_and_checked_builds_say_which_they_are():
     assert r.returncode == 0, r.stderr[-2000:]
     path, flag = r.stdout.strip().splitlines()[-2:]
     assert path.endswith("libmoe_b300_checked.so") and flag == "True"
+
+
+def test_route_backward_rejects_bad_arguments_before_any_launch():
+    lib = moe.library()
+    c = _cfg(dtype="bf16", act="swiglu")
+
+    def call(x=0x1000, w=0x2000, lb=None, idx=0x3000, dg=0x4000, dl=0x5000, dx=0x6000, dw=0x7000,
+             dlb=None):
+        return lib.moe_route_backward(ctypes.byref(c), x, w, lb, idx, dg, dl, dx, dw, dlb, None)
+    assert call(dl=None) == moe.MOE_ERR_INVALID_ARG          # d_logits is required
+    assert call(x=None) == moe.MOE_ERR_INVALID_ARG
+    assert call(dx=0x6008) == moe.MOE_ERR_INVALID_ARG        # misaligned dx
+    assert call(idx=0x3002) == moe.MOE_ERR_INVALID_ARG       # misaligned topk_idx
+    assert lib.moe_route_backward(ctypes.byref(_cfg(k=0)), 0x1000, 0x2000, None, 0x3000, 0x4000,
+                                  0x5000, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_layer_forward_host_checks_before_its_first_copy():
+    """moe_layer_forward_host runs the layer's argument checks before it
+    enqueues the input copy: on this GPU-less host a copy that went out would
+    fail as MOE_ERR_CUDA, an argument error comes back as MOE_ERR_INVALID_ARG."""
+    import torch
+    lib = moe.library()
+    c = _cfg(dtype="bf16", act="swiglu")
+    host = (ctypes.c_uint8 * 64)()
+    buf = moe.moe_buffers(xp=0x70000, h=0x80000, yp=0x90000)
+
+    def call(x_host=ctypes.addressof(host), y_host=ctypes.addressof(host), w_up=0x30000,
+             x_dev=0x10000, y_dev=0x50000):
+        return lib.moe_layer_forward_host(ctypes.byref(c), x_host, x_dev, 0x20000, None, None,
+                                          w_up, 0x40000, None, None, ctypes.byref(buf), y_dev,
+                                          y_host, 0x60000, None)
+    assert call(y_host=None) == moe.MOE_ERR_INVALID_ARG
+    assert call(x_dev=None) == moe.MOE_ERR_INVALID_ARG
+    assert call(w_up=None) == moe.MOE_ERR_INVALID_ARG          # a layer argument
+    assert call(y_dev=0x50008) == moe.MOE_ERR_INVALID_ARG       # misaligned staging y
+    if not torch.cuda.is_available():
+        assert call() == moe.MOE_ERR_CUDA                        # valid: gets as far as the copy

@@ -26,6 +26,8 @@ def _setup(T, d, E, k, R, cap, dtype, seed):
 @pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, 2e-2), (torch.float32, 1e-4)])
 @pytest.mark.parametrize("T,d,E,k,cap,resid,shared", [
     (1, 64, 4, 2, 0, False, False),
+    (3000, 1024, 64, 1, 40, True, False),   # top-1 (its own eight-in-flight variant), drops
+    (2049, 576, 16, 1, 0, False, True),     # top-1, 72 vectors per bf16 row (not a multiple of 32)
     (333, 128, 8, 2, 60, False, False),
     (333, 128, 8, 2, 60, True, False),
     (1024, 512, 64, 8, 90, True, True),

@@ -133,3 +133,22 @@ def test_layer_full_size_sampled(name):
         toks = torch.unique(torch.cat([toks, dropped[:64]]))
     ref = _oracle(w, inp, False, tokens=toks)
     _compare(w, layer, y, ref, toks)
+
+
+@pytest.mark.parametrize("name,T", [("deepseek", 96), ("toy", 500), ("switch", 700)])
+def test_layer_forward_host_equals_device_call(name, T):
+    """moe_layer_forward_host (host x in, host y out, copies enqueued by the
+    library) gives the device call's output bit for bit, twice in a row."""
+    w = W.WORKLOADS[name]
+    if name == "deepseek":
+        w = w.replace(d=512, add_residual=True)
+    inp = W.make_inputs(w, T=T)
+    dev = to_dev(inp)
+    layer, y = _run_layer(w, dev, T, w.add_residual)
+    x_host = inp["x"].contiguous().pin_memory()
+    for _ in range(2):
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        layer.forward_host(x_host, y_host)
+        torch.cuda.synchronize()
+        assert layer.device_status() == 0
+        assert torch.equal(y_host, y.cpu())

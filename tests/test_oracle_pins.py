@@ -638,3 +638,61 @@ def test_expert_ffn_backward_matches_autograd(act):
     assert torch.allclose(d_in, xd.grad, rtol=1e-10, atol=1e-12)
     assert torch.allclose(dwu, wud.grad, rtol=1e-10, atol=1e-12)
     assert torch.allclose(dwd, wdd.grad, rtol=1e-10, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Router backward: gradients through the gates (training the router)
+# --------------------------------------------------------------------------
+
+def _router_autograd(x, w, lb, idx, dg, score, renorm):
+    """fp64 autograd of the forward gate definitions, with the selection fixed."""
+    X = x.double().clone().requires_grad_(True)
+    Wt = w.double().clone().requires_grad_(True)
+    B = (lb.double() if lb is not None else torch.zeros(w.shape[0], dtype=torch.float64))
+    B = B.clone().requires_grad_(True)
+    L = X @ Wt.T + B
+    L.retain_grad()
+    ix = idx.long()
+    Lc = L.gather(1, ix)
+    if score == "softmax" and renorm:
+        g = torch.softmax(Lc, dim=1)
+    elif score == "softmax":
+        g = torch.softmax(L, dim=1).gather(1, ix)
+    elif renorm:
+        s = torch.sigmoid(Lc)
+        g = s / s.sum(1, keepdim=True)
+    else:
+        g = torch.sigmoid(Lc)
+    (g * dg.double()).sum().backward()
+    return L.grad, X.grad, Wt.grad, B.grad
+
+
+@pytest.mark.parametrize("score,renorm", [("softmax", True), ("softmax", False),
+                                          ("sigmoid", True), ("sigmoid", False)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_router_backward_matches_autograd(score, renorm, dtype):
+    """The oracle's router backward equals fp64 autograd of the gate
+    definitions on a fixed selection, for each gate form, with a logit bias;
+    the selection-only bias (sigmoid) changes the selection but not the
+    gradient formula."""
+    T, d, E, k = 24, 32, 16, 3
+    g = W._gen(41, "cpu")
+    x = W._grid_int((T, d), -8, 8, 8.0, g, "cpu").to(dtype)
+    w = W._grid_int((E, d), -8, 8, 64.0, g, "cpu").to(dtype)
+    lb = W._grid_int((E,), -8, 8, 64.0, g, "cpu")
+    sel = W._grid_int((E,), -8, 8, 256.0, g, "cpu") if score == "sigmoid" else None
+    idx, _ = oracle.route(x, w, k, score, renorm, lb, sel)
+    dg = torch.randn((T, k), generator=torch.Generator().manual_seed(5))
+    dL, dx, dw, dlb = oracle.route_backward(x, w, idx, dg, score, renorm, lb)
+    rL, rx, rw, rb = _router_autograd(x, w, lb, idx, dg, score, renorm)
+    for got, ref in ((dL, rL), (dx, rx), (dw, rw), (dlb, rb)):
+        assert torch.allclose(got, ref, rtol=1e-10, atol=1e-12)
+    if score != "softmax" or renorm:
+        # only the chosen experts' logits carry gradient
+        mask = torch.zeros((T, E), dtype=torch.bool)
+        mask.scatter_(1, idx.long(), True)
+        assert torch.all(dL[~mask] == 0)
+    if score == "softmax" and renorm:
+        # renormalised softmax gates sum to 1 whatever the logits: the
+        # gradient is orthogonal to a common shift of the chosen logits
+        assert torch.allclose(dL.sum(1), torch.zeros(T, dtype=torch.float64), atol=1e-12)
