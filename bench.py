@@ -416,9 +416,10 @@ class L2Flush:
 
 
 def measure_config(moe, W, w, dev, stream, peaks, sms, uuid, target_ms=400.0):
-    """One per-config record for the bench line: inputs drawn on the device,
-    3 warm-up steps, then K steps (K sized to ~target_ms of step time, 20..200)
-    with L2 flushed before each step; the four calls timed with events, clocks
+    """One per-config record for the bench line: inputs drawn on the device, a
+    1 s pause and ~0.2 s of warm-up steps (the clocks settle after the previous
+    workload), then K steps (K sized to ~target_ms of step time, 20..200) with
+    L2 flushed before each step; the four calls timed with events, clocks
     sampled during the timed steps."""
     import torch
     inp = W.make_inputs(w, device=dev)
@@ -427,7 +428,13 @@ def measure_config(moe, W, w, dev, stream, peaks, sms, uuid, target_ms=400.0):
     x = inp["x"]
     phases = _phase_calls(moe, cfg, w, inp, b, x)
     flush = L2Flush(dev)
+    # let the clocks and power settle after the previous workload, then warm up
+    # for ~0.2 s of this workload's own steps before timing
+    torch.cuda.synchronize()
+    time.sleep(1.0)
     _, per, _ = timed_steps(3, phases, stream, flush)
+    warm = int(max(3, min(400, 200.0 / max(statistics.median(per), 1e-3))))
+    timed_steps(warm, phases, stream, flush)
     assert moe.moe_read_device_status(b.ws) == 0
     steps = int(max(20, min(200, target_ms / max(statistics.median(per), 1e-3))))
     with ClockSampler(uuid) as clk:
@@ -439,7 +446,7 @@ def measure_config(moe, W, w, dev, stream, peaks, sms, uuid, target_ms=400.0):
     rec = {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.d_ff,
            "act": w.act, "dtype": w.dtype, "score": w.score, "n_shared": w.n_shared,
            "capacity_factor": w.capacity_factor, "kept_rows": n_kept,
-           "dropped_frac": 1.0 - n_kept / (w.T * w.k), "steps": steps, "warmup": 3,
+           "dropped_frac": 1.0 - n_kept / (w.T * w.k), "steps": steps, "warmup": 3 + warm,
            "ms_per_step": ms, "value": w.T / (ms * 1e-3), "unit": UNIT,
            "l2": "flushed before every step (512 MiB write, outside the step's events)",
            "kernels": kernel_report(w, work, phase, peaks, sms), "clocks": clk.summary(),

@@ -18,10 +18,10 @@
 // products, forms the gates and dL in fp32 (fast divisions: a few ulp, well
 // inside the gradient's tolerance), writes the token's dense dL row,
 // and, when asked, dx[t] from the nonzero dL entries (fp32 accumulation, one
-// rounding).  route_bwd_weight_kernel: one CTA per (expert, column chunk)
-// walks the tokens in order and accumulates dL[t,e] x[t] over the nonzero
-// dL entries (a deterministic order), rounding dW once; the chunk-0 CTA also
-// sums d_logit_bias.
+// rounding).  route_bwd_weight_kernel: one CTA per (expert, 32 column
+// vectors), eight warps over interleaved tokens, accumulates dL[t,e] x[t] over
+// the nonzero dL entries and adds the warps' sums in a fixed order
+// (deterministic), rounding dW once; the chunk-0 CTA also sums d_logit_bias.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -166,14 +166,20 @@ __global__ void __launch_bounds__(256) route_bwd_token_kernel(RouteBwdArgs a) {
     }
 }
 
-// dW[e, cols] = sum over t of dL[t,e] x[t, cols], tokens in order; one 16-byte
-// vector of columns per thread.
+// dW[e, cols] = sum over t of dL[t,e] x[t, cols].  One CTA per (expert, 32
+// column vectors); its 8 warps take every 8th token (warp w: t = w, w+8, ...),
+// each lane one 16-byte column vector, and the 8 partial sums are added in warp
+// order through shared memory: a fixed order, so the result is deterministic.
+constexpr int kWGroups = 8;
 template <typename T>
 __global__ void __launch_bounds__(256) route_bwd_weight_kernel(RouteBwdArgs a) {
     constexpr int V = Elem<T>::kPerVec;
+    __shared__ float red[kWGroups][32][V + 1];
+    __shared__ float bias_red[kWGroups];
     pdl_wait();  // the token kernel's dL rows
     const int e = blockIdx.x;
-    const int c = blockIdx.y * blockDim.x + threadIdx.x;  // vector index
+    const int gi = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.y * 32 + lane;  // column vector
     const int nvec = a.d / V;
     const bool has_col = c < nvec;
     const T* x = static_cast<const T*>(a.x);
@@ -181,7 +187,7 @@ __global__ void __launch_bounds__(256) route_bwd_weight_kernel(RouteBwdArgs a) {
 #pragma unroll
     for (int q = 0; q < V; ++q) acc[q] = 0.f;
     float bias_acc = 0.f;
-    for (int64_t t = 0; t < a.T; ++t) {
+    for (int64_t t = gi; t < a.T; t += kWGroups) {
         const float v = a.d_logits[t * a.E + e];
         bias_acc += v;
         if (v == 0.f || !has_col) continue;
@@ -190,9 +196,24 @@ __global__ void __launch_bounds__(256) route_bwd_weight_kernel(RouteBwdArgs a) {
 #pragma unroll
         for (int q = 0; q < V; ++q) acc[q] = fmaf(v, f[q], acc[q]);
     }
+#pragma unroll
+    for (int q = 0; q < V; ++q) red[gi][lane][q] = acc[q];
+    if (lane == 0) bias_red[gi] = bias_acc;
+    __syncthreads();
+    if (gi != 0) return;
+    float sum[V];
+#pragma unroll
+    for (int q = 0; q < V; ++q) {
+        sum[q] = 0.f;
+        for (int g = 0; g < kWGroups; ++g) sum[q] += red[g][lane][q];
+    }
     if (a.d_w && has_col)
-        st_v4(static_cast<T*>(a.d_w) + (int64_t)e * a.d + (int64_t)c * V, Elem<T>::pack(acc));
-    if (a.d_logit_bias && blockIdx.y == 0 && threadIdx.x == 0) a.d_logit_bias[e] = bias_acc;
+        st_v4(static_cast<T*>(a.d_w) + (int64_t)e * a.d + (int64_t)c * V, Elem<T>::pack(sum));
+    if (a.d_logit_bias && blockIdx.y == 0 && lane == 0) {
+        float b = 0.f;
+        for (int g = 0; g < kWGroups; ++g) b += bias_red[g];
+        a.d_logit_bias[e] = b;
+    }
 }
 
 template <typename T>
@@ -203,7 +224,7 @@ cudaError_t launch_typed(const RouteBwdArgs& a, cudaStream_t s) {
     if (e != cudaSuccess || (!a.d_w && !a.d_logit_bias)) return e;
     constexpr int V = Elem<T>::kPerVec;
     const int nvec = a.d / V;
-    const dim3 grid((unsigned)a.E, (unsigned)((nvec + 255) / 256));
+    const dim3 grid((unsigned)a.E, (unsigned)((nvec + 31) / 32));
     return launch_pdl(route_bwd_weight_kernel<T>, grid, 256, 0, s, a);
 }
 
