@@ -403,16 +403,25 @@ def kernel_report(w, work, phase, peaks, sms):
 
 
 class L2Flush:
-    """Writes a 512 MiB buffer (over 4x the 126 MB L2) before each timed step."""
+    """Before each timed step: writes a 512 MiB buffer (over 4x the 126 MB L2),
+    then reads a second 256 MiB buffer, so that the step finds none of its
+    inputs in L2 and no dirty line of the flush left to write back (a write-only
+    flush leaves up to ~126 MB of dirty lines whose write-back the step's first
+    kernel would pay for)."""
+
+    DESC = ("flushed before every step: 512 MiB written, then 256 MiB of a second buffer read "
+            "(no dirty flush lines left); outside the step's events")
 
     def __init__(self, dev):
         import torch
         self.buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.rbuf = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
         self.v = 0
 
     def __call__(self):
         self.v ^= 1
         self.buf.fill_(self.v)
+        self.rbuf.sum()
 
 
 def measure_config(moe, W, w, dev, stream, peaks, sms, uuid, target_ms=400.0):
@@ -437,8 +446,10 @@ def measure_config(moe, W, w, dev, stream, peaks, sms, uuid, target_ms=400.0):
     timed_steps(warm, phases, stream, flush)
     assert moe.moe_read_device_status(b.ws) == 0
     steps = int(max(20, min(200, target_ms / max(statistics.median(per), 1e-3))))
+    n0 = moe.moe_launch_count()
     with ClockSampler(uuid) as clk:
         _, per, phase = timed_steps(steps, phases, stream, flush)
+    launches = moe.moe_launch_count() - n0
     assert moe.moe_read_device_status(b.ws) == 0
     n_kept = int(b.expert_offsets[-1].item())
     ms = statistics.mean(per)
@@ -448,9 +459,9 @@ def measure_config(moe, W, w, dev, stream, peaks, sms, uuid, target_ms=400.0):
            "capacity_factor": w.capacity_factor, "kept_rows": n_kept,
            "dropped_frac": 1.0 - n_kept / (w.T * w.k), "steps": steps, "warmup": 3 + warm,
            "ms_per_step": ms, "value": w.T / (ms * 1e-3), "unit": UNIT,
-           "l2": "flushed before every step (512 MiB write, outside the step's events)",
+           "l2": L2Flush.DESC,
            "kernels": kernel_report(w, work, phase, peaks, sms), "clocks": clk.summary(),
-           "gpu_launches": (5 + (0 if w.act == "identity" else 2 * (1 + w.n_shared))) * steps}
+           "gpu_launches": launches, "launches_per_step": launches / steps}
     del inp, b, phases, flush
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -476,21 +487,28 @@ def time_route_backward(args, w, cfg, b, inp, stream):
     dw = torch.empty_like(inp["w_router"])
     dlb = torch.empty(w.E, dtype=torch.float32, device=b.xp.device)
 
-    def call():
+    def call(weights=True):
         moe.moe_route_backward(cfg, inp["x"], inp["w_router"], inp.get("logit_bias"), b.topk_idx,
-                               d_gate, d_logits, dx, dw, dlb)
+                               d_gate, d_logits, dx, dw if weights else None,
+                               dlb if weights else None)
 
-    for _ in range(max(args.warmup, 1)):
-        call()
-    torch.cuda.synchronize()
-    n = max(args.steps // 4, 3)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(n):
-        call()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    return {"ms": e0.elapsed_time(e1) / n, "calls": n}
+    def timed(weights):
+        for _ in range(max(args.warmup, 1)):
+            call(weights)
+        torch.cuda.synchronize()
+        n = max(args.steps // 4, 3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            call(weights)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n, n
+
+    ms, n = timed(True)
+    # without weight and bias gradients only the per-token kernel (dL, dx) runs
+    ms_tok, _ = timed(False)
+    return {"ms": ms, "calls": n, "token_kernel_ms": ms_tok, "weight_kernel_ms": ms - ms_tok}
 
 
 def run_ours(args, w):
@@ -518,8 +536,6 @@ def run_ours(args, w):
     x = inp["x"]
     stream = torch.cuda.current_stream()
     ident = w.act == "identity"
-    # route 1, dispatch 3 (count, scan, place), combine 1, FFN 2 per expert set
-    per_step_launches = 5 + (0 if ident else 2 * (1 + w.n_shared))
 
     def barrier():
         if world > 1:
@@ -546,8 +562,11 @@ def run_ours(args, w):
     # so the per-kernel times come from this same pass and add up to the step.
     b = layer.buf
     phases = _phase_calls(moe, cfg, w, inp, b, x)
+    # the library counts its own kernel launches: the timed region's are the difference
+    n0 = moe.moe_launch_count()
     with ClockSampler(uuid if rank == 0 else None) as clk:
         total_ms, per_step, phase = timed_steps(args.steps, phases, stream, None, barrier)
+    launches = moe.moe_launch_count() - n0
     ms = max_over_ranks(total_ms) / args.steps
     clocks = clk.summary() if rank == 0 else None
     value = world * w.T / (ms / 1e3)
@@ -678,7 +697,8 @@ def run_ours(args, w):
                 "via": "moe_layer_forward_host (host x in, host y out; copies enqueued by the library)",
                 "overlap": "two layer instances alternate on two streams: one step's copies "
                            "overlap the other's kernels"},
-        "gpu_launches": per_step_launches * args.steps,
+        "gpu_launches": launches,
+        "launches_per_step": launches / args.steps,
         "roofline": roofline,
         "kernels": kernels,
         "phase_sum_ms": phase_sum,

@@ -117,6 +117,8 @@ def _load():
     lib.moe_read_device_status.restype = i32
     lib.moe_build_checked.argtypes = []
     lib.moe_build_checked.restype = i32
+    lib.moe_launch_count.argtypes = []
+    lib.moe_launch_count.restype = ctypes.c_uint64
     _lib = lib
     return lib
 
@@ -308,6 +310,11 @@ def moe_update_sel_bias(cfg, expert_counts, sel_bias, gamma, stream=None):
 def moe_build_checked() -> bool:
     """True if the loaded library is the range-checked debugging build."""
     return bool(_load().moe_build_checked())
+
+
+def moe_launch_count() -> int:
+    """Kernel launches the library has enqueued since it loaded (all threads)."""
+    return int(_load().moe_launch_count())
 
 
 def moe_read_device_status(ws, stream=None) -> int:

@@ -4,10 +4,17 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
+
+// Kernel launches enqueued since the library loaded (all threads and devices).
+std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -695,5 +702,7 @@ moe_status moe_read_device_status(const void* ws, uint32_t* out, moe_stream_t st
 }
 
 int moe_build_checked(void) { return kChecked ? 1 : 0; }
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

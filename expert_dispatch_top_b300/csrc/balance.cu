@@ -29,7 +29,7 @@ __global__ void update_sel_bias_kernel(const int32_t* counts, float* bias, int E
 cudaError_t launch_update_sel_bias(const int32_t* counts, float* bias, int E, int64_t T, int k,
                                    float gamma, cudaStream_t s) {
     update_sel_bias_kernel<<<(E + 255) / 256, 256, 0, s>>>(counts, bias, E, T * (int64_t)k, gamma);
-    return cudaGetLastError();
+    return noted_launch();
 }
 
 }  // namespace moe

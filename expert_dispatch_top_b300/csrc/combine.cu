@@ -232,13 +232,13 @@ cudaError_t launch_combine_backward(const CombineBwdArgs& a, cudaStream_t s) {
         launch_combine_bwd_typed<float>(a, (unsigned)blocks, s);
     else
         launch_combine_bwd_typed<__nv_bfloat16>(a, (unsigned)blocks, s);
-    return cudaGetLastError();
+    return noted_launch();
 }
 
 cudaError_t launch_sanitize_offsets(const int32_t* in, int32_t* out, int G, int64_t rows_cap,
                                     uint32_t* status, cudaStream_t s) {
     sanitize_offsets_kernel<<<1, 32, 0, s>>>(in, out, G, rows_cap, status);
-    return cudaGetLastError();
+    return noted_launch();
 }
 
 cudaError_t take_checked_status(uint32_t* out, cudaStream_t s) {

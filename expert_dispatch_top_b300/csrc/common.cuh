@@ -133,6 +133,15 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Counts one kernel launch enqueued by this library (moe_launch_count).
+void note_launch();
+// Counts the launch just made with <<<...>>> if it was accepted; returns its error.
+inline cudaError_t noted_launch() {
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) note_launch();
+    return e;
+}
+
 // Launch with programmatic stream serialization (see pdl_wait).
 template <typename K, typename... Args>
 cudaError_t launch_pdl(K kernel, dim3 grid, unsigned block, size_t smem, cudaStream_t s,
@@ -147,7 +156,9 @@ cudaError_t launch_pdl(K kernel, dim3 grid, unsigned block, size_t smem, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e == cudaSuccess) note_launch();
+    return e;
 }
 
 // Key order of the router's selection: larger key first, ties to the lower index.

@@ -246,7 +246,7 @@ template <typename T>
 cudaError_t transpose_batched(const void* in, void* out, int B, int R, int C, cudaStream_t s) {
     dim3 grid((C + 31) / 32, (R + 31) / 32, B);
     transpose_kernel<T><<<grid, 256, 0, s>>>(static_cast<const T*>(in), static_cast<T*>(out), R, C);
-    return cudaGetLastError();
+    return noted_launch();
 }
 
 }  // namespace
@@ -354,7 +354,7 @@ cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
             static_cast<const __nv_bfloat16*>(pre), static_cast<const __nv_bfloat16*>(dh),
             static_cast<__nv_bfloat16*>(d_pre), nullptr, a.offsets, a.E, a.f, gated, a.rows_cap);
     }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = noted_launch()) != cudaSuccess) return e;
     if ((e = gemm(d_pre, tc ? a.w_up : w_upT, a.d_xp, a.d, up, tc)) != cudaSuccess) return e;  // 4
     if (!wg) return cudaSuccess;
     // 5: weight gradients
@@ -364,20 +364,22 @@ cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
             wgrad_simt_kernel<<<grid, 256, 0, s>>>(static_cast<const float*>(a.d_yp),
                                                    static_cast<const float*>(h),
                                                    static_cast<float*>(a.d_w_down), a.offsets, a.d, a.f);
+            if ((e = noted_launch()) != cudaSuccess) return e;
         }
         if (a.d_w_up) {
             dim3 grid((a.d + 63) / 64, (up + 63) / 64, a.E);
             wgrad_simt_kernel<<<grid, 256, 0, s>>>(static_cast<const float*>(d_pre),
                                                    static_cast<const float*>(a.xp),
                                                    static_cast<float*>(a.d_w_up), a.offsets, up, a.d);
+            if ((e = noted_launch()) != cudaSuccess) return e;
         }
-        return cudaGetLastError();
+        return cudaSuccess;
     }
     pad_rows_kernel<<<sms * 4, 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(a.xp), static_cast<__nv_bfloat16*>(xp_pad),
         static_cast<const __nv_bfloat16*>(a.d_yp), static_cast<__nv_bfloat16*>(dyp_pad), a.offsets,
         a.E, a.d);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = noted_launch()) != cudaSuccess) return e;
     // dW[e] = A_pad[K_e, :]^T . B_pad[K_e, :] over expert e's padded rows
     auto kgemm = [&](const void* A, const void* B, void* out, int M, int N) {
         GemmArgs g;

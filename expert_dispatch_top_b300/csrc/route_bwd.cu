@@ -18,10 +18,9 @@
 // products, forms the gates and dL in fp32 (fast divisions: a few ulp, well
 // inside the gradient's tolerance), writes the token's dense dL row,
 // and, when asked, dx[t] from the nonzero dL entries (fp32 accumulation, one
-// rounding).  route_bwd_weight_kernel: one CTA per (expert, 32 column
-// vectors), eight warps over interleaved tokens, accumulates dL[t,e] x[t] over
-// the nonzero dL entries and adds the warps' sums in a fixed order
-// (deterministic), rounding dW once; the chunk-0 CTA also sums d_logit_bias.
+// rounding).  route_bwd_weight_kernel (below) forms dW and d_logit_bias from
+// the dL rows and x with sums in a fixed order (deterministic), rounding dW
+// once.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -73,6 +72,19 @@ __global__ void __launch_bounds__(256) route_bwd_token_kernel(RouteBwdArgs a) {
         if (lane == j) L_l = L;
     }
     const bool mine = lane < a.k;
+    // sum over the chosen slots i of g_i (dg_l - dg_i).  With gates that sum to 1
+    // this equals dg_l - sum_i g_i dg_i, without that difference's cancellation
+    // when one gate is close to 1 (the other slots' terms are then tiny and the
+    // fp32 difference would lose most of their digits).
+    auto centred = [&](float g) {
+        float acc = 0.f;
+        for (int i = 0; i < a.k; ++i) {
+            const float gi = __shfl_sync(0xffffffffu, g, i);
+            const float dgi = __shfl_sync(0xffffffffu, dg_l, i);
+            acc = fmaf(gi, dg_l - dgi, acc);
+        }
+        return acc;
+    };
     if (!full) {
         float v = 0.f;  // dL of this lane's slot
         if (a.score == MOE_SCORE_SOFTMAX) {
@@ -83,10 +95,7 @@ __global__ void __launch_bounds__(256) route_bwd_token_kernel(RouteBwdArgs a) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
             const float g = __fdividef(ex, z);
-            float dot = g * dg_l;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-            v = g * (dg_l - dot);
+            v = g * centred(g);
         } else {
             const float s = mine ? __fdividef(1.f, 1.f + expf(-L_l)) : 0.f;
             float ds = dg_l;
@@ -95,10 +104,7 @@ __global__ void __launch_bounds__(256) route_bwd_token_kernel(RouteBwdArgs a) {
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
                 const float g = __fdividef(s, sum);
-                float dot = g * dg_l;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-                ds = __fdividef(dg_l - dot, sum);
+                ds = __fdividef(centred(g), sum);
             }
             v = ds * s * (1.f - s);
         }
@@ -123,17 +129,35 @@ __global__ void __launch_bounds__(256) route_bwd_token_kernel(RouteBwdArgs a) {
         float dot = pj * dg_l;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        // A chosen slot j: dL = p_j (dg_j - dot) = p_j (dg_j (1 - p_j) - sum_(i!=j) p_i dg_i),
+        // with 1 - p_j summed over the other experts rather than subtracted from 1
+        // (stable when p_j is close to 1).
+        float zx = 0.f;  // slot lane < k: the exp sum over every expert but its own
+        for (int j = 0; j < a.k; ++j) {
+            const int ej = __shfl_sync(0xffffffffu, e_l, j);
+            float part = 0.f;
+            for (int e = lane; e < a.E; e += 32)
+                if (e != ej) part += expf(dL[e] - m);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (lane == j) zx = part;
+        }
+        float other = 0.f;
+        for (int i = 0; i < a.k; ++i) {
+            const float pi = __shfl_sync(0xffffffffu, pj, i);
+            const float dgi = __shfl_sync(0xffffffffu, dg_l, i);
+            if (i != lane) other = fmaf(pi, dgi, other);
+        }
+        const float dl_slot = pj * (dg_l * __fdividef(zx, z) - other);
         __syncwarp();
         // every lane runs the same number of rounds (the shuffles need all 32)
         for (int e0 = 0; e0 < a.E; e0 += 32) {
             const int e = e0 + lane;
-            float dge = 0.f;
-            for (int j = 0; j < a.k; ++j) {
-                const int ej = __shfl_sync(0xffffffffu, e_l, j);
-                const float dgj = __shfl_sync(0xffffffffu, dg_l, j);
-                if (ej == e) dge = dgj;
-            }
-            if (e < a.E) dL[e] = __fdividef(expf(dL[e] - m), z) * (dge - dot);
+            int js = -1;
+            for (int j = 0; j < a.k; ++j)
+                if (__shfl_sync(0xffffffffu, e_l, j) == e) js = j;
+            const float vs = __shfl_sync(0xffffffffu, dl_slot, js < 0 ? 0 : js);
+            if (e < a.E) dL[e] = js >= 0 ? vs : -__fdividef(expf(dL[e] - m), z) * dot;
         }
     }
     if (!a.dx) return;
@@ -166,66 +190,207 @@ __global__ void __launch_bounds__(256) route_bwd_token_kernel(RouteBwdArgs a) {
     }
 }
 
-// dW[e, cols] = sum over t of dL[t,e] x[t, cols].  One CTA per (expert, 32
-// column vectors); its 8 warps take every 8th token (warp w: t = w, w+8, ...),
-// each lane one 16-byte column vector, and the 8 partial sums are added in warp
-// order through shared memory: a fixed order, so the result is deterministic.
-constexpr int kWGroups = 8;
+// dW[e, cols] = sum over t of dL[t,e] x[t, cols], and d_logit_bias[e] = sum
+// over t of dL[t,e].  A CTA owns 8 experts and 32 column vectors (256 bf16 or
+// 128 fp32 columns) for a contiguous range of tokens; its 16 warps take
+// interleaved groups of 32 tokens.  Per group, lane l reads token l's 8 dL
+// entries (32 contiguous bytes), then the warp walks the group's tokens with
+// any nonzero entry four at a time: each lane loads its column vector of the
+// four x rows, and for every expert whose dL is nonzero (a warp-uniform test)
+// adds dL * x into its accumulators -- x is read once per token for all 8
+// experts.  The token range is split over the S CTAs of a thread-block
+// cluster when there are too few (expert block, column block) pairs to fill
+// the GPU; the partial sums are then added through distributed shared memory.
+// Every sum is taken in a fixed order (warps in index order, cluster ranks in
+// rank order, lanes by a fixed shuffle tree), so the result is deterministic.
+constexpr int kWExperts = 8;
+constexpr int kWWarps = 16;
+constexpr int kWMaxSplit = 8;
+constexpr int kWBatch = 4;  // x rows in flight per lane
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+// Shared-memory address of the same variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+    uint32_t out;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(out)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
+    return out;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 template <typename T>
-__global__ void __launch_bounds__(256) route_bwd_weight_kernel(RouteBwdArgs a) {
+__global__ void __launch_bounds__(kWWarps * 32, 1) route_bwd_weight_kernel(RouteBwdArgs a, int S) {
     constexpr int V = Elem<T>::kPerVec;
-    __shared__ float red[kWGroups][32][V + 1];
-    __shared__ float bias_red[kWGroups];
+    constexpr int COLS = 32 * V;
+    __shared__ float part[kWExperts][COLS];  // this CTA's sums (warps added in order)
+    __shared__ float bpart[kWExperts];       // this CTA's d_logit_bias sums
     pdl_wait();  // the token kernel's dL rows
-    const int e = blockIdx.x;
-    const int gi = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = blockIdx.y * 32 + lane;  // column vector
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e0 = blockIdx.x * kWExperts;
+    const int ne = a.E - e0 < kWExperts ? a.E - e0 : kWExperts;
     const int nvec = a.d / V;
+    const int c = blockIdx.y * 32 + lane;  // this lane's column vector
     const bool has_col = c < nvec;
     const T* x = static_cast<const T*>(a.x);
-    float acc[V];
+    // this CTA's tokens: split z of S
+    const int z = S > 1 ? (int)cluster_rank() : 0;
+    const int64_t groups = (a.T + 31) / 32;
+    const int64_t g_lo = groups * z / S, g_hi = groups * (z + 1) / S;
+    const bool vec_dl = (a.E % 4) == 0 && (reinterpret_cast<uintptr_t>(a.d_logits) & 15) == 0;
+    float acc[kWExperts][V];
 #pragma unroll
-    for (int q = 0; q < V; ++q) acc[q] = 0.f;
-    float bias_acc = 0.f;
-    for (int64_t t = gi; t < a.T; t += kWGroups) {
-        const float v = a.d_logits[t * a.E + e];
-        bias_acc += v;
-        if (v == 0.f || !has_col) continue;
-        float f[V];
-        Elem<T>::unpack(ld_nc_v4(x + t * a.d + (int64_t)c * V), f);
+    for (int j = 0; j < kWExperts; ++j)
 #pragma unroll
-        for (int q = 0; q < V; ++q) acc[q] = fmaf(v, f[q], acc[q]);
+        for (int q = 0; q < V; ++q) acc[j][q] = 0.f;
+    float bsum[kWExperts];
+#pragma unroll
+    for (int j = 0; j < kWExperts; ++j) bsum[j] = 0.f;
+    for (int64_t g = g_lo + warp; g < g_hi; g += kWWarps) {
+        const int64_t t = g * 32 + lane;
+        float dv[kWExperts];
+#pragma unroll
+        for (int j = 0; j < kWExperts; ++j) dv[j] = 0.f;
+        if (t < a.T) {
+            const float* row = a.d_logits + t * a.E + e0;
+            if (vec_dl && ne == kWExperts) {
+                const float4 u0 = *reinterpret_cast<const float4*>(row);
+                const float4 u1 = *reinterpret_cast<const float4*>(row + 4);
+                dv[0] = u0.x; dv[1] = u0.y; dv[2] = u0.z; dv[3] = u0.w;
+                dv[4] = u1.x; dv[5] = u1.y; dv[6] = u1.z; dv[7] = u1.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < kWExperts; ++j)
+                    if (j < ne) dv[j] = row[j];
+            }
+        }
+        bool nz = false;
+#pragma unroll
+        for (int j = 0; j < kWExperts; ++j) {
+            bsum[j] += dv[j];
+            nz |= dv[j] != 0.f;
+        }
+        uint32_t mask = __ballot_sync(0xffffffffu, nz);
+        while (mask) {
+            // up to kWBatch tokens of the group: their x vectors in flight together
+            int src[kWBatch];
+            uint4 raw[kWBatch];
+#pragma unroll
+            for (int u = 0; u < kWBatch; ++u) {
+                src[u] = mask ? __ffs(mask) - 1 : -1;
+                if (mask) mask &= mask - 1;
+                if (src[u] >= 0 && has_col)
+                    raw[u] = ld_nc_v4(x + (g * 32 + src[u]) * a.d + (int64_t)c * V);
+            }
+#pragma unroll
+            for (int u = 0; u < kWBatch; ++u) {
+                if (src[u] < 0) break;  // warp-uniform
+                float f[V];
+                if (has_col) Elem<T>::unpack(raw[u], f);
+#pragma unroll
+                for (int j = 0; j < kWExperts; ++j) {
+                    const float v = __shfl_sync(0xffffffffu, dv[j], src[u]);
+                    if (v != 0.f && has_col) {
+#pragma unroll
+                        for (int q = 0; q < V; ++q) acc[j][q] = fmaf(v, f[q], acc[j][q]);
+                    }
+                }
+            }
+        }
     }
+    // d_logit_bias: lanes by a fixed butterfly, then warps in order below
 #pragma unroll
-    for (int q = 0; q < V; ++q) red[gi][lane][q] = acc[q];
-    if (lane == 0) bias_red[gi] = bias_acc;
-    __syncthreads();
-    if (gi != 0) return;
-    float sum[V];
+    for (int j = 0; j < kWExperts; ++j)
 #pragma unroll
-    for (int q = 0; q < V; ++q) {
-        sum[q] = 0.f;
-        for (int g = 0; g < kWGroups; ++g) sum[q] += red[g][lane][q];
+        for (int o = 16; o > 0; o >>= 1) bsum[j] += __shfl_xor_sync(0xffffffffu, bsum[j], o);
+    // warps add their sums into part[] one after another (fixed order)
+    for (int w = 0; w < kWWarps; ++w) {
+        if (warp == w) {
+#pragma unroll
+            for (int j = 0; j < kWExperts; ++j) {
+#pragma unroll
+                for (int q = 0; q < V; ++q) {
+                    float* dst = &part[j][lane * V + q];
+                    *dst = (w == 0 ? 0.f : *dst) + acc[j][q];
+                }
+                if (lane == 0) bpart[j] = (w == 0 ? 0.f : bpart[j]) + bsum[j];
+            }
+        }
+        __syncthreads();
     }
-    if (a.d_w && has_col)
-        st_v4(static_cast<T*>(a.d_w) + (int64_t)e * a.d + (int64_t)c * V, Elem<T>::pack(sum));
-    if (a.d_logit_bias && blockIdx.y == 0 && lane == 0) {
+    if (S > 1) cluster_sync();  // every rank's part[] is complete
+    // CTA rank z finalises its share of the 8 x COLS outputs, adding the ranks in order
+    const int n_out = kWExperts * COLS;
+    for (int i = z * (n_out / S) + (int)threadIdx.x; i < (z + 1) * (n_out / S); i += kWWarps * 32) {
+        const int j = i / COLS, col = i - j * COLS;
+        float sum = part[j][col];
+        if (S > 1) {
+            sum = 0.f;
+            for (int r = 0; r < S; ++r) sum += ld_cluster_f32(cluster_addr(&part[j][col], (uint32_t)r));
+        }
+        const int cc = blockIdx.y * COLS + col;  // element column
+        if (a.d_w && j < ne && cc < a.d) {
+            T* out = static_cast<T*>(a.d_w) + (int64_t)(e0 + j) * a.d + cc;
+            *out = Elem<T>::from_f(sum);
+        }
+    }
+    if (a.d_logit_bias && blockIdx.y == 0 && z == 0 && threadIdx.x < kWExperts &&
+        (int)threadIdx.x < ne) {
         float b = 0.f;
-        for (int g = 0; g < kWGroups; ++g) b += bias_red[g];
-        a.d_logit_bias[e] = b;
+        for (int r = 0; r < S; ++r)
+            b += S > 1 ? ld_cluster_f32(cluster_addr(&bpart[threadIdx.x], (uint32_t)r))
+                       : bpart[threadIdx.x];
+        a.d_logit_bias[e0 + threadIdx.x] = b;
     }
+    if (S > 1) cluster_sync();  // no CTA leaves while another reads its shared memory
 }
 
 template <typename T>
 cudaError_t launch_typed(const RouteBwdArgs& a, cudaStream_t s) {
     const unsigned blocks = (unsigned)((a.T + 7) / 8);  // 8 warps (tokens) per block
     route_bwd_token_kernel<T><<<blocks, 256, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = noted_launch();
     if (e != cudaSuccess || (!a.d_w && !a.d_logit_bias)) return e;
     constexpr int V = Elem<T>::kPerVec;
     const int nvec = a.d / V;
-    const dim3 grid((unsigned)a.E, (unsigned)((nvec + 31) / 32));
-    return launch_pdl(route_bwd_weight_kernel<T>, grid, 256, 0, s, a);
+    const unsigned eb = (unsigned)((a.E + kWExperts - 1) / kWExperts);
+    const unsigned cb = (unsigned)((nvec + 31) / 32);
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // token splits (a power of two <= 8) until there is a CTA per SM (one fits
+    // an SM), with at least 64 token groups per split
+    int S = 1;
+    while (S < kWMaxSplit && (int64_t)eb * cb * S < (int64_t)sms && (a.T + 31) / 32 >= 64 * 2 * S)
+        S *= 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(eb, cb, (unsigned)S);
+    cfg.blockDim = dim3(kWWarps * 32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = (unsigned)S;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, route_bwd_weight_kernel<T>, a, S);
+    if (e == cudaSuccess) note_launch();
+    return e;
 }
 
 }  // namespace

@@ -24,15 +24,20 @@
 //              (ties to the lower expert index), then computes the gates and
 //              writes topk_idx / topk_gate.
 // Sigmoid routers: the exact score fp32(1/(1+exp(-L))) needs double
-// precision, which is slow on this part.  The epilogue first ranks all
-// experts by an approximation a = 1/2 + tanh(L/2)/2 (+ bias), using the
-// hardware tanh whose documented maximum relative error is 2^-11 (so
-// |a - key| < 2.5e-4), finds the k-th largest approximation A_k, and
-// evaluates the exact score only for experts with a >= A_k - 2*delta, with
-// delta = 2^-8 (16x the bound).  Any expert of the exact top-k has key >=
-// (k-th exact key) >= A_k - delta and hence a >= A_k - 2*delta, so the exact
-// top-k over these candidates is the exact top-k over all experts, ties
-// included.
+// precision, which is slow on this part.  The epilogue ranks all experts by
+// an approximation a of the key (score + selection bias) with a known bound
+// |a - key| <= eps, finds the k-th largest approximation A_k, and evaluates
+// the exact score only for experts with a >= A_k - 2*delta, delta > eps.  The
+// k experts with the largest a have keys >= A_k - eps, so the k-th exact key
+// is >= A_k - eps; any expert of the exact top-k therefore has key >= A_k -
+// eps and a >= A_k - 2*eps > A_k - 2*delta.  The exact top-k over these
+// candidates is the exact top-k over all experts, ties included.  The main
+// pass uses a fast fp32 sigmoid (delta = 2^-14, over 100x its bound, plus
+// 2^-21 |A_k| for the rounding of large keys) and keeps the k + 4 best
+// experts with their logits, so the candidates are almost always in that list;
+// the rank pass of rank-limited routing uses 1/2 + tanh(L/2)/2 with the
+// hardware tanh (documented relative error 2^-11, so eps < 2.5e-4) and
+// delta = 2^-8.
 //
 // Epilogue layout: per 32-logit chunk, one compact unrolled pass stashes the
 // logits in shared memory (one padded row per thread) and builds a 32-bit
@@ -85,6 +90,9 @@ struct RtParams {
     // gates without renormalisation, its partial softmax sum to `zpart`), and
     // route_merge_kernel forms the final top-k and gates.
     int split, Eh, units;
+    // 1: epilogue group 0 first runs its code once on the unused TMEM buffer,
+    // storing nothing, while the K loop streams x (see the epilogue)
+    int warm;
     RoutePartial* part;
     float2* zpart;
 };
@@ -100,41 +108,62 @@ __device__ __forceinline__ float tanh_approx(float x) {
 __device__ __forceinline__ float sigmoid_approx(float L) {
     return fmaf(0.5f, tanh_approx(0.5f * L), 0.5f);
 }
+// A fast fp32 sigmoid for ranking.  With e = exp(-L), the documented bounds of
+// the intrinsics (__expf: 2 + floor(|1.173 L|) ulp; the fp32 add: 1/2 ulp;
+// __fdividef: 2 ulp for divisors up to 2^126, and 0 beyond, where the true
+// value is below 2^-126) give |f - s| <= s (1 - s) (2 + 1.2 |L|) 2^-23 + 3 s 2^-23,
+// at most ~4e-7 over all L (s (1 - s) decays like e^-|L|).  kFastDelta = 2^-14
+// is over 100 times that.
+__device__ __forceinline__ float sigmoid_fast(float L) { return __fdividef(1.f, 1.f + __expf(-L)); }
+constexpr float kFastDelta = 1.0f / 16384.0f;
 
 // Sorted top-k (k <= 8) in registers: key, a payload value and the index.
 // The list always has 8 entries, in descending key order: 8 - k sentinels
 // (key +inf, never displaced) followed by the k best so far, so the k-th best
 // is always entry 7.  A fixed position keeps the list in registers (reading
 // entry k - 1 for a runtime k would make it an indexed array in local memory).
-struct TopK {
-    float key[8], val[8];
-    int idx[8];
-    __device__ __forceinline__ void init(int k) {
+template <int N>
+struct TopKN {
+    float key[N], val[N];
+    int idx[N];
+    // n (<= N) real entries, behind N - n sentinels
+    __device__ __forceinline__ void init(int n) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const bool sentinel = j < 8 - k;
+        for (int j = 0; j < N; ++j) {
+            const bool sentinel = j < N - n;
             key[j] = sentinel ? INFINITY : -INFINITY;
             val[j] = 0.f;
             idx[j] = sentinel ? -1 : 0x7fffffff;
         }
     }
-    __device__ __forceinline__ float kth_key() const { return key[7]; }
+    __device__ __forceinline__ float last_key() const { return key[N - 1]; }
+    // Sorted insertion.  The new entry's place is the number of entries that
+    // rank before it (the list is sorted, so they form a prefix); every slot's
+    // new content then depends only on the old list and that place, so the
+    // eight compares and the shifts are independent instructions rather than
+    // one chain of compare-and-swap steps.
     __device__ __forceinline__ void insert(float kv, float v, int e) {
-        if (!key_better(kv, e, key[7], idx[7])) return;
+        if (!key_better(kv, e, key[N - 1], idx[N - 1])) return;
+        int pos = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (key_better(kv, e, key[j], idx[j])) {
-                const float tk = key[j], tv = val[j];
-                const int ti = idx[j];
-                key[j] = kv;
-                val[j] = v;
-                idx[j] = e;
-                kv = tk;
-                v = tv;
-                e = ti;
-            }
+        for (int j = 0; j < N - 1; ++j) pos += key_better(key[j], idx[j], kv, e) ? 1 : 0;
+#pragma unroll
+        for (int j = N - 1; j > 0; --j) {
+            const bool shift = j > pos, here = j == pos;
+            key[j] = shift ? key[j - 1] : (here ? kv : key[j]);
+            val[j] = shift ? val[j - 1] : (here ? v : val[j]);
+            idx[j] = shift ? idx[j - 1] : (here ? e : idx[j]);
+        }
+        if (pos == 0) {
+            key[0] = kv;
+            val[0] = v;
+            idx[0] = e;
         }
     }
+};
+// The router's top-k: 8 - k sentinels, then the k best, the k-th always entry 7.
+struct TopK : TopKN<8> {
+    __device__ __forceinline__ float kth_key() const { return key[7]; }
 };
 
 // The best m of R scores s[0..R) by rounds of selection (ties to the lower
@@ -313,20 +342,32 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
         const bool limited = !SPLIT && p.max_ranks > 0;
         const int per = p.E / p.R;
         const float inv_per = 1.0f / (float)per;  // (e + 1/2) * inv_per truncates to e / per exactly
-        int local = -1;
-        for (int unit = blockIdx.x; unit < p.units; unit += gridDim.x) {
+        // Warm-up: with one tile per CTA and few experts the epilogue is a
+        // short stretch of code that runs once, after the K loop, mostly
+        // waiting for its instructions to arrive.  Group 0 then first runs the
+        // same code on TMEM buffer 1 (allocated, never written by this CTA's
+        // MMAs) while the K loop streams x, with every store, status bit and
+        // barrier arrival suppressed (`dry`), so that the real pass finds its
+        // instructions cached.
+        const bool warm_up = p.warm && egroup == 0;
+        int local = warm_up ? -2 : -1;
+        for (int unit = (int)blockIdx.x - (warm_up ? (int)gridDim.x : 0); unit < p.units;
+             unit += gridDim.x) {
             ++local;
-            if (local % p.epi_groups != egroup) continue;
-            const int acc = local & 1;                       // the MMA alternates buffers per tile
+            const bool dry = local < 0;
+            if (!dry && local % p.epi_groups != egroup) continue;
+            const int acc = dry ? 1 : local & 1;  // the MMA alternates buffers per tile
             const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;  // n-th use of that buffer
-            const bool ok =
-                __all_sync(0xffffffffu, mbar_wait(accf0 + 8 * acc, acc_phase, abort_flag, p.status,
-                                                  MOE_DEV_GEMM_TIMEOUT));
-            if (!ok) break;
+            if (!dry) {
+                const bool ok = __all_sync(0xffffffffu, mbar_wait(accf0 + 8 * acc, acc_phase,
+                                                                  abort_flag, p.status,
+                                                                  MOE_DEV_GEMM_TIMEOUT));
+                if (!ok) break;
+            }
             fence_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256);
             // rows past tile_rows hold whatever the stage held before: computed, never stored
-            const bool row_ok = q * 32 + lane < p.tile_rows;
+            const bool row_ok = !dry && q * 32 + lane < p.tile_rows;
             const int tile = SPLIT ? unit / p.split : unit;
             const int h = SPLIT ? unit - tile * p.split : 0;
             const int e0 = SPLIT ? h * p.Eh : 0;  // this unit's experts: [e0, e_end)
@@ -417,11 +458,21 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                     }
                 }
             } else {
-                TopK approx;
-                approx.init(p.k);
+                // One pass ranks the experts by the fast score (plus the selection
+                // bias) and keeps the k + 4 best with their logits.  The exact
+                // score is then needed only for kept experts within 2 delta of the
+                // k-th fast key: every expert of the exact top-k is that close (see
+                // the proof at the top of this file, with the fast score's bound
+                // and the fp32 rounding of large keys, 2^-21 |key|, in delta).  If
+                // even the (k+4)-th kept key is that close, the list may have
+                // dropped a candidate, and a second pass visits every expert (with
+                // k + 2 kept, that pass ran in a few warps of every large batch and
+                // set the kernel's end).
+                TopKN<12> approx;
+                approx.init(p.k + 4);
                 for (int c = 0; c < nchunks; ++c) {
                     tmem_ld32(tb + (uint32_t)(c * 32), v);
-                    const float thr = approx.kth_key();
+                    const float thr = approx.last_key();
                     uint32_t mask = 0;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -429,36 +480,51 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                         const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
                         stash[i] = L;
                         nonfinite |= (SPLIT || e < e_end) && !(fabsf(L) <= FLT_MAX);
-                        const float a = __fadd_rn(sigmoid_approx(L), sb_s[e & 255]);
+                        const float a = __fadd_rn(sigmoid_fast(L), sb_s[e & 255]);
                         if ((SPLIT || e < e_end) && a > thr && rank_ok(e)) mask |= 1u << i;
                     }
                     while (mask) {
                         const int i = __ffs(mask) - 1;
                         mask &= mask - 1;
                         const int e = e0 + c * 32 + i;
-                        const float a = __fadd_rn(sigmoid_approx(stash[i]), sb_s[e]);
-                        approx.insert(a, 0.f, e);
+                        const float L = stash[i];
+                        approx.insert(__fadd_rn(sigmoid_fast(L), sb_s[e]), L, e);
                     }
                 }
-                const float thresh = approx.kth_key() - 2.f * kApproxDelta;
-                for (int c = 0; c < nchunks; ++c) {
-                    tmem_ld32(tb + (uint32_t)(c * 32), v);
-                    uint32_t mask = 0;
+                const float ak = approx.key[7];  // the k-th fast key
+                const float band = ak - 2.f * (kFastDelta + fabsf(ak) * (1.0f / 2097152.0f));
+                const bool every = approx.key[11] >= band;
+                if (!every) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int e = e0 + c * 32 + i;
-                        const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
-                        stash[i] = L;
-                        const float a = __fadd_rn(sigmoid_approx(L), sb_s[e & 255]);
-                        if ((SPLIT || e < e_end) && a >= thresh && rank_ok(e)) mask |= 1u << i;
+                    for (int j = 0; j < 12; ++j) {
+                        if (approx.idx[j] >= 0 && approx.key[j] >= band) {
+                            const int e = approx.idx[j];
+                            const float s = sigmoid_exact(approx.val[j]);
+                            top.insert(has_sb ? __fadd_rn(s, sb_s[e]) : s, s, e);
+                        }
                     }
-                    while (mask) {
-                        const int i = __ffs(mask) - 1;
-                        mask &= mask - 1;
-                        const int e = e0 + c * 32 + i;
-                        const float s = sigmoid_exact(stash[i]);
-                        const float key = has_sb ? __fadd_rn(s, sb_s[e]) : s;
-                        top.insert(key, s, e);
+                }
+                if (__any_sync(0xffffffffu, every)) {
+                    for (int c = 0; c < nchunks; ++c) {
+                        tmem_ld32(tb + (uint32_t)(c * 32), v);
+                        uint32_t mask = 0;
+                        if (every) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int e = e0 + c * 32 + i;
+                                const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
+                                stash[i] = L;
+                                const float a = __fadd_rn(sigmoid_fast(L), sb_s[e & 255]);
+                                if ((SPLIT || e < e_end) && a >= band && rank_ok(e)) mask |= 1u << i;
+                            }
+                        }
+                        while (mask) {
+                            const int i = __ffs(mask) - 1;
+                            mask &= mask - 1;
+                            const int e = e0 + c * 32 + i;
+                            const float s = sigmoid_exact(stash[i]);
+                            top.insert(has_sb ? __fadd_rn(s, sb_s[e]) : s, s, e);
+                        }
                     }
                 }
             }
@@ -517,7 +583,7 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
             if (nonfinite && row_ok && t < p.T) atomicOr(p.status, MOE_DEV_NONFINITE);
             fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+            if (lane == 0 && !dry) mbar_arrive(acce0 + 8 * acc);
             if (!SPLIT && row_ok && t < p.T) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
@@ -698,6 +764,9 @@ cudaError_t launch_route_tc(const RouteArgs& a, cudaStream_t s) {
     // A second epilogue group overlaps the epilogues of a CTA's tiles.  It pays
     // off once CTAs average two tiles; with fewer, only if its stash leaves the
     // TMA ring at least 4 stages deep (small E: stages are small).
+    // the warm-up pass: one 32-expert chunk and at most one tile per CTA
+    // (A/B, moe_route alone, CUDA events: Mixtral shape ~35 -> ~33 us)
+    p.warm = (p.Np <= 32 && p.split == 1 && p.units <= grid) ? 1 : 0;
     p.epi_groups = (p.max_ranks == 0 && (p.units >= 2 * grid ||
                                          (p.units > grid && stages_for(2) >= 4)))
                        ? 2 : 1;

@@ -430,6 +430,18 @@ moe_status moe_read_device_status(const void* ws, uint32_t* out, moe_stream_t st
  */
 int moe_build_checked(void);
 
+/*
+ * Kernel launches this library has enqueued since it was loaded, over all
+ * threads, streams and devices (each successful launch counts one; a call
+ * that fails its argument checks launches nothing).  The difference of two
+ * readings around a region counts the library's kernels enqueued in it, e.g.
+ * the launches one moe_layer_forward makes for a configuration (route 1, or 2
+ * when a small batch's experts are sliced; dispatch 3; FFN 2 per expert set;
+ * combine 1).  Host-side; no
+ * synchronisation.
+ */
+uint64_t moe_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -236,8 +236,11 @@ def test_layer_forward_rejects_every_argument_error_before_any_launch(dtype, act
            dict(w_router=None), dict(logit_bias=0x1002)]
     if n_shared:
         bad += [dict(shared_up=None), dict(shared_out=0xd0008), dict(shared_h=None)]
+    launches = moe.moe_launch_count()
     for over in bad:
         assert _layer_args(c, **over) == moe.MOE_ERR_INVALID_ARG, over
+    # the library's own launch counter agrees: nothing was enqueued
+    assert moe.moe_launch_count() == launches
     # a selection-only bias with softmax scores is a valid call this library does not run
     if not n_shared:
         assert _layer_args(c, sel_bias=0x1000) == moe.MOE_ERR_UNSUPPORTED

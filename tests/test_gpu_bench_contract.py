@@ -32,7 +32,8 @@ def test_bench_json_line():
     e2e = line["e2e"]
     assert e2e["value"] > 0 and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 4096 * 512 * 4 == e2e["d2h_bytes_per_step"]
-    assert line["gpu_launches"] == 7 * 3  # route, count, scan, place, up, down, combine
+    # counted by the library: route, count, scan, place, up, down, combine
+    assert line["gpu_launches"] == 7 * 3 and line["launches_per_step"] == 7
     rf = line["roofline"]
     for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
         assert key in rf, key
@@ -49,4 +50,6 @@ def test_bench_json_line():
     (rec,) = line["configs"]
     assert rec["workload"] == "sweep_T4096_s0" and rec["value"] > 0 and rec["steps"] >= 20
     assert "route_permute_unpermute" in rec["kernels"] and "flushed" in rec["l2"]
+    # 256 experts at T=4096: a sliced router (router + merge), count, scan, place, combine
+    assert rec["launches_per_step"] == 6 and rec["gpu_launches"] == 6 * rec["steps"]
     assert set(rec["clocks"]) >= {"sm_mhz", "reasons"}

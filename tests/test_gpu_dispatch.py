@@ -154,3 +154,16 @@ def test_dispatch_deterministic():
     b = run_dispatch(cfg, x, idx)
     for key in ["slot_row", "row_token", "expert_offsets", "xp", "rank_splits"]:
         assert torch.equal(a[key], b[key]), key
+
+
+@pytest.mark.parametrize("T,E,k", [(3000, 16, 2), (4099, 256, 8)])
+def test_dispatch_launch_count(T, E, k):
+    """One moe_dispatch call enqueues three kernels (count, scan, place), as the
+    library's own launch counter reports."""
+    cfg = _cfg(T, 256, E, k, 8)
+    idx = W.random_topk(T, E, k, seed=T + E, skew=0.8)
+    x = W._grid_int((T, 256), -8, 8, 8.0, W._gen(T, "cpu"), "cpu").to(torch.bfloat16).to(DEV)
+    n0 = moe.moe_launch_count()
+    out = run_dispatch(cfg, x, idx)
+    assert moe.moe_launch_count() - n0 == 3
+    _compare(cfg, x, idx, out)

@@ -33,6 +33,9 @@ def _case(name, T, **over):
     ("deepseek", 96, {"d": 512, "max_ranks": 4}),              # rank-limited choices
     ("deepseek", 64, {}),                                      # full width, 256 experts
     ("toy", 77, {"score": "sigmoid", "renorm": False, "E": 16, "R": 4, "k": 3}),  # fp32 sigmoid
+    # long batches: the weight gradient's token range split over a cluster of 8 / 2 CTAs
+    ("mixtral", 16384, {"d": 1024}),
+    ("toy", 5000, {"E": 6, "R": 2}),                           # fp32, an expert block of 6
 ])
 def test_route_backward_matches_oracle(name, T, over):
     w, inp = _case(name, T, **over)
@@ -85,3 +88,23 @@ def test_route_backward_optional_outputs_and_empty_batch():
                            dlb)
     torch.cuda.synchronize()
     assert torch.all(dw == 0) and torch.all(dlb == 0)
+
+
+def test_route_backward_weight_gradient_is_deterministic():
+    """The weight and bias gradients add their partial sums in a fixed order
+    (also across the CTAs of a cluster): two calls agree bit for bit."""
+    w, inp = _case("mixtral", 8192, d=1024)
+    cfg = moe.config_from_workload(w, T=8192)
+    dev = {k: (v.to(DEV) if torch.is_tensor(v) else v) for k, v in inp.items()}
+    idx, _ = run_route(cfg, dev)
+    dg = torch.randn((8192, w.k), generator=torch.Generator().manual_seed(5)).to(DEV)
+    outs = []
+    for _ in range(2):
+        dL = torch.empty((8192, w.E), device=DEV)
+        dw = torch.empty((w.E, w.d), dtype=w.torch_dtype, device=DEV)
+        dlb = torch.empty(w.E, device=DEV)
+        moe.moe_route_backward(cfg, dev["x"], dev["w_router"], None, idx.to(DEV), dg, dL, None,
+                               dw, dlb)
+        torch.cuda.synchronize()
+        outs.append((dw.view(torch.int16).clone(), dlb.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
