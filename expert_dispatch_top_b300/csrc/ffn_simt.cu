@@ -9,7 +9,8 @@
 // up columns), K in steps of 8 through double-buffered shared memory with the
 // next step's loads in registers, 8 x 8 outputs per thread split over rows
 // {4ty.., 64+4ty..} and columns {4tx.., 64+4tx..} so that every shared-memory
-// read is a conflict-free float4.
+// read is a conflict-free float4; the products run as paired FMAs (two
+// columns per instruction).
 //
 // Groups are ragged: group g owns rows [offsets[g], offsets[g+1]) of A and
 // out.  blockIdx.x enumerates (group, m-tile) pairs from the device-side
@@ -26,6 +27,24 @@ __device__ __forceinline__ float gelu_f(float v) {
     return 0.5f * v * (1.f + erff(v * 0.70710678118654752440f));
 }
 __device__ __forceinline__ float silu_f(float v) { return v / (1.f + expf(-v)); }
+
+// Packed fp32 pairs (a .b64 register holding two floats) and the paired FMA
+// of sm_100+: two IEEE single-precision FMAs per instruction, each rounded as
+// fmaf rounds, so results are bit-identical to scalar FMAs while the FMA
+// instructions a warp must issue halve.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
 
 template <bool GATED>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a) {
@@ -79,11 +98,12 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a) {
     const bool b_ok = GATED ? ((lr < 64 ? n0 + lr : n0 + lr - 64) < N) : (brow < N);
     const float* b_src = B + (int64_t)(b_ok ? brow : 0) * K + lk;
 
-    float acc[8][8];
+    // accumulators: row i, column pairs (2jp, 2jp+1) packed
+    uint64_t acc2[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        for (int jp = 0; jp < 4; ++jp) acc2[i][jp] = 0ull;
 
     auto load = [&](int k0, float4& ra, float4& rb) {
         const bool kin = k0 + lk < K;  // K % 4 == 0: a float4 is all in or all out
@@ -116,16 +136,24 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a) {
             const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
             const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
             const float ar[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float br[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const uint64_t bp[4] = {pack2(b0.x, b0.y), pack2(b0.z, b0.w), pack2(b1.x, b1.y),
+                                    pack2(b1.z, b1.w)};
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 8; ++i) {
+                const uint64_t ai = pack2(ar[i], ar[i]);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
+                for (int jp = 0; jp < 4; ++jp) acc2[i][jp] = ffma2(ai, bp[jp], acc2[i][jp]);
+            }
         }
         if (more) store(buf ^ 1, ra, rb);
         __syncthreads();
         buf ^= 1;
     }
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int jp = 0; jp < 4; ++jp) unpack2(acc2[i][jp], acc[i][2 * jp], acc[i][2 * jp + 1]);
     // epilogue: row r = {4ty + i, 64 + 4ty + i}; plain columns {4tx + j, 64 + 4tx + j};
     // gated: gate column 4tx + j pairs with up column (tile column 64 + 4tx + j)
     float* out = static_cast<float*>(a.out);

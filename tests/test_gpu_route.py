@@ -114,6 +114,27 @@ def test_route_sigmoid_every_grid_logit():
     assert torch.equal(gate, rgate)   # no-renorm sigmoid gates are the scores themselves
 
 
+@pytest.mark.parametrize("lo,hi", [(-12.0, 4.0), (-95.0, -60.0)])
+def test_route_sigmoid_scores_of_arbitrary_fp32_logits(lo, hi):
+    """Sigmoid scores of logits with arbitrary fp32 mantissas (a random logit
+    bias per expert on top of the grid logits), bit for bit against the oracle's
+    double-precision evaluation rounded to fp32: 32768 chosen scores in the
+    middle of the sigmoid (bias in [-12, 4]), or far out in its tail (bias in
+    [-95, -60], down to the subnormal range, where the double path decides)."""
+    E, k, d, T = 256, 8, 64, 4096
+    g = torch.Generator().manual_seed(int(lo * 7 + hi))
+    x = torch.randint(-8, 9, (T, d), generator=g).float().div(8).to(torch.bfloat16)
+    wr = torch.randint(-8, 9, (E, d), generator=g).float().div(64).to(torch.bfloat16)
+    lb = (torch.rand(E, generator=g, dtype=torch.float64) * (hi - lo) + lo).float()
+    w = W.Workload("sigf", T, d, E, 1, k, 64, "identity", "bf16", "sigmoid", False, 0.0, 0, 0,
+                   "normal512")
+    inp = dict(x=x, w_router=wr, logit_bias=lb, sel_bias=None)
+    idx, gate = run_route(cfg_for(w), to_dev(inp))
+    ridx, rgate = oracle.route(x, wr, k, "sigmoid", False, lb, None)
+    assert torch.equal(idx, ridx.to(idx.dtype))
+    assert torch.equal(gate, rgate)
+
+
 def test_route_snippet_loads_on_gpu():
     """The Ultralytics routing snippet through the GPU route and dispatch:
     per-expert loads 948..1087 and per-GPU loads 1968..2139."""
