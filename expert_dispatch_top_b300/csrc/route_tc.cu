@@ -446,10 +446,14 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                     for (int i = 0; i < 32; ++i) {
                         const int e = e0 + c * 32 + i;
                         const float L = has_lb ? __fadd_rn(v[i], lb_s[e & 255]) : v[i];
-                        stash[i] = L;
+                        v[i] = L;
                         nonfinite |= (SPLIT || e < e_end) && !(fabsf(L) <= FLT_MAX);
                         if ((SPLIT || e < e_end) && L > thr && rank_ok(e)) mask |= 1u << i;
                     }
+                    // stored after the loop: a store between the bias loads would
+                    // order them (the compiler cannot tell the areas apart)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) stash[i] = v[i];
                     while (mask) {
                         const int i = __ffs(mask) - 1;
                         mask &= mask - 1;
