@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(256) route_bwd_token_kernel(RouteBwdArgs a) {
 
 // dW[e, cols] = sum over t of dL[t,e] x[t, cols], and d_logit_bias[e] = sum
 // over t of dL[t,e].  A CTA owns 8 experts and 32 column vectors (256 bf16 or
-// 128 fp32 columns) for a contiguous range of tokens; its 16 warps take
+// 128 fp32 columns) for a contiguous range of tokens; its 8 warps take
 // interleaved groups of 32 tokens.  Per group, lane l reads token l's 8 dL
 // entries (32 contiguous bytes), then the warp walks the group's tokens with
 // any nonzero entry four at a time: each lane loads its column vector of the
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(256) route_bwd_token_kernel(RouteBwdArgs a) {
 // Every sum is taken in a fixed order (warps in index order, cluster ranks in
 // rank order, lanes by a fixed shuffle tree), so the result is deterministic.
 constexpr int kWExperts = 8;
-constexpr int kWWarps = 16;
+constexpr int kWWarps = 8;
 constexpr int kWMaxSplit = 8;
 constexpr int kWBatch = 4;  // x rows in flight per lane
 
@@ -232,7 +232,7 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kWWarps * 32, 1) route_bwd_weight_kernel(RouteBwdArgs a, int S) {
+__global__ void __launch_bounds__(kWWarps * 32) route_bwd_weight_kernel(RouteBwdArgs a, int S) {
     constexpr int V = Elem<T>::kPerVec;
     constexpr int COLS = 32 * V;
     __shared__ float part[kWExperts][COLS];  // this CTA's sums (warps added in order)
@@ -370,10 +370,13 @@ cudaError_t launch_typed(const RouteBwdArgs& a, cudaStream_t s) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // token splits (a power of two <= 8) until there is a CTA per SM (one fits
-    // an SM), with at least 64 token groups per split
+    // token splits (a power of two <= 8) until there are about two CTAs per SM
+    // (two fit an SM), with at least 64 token groups per split.  Measured with 8
+    // warps per CTA (Mixtral shape 0.133 ms, DeepSeek shape 0.441 ms) against
+    // 16 warps and one CTA per SM (0.186 / 0.515 ms).
     int S = 1;
-    while (S < kWMaxSplit && (int64_t)eb * cb * S < (int64_t)sms && (a.T + 31) / 32 >= 64 * 2 * S)
+    while (S < kWMaxSplit && (int64_t)eb * cb * S < 2 * (int64_t)sms &&
+           (a.T + 31) / 32 >= 64 * 2 * S)
         S *= 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(eb, cb, (unsigned)S);
