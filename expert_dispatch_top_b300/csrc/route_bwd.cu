@@ -208,29 +208,6 @@ constexpr int kWWarps = 8;
 constexpr int kWMaxSplit = 8;
 constexpr int kWBatch = 4;  // x rows in flight per lane
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-}
-// Shared-memory address of the same variable in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
-    uint32_t out;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-                 : "=r"(out)
-                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
-    return out;
-}
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kWWarps * 32) route_bwd_weight_kernel(RouteBwdArgs a, int S) {
     constexpr int V = Elem<T>::kPerVec;
@@ -378,22 +355,8 @@ cudaError_t launch_typed(const RouteBwdArgs& a, cudaStream_t s) {
     while (S < kWMaxSplit && (int64_t)eb * cb * S < 2 * (int64_t)sms &&
            (a.T + 31) / 32 >= 64 * 2 * S)
         S *= 2;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(eb, cb, (unsigned)S);
-    cfg.blockDim = dim3(kWWarps * 32);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 1;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = (unsigned)S;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, route_bwd_weight_kernel<T>, a, S);
-    if (e == cudaSuccess) note_launch();
-    return e;
+    return launch_pdl_cluster(route_bwd_weight_kernel<T>, dim3(eb, cb, (unsigned)S), kWWarps * 32, 0,
+                              s, dim3(1, 1, (unsigned)S), a, S);
 }
 
 }  // namespace

@@ -90,6 +90,11 @@ struct RtParams {
     // gates without renormalisation, its partial softmax sum to `zpart`), and
     // route_merge_kernel forms the final top-k and gates.
     int split, Eh, units;
+    // 1 (split only, one unit per CTA): the split units of a tile form a
+    // thread-block cluster; each leaves its partial list in its stash rows and
+    // the slice-0 CTA merges them through distributed shared memory (no merge
+    // kernel, no partial lists in global memory)
+    int cmerge;
     // 1: epilogue group 0 first runs its code once on the unused TMEM buffer,
     // storing nothing, while the K loop streams x (see the epilogue)
     int warm;
@@ -556,7 +561,19 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
                     }
                 }
             }
-            if (SPLIT) {
+            if (SPLIT && p.cmerge) {
+                // this slice's exact top-k (and partial softmax sum), left in the
+                // thread's stash row for the cluster merge at the end
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j >= j0) {
+                        stash[3 * (j - j0)] = top.key[j];
+                        stash[3 * (j - j0) + 1] = top.val[j];
+                        stash[3 * (j - j0) + 2] = __int_as_float(top.idx[j]);
+                    }
+                stash[24] = m;
+                stash[25] = z;
+            } else if (SPLIT) {
                 // this slice's exact top-k (and partial softmax sum) for the merge
                 if (row_ok && t < p.T) {
                     RoutePartial* pp = p.part + ((int64_t)t * p.split + h) * p.k;
@@ -604,6 +621,71 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
     if (warp == 1) {
         __syncwarp();
         tmem_dealloc(tmem_base, R_TMEM_COLS);
+    }
+    if (SPLIT && p.cmerge) {
+        // Cluster merge: every slice's lists are in its CTA's stash rows (the same
+        // offsets in every CTA of the cluster, one row per token of the tile).
+        cluster_sync();
+        if (warp >= 2 && warp < 6 && (int)blockIdx.x < p.units && (int)blockIdx.x % p.split == 0) {
+            const int row = (warp & 3) * 32 + lane;
+            const int64_t t = (int64_t)((int)blockIdx.x / p.split) * p.tile_rows + row;
+            const float* own = stash_all + (threadIdx.x - 64) * p.stash_pitch;
+            TopK top;
+            top.init(p.k);
+            for (int h = 0; h < p.split; ++h) {
+                for (int jj = 0; jj < p.k; ++jj) {
+                    float kv, vv, iv;
+                    if (h == 0) {
+                        kv = own[3 * jj];
+                        vv = own[3 * jj + 1];
+                        iv = own[3 * jj + 2];
+                    } else {
+                        kv = ld_cluster_f32(cluster_addr(own + 3 * jj, (uint32_t)h));
+                        vv = ld_cluster_f32(cluster_addr(own + 3 * jj + 1, (uint32_t)h));
+                        iv = ld_cluster_f32(cluster_addr(own + 3 * jj + 2, (uint32_t)h));
+                    }
+                    top.insert(kv, vv, __float_as_int(iv));
+                }
+            }
+            const int j0 = 8 - p.k;
+            float g[8];
+            if (p.score != MOE_SCORE_SIGMOID) {
+                float m = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j == j0) m = top.val[j];
+                float z = 0.f;
+                if (p.renorm) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (j >= j0) z += expf(top.val[j] - m);
+                } else {
+                    for (int h = 0; h < p.split; ++h) {
+                        const float mh = h == 0 ? own[24] : ld_cluster_f32(cluster_addr(own + 24, (uint32_t)h));
+                        const float zh = h == 0 ? own[25] : ld_cluster_f32(cluster_addr(own + 25, (uint32_t)h));
+                        z += zh * expf(mh - m);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) g[j] = expf(top.val[j] - m) / z;
+            } else {
+                float z = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j >= j0) z += top.val[j];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) g[j] = p.renorm ? top.val[j] / z : top.val[j];
+            }
+            if (row < p.tile_rows && t < p.T) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j >= j0) {
+                        p.idx[t * p.k + (j - j0)] = top.idx[j];
+                        p.gate[t * p.k + (j - j0)] = g[j];
+                    }
+            }
+        }
+        cluster_sync();  // no CTA leaves while the merge reads its shared memory
     }
 }
 
@@ -747,6 +829,7 @@ cudaError_t launch_route_tc(const RouteArgs& a, cudaStream_t s) {
     p.m_tiles = (int)((a.T + p.tile_rows - 1) / p.tile_rows);
     p.units = p.m_tiles * p.split;
     const int grid = p.units < sms ? p.units : sms;
+    p.cmerge = (p.split > 1 && p.units <= grid) ? 1 : 0;
     // K blocks per ring stage (their x boxes issued back to back, so each row is
     // read in runs of kbs * 128 bytes).  Measured (moe_route alone, CUDA events,
     // L2 flushed): 8 experts 41.0 / 38.9 / 41.0 us for 1 / 2 / 4 blocks; 64-expert
@@ -792,6 +875,32 @@ cudaError_t launch_route_tc(const RouteArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kDevs) attr_bytes[dev][form] = smem;
     }
+    if (p.cmerge) {
+        // only if the cluster fits beside nothing else (it needs p.split SMs of one GPC)
+        static int fits[kDevs][5] = {};  // 0 unknown, 1 yes, 2 no
+        int& f = fits[dev >= 0 && dev < kDevs ? dev : 0][p.split];
+        if (f == 0) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(grid);
+            cfg.blockDim = dim3(64 + 128 * p.epi_groups);
+            cfg.dynamicSmemBytes = (size_t)smem;
+            cfg.stream = s;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)p.split;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            f = (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) ? 1 : 2;
+            cudaGetLastError();  // a refused query leaves no error behind
+        }
+        if (f != 1) p.cmerge = 0;
+    }
+    if (p.cmerge)
+        return launch_pdl_cluster(kern, dim3(grid), 64 + 128 * p.epi_groups, (size_t)smem, s,
+                                  dim3((unsigned)p.split, 1, 1), tmX, tmW, p);
     cudaError_t e =
         launch_pdl(kern, dim3(grid), 64 + 128 * p.epi_groups, (size_t)smem, s, tmX, tmW, p);
     if (e != cudaSuccess || p.split == 1) return e;

@@ -436,8 +436,8 @@ int moe_build_checked(void);
  * that fails its argument checks launches nothing).  The difference of two
  * readings around a region counts the library's kernels enqueued in it, e.g.
  * the launches one moe_layer_forward makes for a configuration (route 1, or 2
- * when a small batch's experts are sliced; dispatch 3; FFN 2 per expert set;
- * combine 1).  Host-side; no
+ * when a batch's expert slices take more than one wave; dispatch 3; FFN 2 per
+ * expert set; combine 1).  Host-side; no
  * synchronisation.
  */
 uint64_t moe_launch_count(void);

@@ -32,6 +32,9 @@ def _setup(T, d, E, k, R, cap, dtype, seed):
     (333, 128, 8, 2, 60, True, False),
     (1024, 512, 64, 8, 90, True, True),
     (4100, 7168, 256, 8, 0, False, True),
+    # small batches of wide k = 8 rows, ragged T, drops, with and without a residual
+    (3001, 4096, 128, 8, 50, False, False),
+    (3001, 4096, 128, 8, 50, True, False),
 ])
 def test_combine_matches_oracle(dtype, tol, T, d, E, k, cap, resid, shared):
     disp, yp, gate, x, sh = _setup(T, d, E, k, 4, cap, dtype, seed=T + d)
