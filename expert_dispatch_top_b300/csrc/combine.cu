@@ -70,7 +70,6 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     const char* rs = static_cast<const char*>(a.resid);
     char* y = static_cast<char*>(a.y);
     pdl_wait();  // the expert FFN's (or dispatch's) rows
-    pdl_launch_dependents();
     for (int64_t t = warp0; t < a.T; t += nwarps) {
         int r_l = -1;
         float g_l = 0.f;

@@ -24,12 +24,12 @@
 //                    decides keep/drop against C and the row; then the block
 //                    copies its tokens' rows with 16-byte vectors.
 // Nothing waits on another CTA: the order comes from the scan, not from a
-// look-back chain, so no kernel here spins.  All three are programmatic
-// dependents of the kernel before them: each starts while its predecessor
-// runs, does what does not need the predecessor's results (place: the
-// per-block bitmaps from topk_idx), and waits (griddepcontrol.wait) before
-// reading them.  Every kernel releases its successor only after its own wait,
-// so when place_kernel starts, the router that wrote topk_idx has completed.
+// look-back chain, so no kernel here spins.  All three are launched as
+// programmatic dependents of the kernel before them (pre-staged, started when
+// it completes) and wait (griddepcontrol.wait) for its memory before reading
+// its results.  place_kernel builds its per-block bitmaps from topk_idx before
+// that wait: it starts only after scan_kernel has completed, which waited for
+// count_kernel, which waited for the router that wrote topk_idx.
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
@@ -89,7 +89,6 @@ __global__ void __launch_bounds__(256) count_kernel(DispatchArgs a, int tb, int 
     // wait, which is safe because no kernel of the chain lets its successor
     // start before its own predecessor has completed.
     pdl_wait();
-    pdl_launch_dependents();
     if (b == 0) {
         int32_t* splits = a.rank_splits ? a.rank_splits : a.splits_acc;
         for (int i = tid; i < a.R * a.R; i += blockDim.x) splits[i] = 0;
@@ -118,7 +117,6 @@ __global__ void __launch_bounds__(256) count_kernel(DispatchArgs a, int tb, int 
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(DispatchArgs a, int nblk) {
     __shared__ int scratch[33];
     pdl_wait();  // count_kernel's histograms
-    pdl_launch_dependents();
     const int e = blockIdx.x;
     const int32_t* in = a.hist + (int64_t)e * nblk;
     int32_t* out = a.prefix + (int64_t)e * nblk;
@@ -241,7 +239,6 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(DispatchArgs a, in
     }
     // scan_kernel's prefixes and totals from here on
     pdl_wait();
-    pdl_launch_dependents();
     {
         const int e = tid;  // E <= 256 = blockDim.x
         int total = 0, kept = 0, pre = 0;

@@ -53,7 +53,6 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a) {
     __shared__ int s_g, s_row0, s_rows;
     const int tid = threadIdx.x;
     pdl_wait();  // programmatic dependent launch: the previous kernel's writes
-    pdl_launch_dependents();
     if (tid == 0) {
         int rem = blockIdx.x, g = -1, row0 = 0, rows = 0;
         for (int q = 0; q < a.G; ++q) {

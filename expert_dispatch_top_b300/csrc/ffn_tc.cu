@@ -217,7 +217,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     // programmatic dependent launch: everything above touched no global data
     pdl_wait();
-    pdl_launch_dependents();
     if (warp == 2) {
         // Per-group tile table: lane l covers groups [8l, 8l+8).
         int cnt[8], kbs[8];

@@ -170,7 +170,6 @@ __device__ __forceinline__ void select_and_gate(const float (&L)[NV], int e_base
 template <typename T, int EMAX>
 __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
     pdl_wait();  // programmatic dependent launch: the previous kernel's writes
-    pdl_launch_dependents();
     constexpr int TPW = 32 / EMAX;
     constexpr int V = Elem<T>::kPerVec;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -263,7 +262,6 @@ template <typename T, int EP>
 __global__ void __launch_bounds__(256) route_big_kernel(RouteArgs a) {
     extern __shared__ __align__(16) float sm[];
     pdl_wait();  // programmatic dependent launch: the previous kernel's writes
-    pdl_launch_dependents();
     float* xs = sm;                // [kKC][kTT]
     float* ws = sm + kKC * kTT;    // [kKC][EP]
     float* Ls = sm;                // [kTT][EP+1] after the GEMM

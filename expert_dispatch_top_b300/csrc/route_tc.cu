@@ -239,7 +239,6 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), R_TMEM_COLS);
     // programmatic dependent launch: everything above touched no global data
     pdl_wait();
-    pdl_launch_dependents();
     if (warp >= 2) {
         for (int e = threadIdx.x - 64; e < 256; e += (int)blockDim.x - 64) {
             lb_s[e] = (p.logit_bias && e < p.E) ? p.logit_bias[e] : 0.f;
@@ -697,7 +696,6 @@ __global__ void __launch_bounds__(R_THREADS_MAX, 1)
 // common maximum.
 __global__ void __launch_bounds__(256) route_merge_kernel(const RtParams p) {
     pdl_wait();  // the router's partial lists
-    pdl_launch_dependents();
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= p.T) return;
     TopK top;
