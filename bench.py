@@ -83,6 +83,17 @@ def fp32_ffma_peak_tflops(sm_count, sm_mhz):
     return sm_count * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
+# Dense tf32 : bf16 tensor rate on B300, nominal (1.1 vs 2.25 PFLOP/s): the
+# tf32 roofline is the measured bf16 burst peak times this ratio.
+TF32_PER_BF16 = 1.1 / 2.25
+
+
+def ffn_on_tf32(w):
+    """fp32 experts whose d and d_ff are multiples of 32 run on the tensor cores
+    as three tf32 products per fp32 product (split pass + up + down)."""
+    return w.dtype == "f32" and w.act != "identity" and w.d % 32 == 0 and w.d_ff % 32 == 0
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
 
@@ -388,11 +399,19 @@ def kernel_report(w, work, phase, peaks, sms):
             fp32_ffma_peak_tflops(sms, peaks["sm_mhz"])
     if not ident:
         tf = work["ffn_flops"] / (phase["ffn"] * 1e-3) / 1e12
-        k["ffn"] = {"ms": phase["ffn"], "TFLOP/s": tf, "launches_per_step": 2 * (1 + w.n_shared)}
+        x3 = ffn_on_tf32(w)
+        k["ffn"] = {"ms": phase["ffn"], "TFLOP/s": tf,
+                    "launches_per_step": (3 if x3 else 2) * (1 + w.n_shared)}
         if w.dtype == "bf16":
             k["ffn"]["frac_bf16_burst"] = tf / peaks["bf16"]
             k["ffn"]["frac_bf16_sustained"] = tf / peaks["bf16_sus"]
+        elif x3:
+            # three tf32 products per fp32 product; the phase includes the split pass
+            k["ffn"]["pipe"] = "tensor (fp32 as three tf32 products)"
+            k["ffn"]["tf32_TFLOP/s"] = 3 * tf
+            k["ffn"]["frac_tf32_burst"] = 3 * tf / (peaks["bf16"] * TF32_PER_BF16)
         else:
+            k["ffn"]["pipe"] = "FFMA (fp32)"
             k["ffn"]["frac_fp32_ffma"] = tf / fp32_ffma_peak_tflops(sms, peaks["sm_mhz"])
     else:
         moved = work["route_bytes"] + work["permute_bytes"] + work["combine_bytes"]
@@ -647,6 +666,18 @@ def run_ours(args, w):
                         "traffic": traffic, "peak_kind": f"bf16 burst ({peaks['src']})",
                         "frac_of_sustained": achieved / peaks["bf16_sus"],
                         "algorithmic_flops_per_step": work["ffn_flops"]}
+        elif ffn_on_tf32(w):
+            # tensor work: three tf32 products per fp32 product, over the phase's
+            # time (the split pass included); the FFN runs in sub-ms windows: burst
+            pk = peaks["bf16"] * TF32_PER_BF16
+            roofline = {"kernel": "tc_gemm_x3_kernel (fp32 expert FFN as three tf32 products: "
+                                  "split pass + up + down per step)",
+                        "bound": "tensor", "achieved": 3 * achieved, "peak": pk, "unit": "TFLOP/s",
+                        "frac": 3 * achieved / pk, "traffic": None,
+                        "peak_kind": f"tf32 dense = bf16 burst ({peaks['src']}) x 1.1/2.25 nominal",
+                        "fp32_TFLOP/s": achieved,
+                        "algorithmic_flops_per_step": work["ffn_flops"],
+                        "tensor_flops_per_step": 3 * work["ffn_flops"]}
         else:
             pk = fp32_ffma_peak_tflops(sms, peaks["sm_mhz"])
             roofline = {"kernel": "gemm_simt_kernel (fp32 expert FFN, up+down per step)",

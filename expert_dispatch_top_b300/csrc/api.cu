@@ -48,8 +48,18 @@ struct Layout {
     size_t totals, hist, prefix, splits_acc, route_part, safe_offsets;
     size_t topk_idx, topk_gate, slot_row, row_token, expert_counts, offsets, rank_counts,
         rank_splits, n_dropped;
+    // fp32 experts on the tensor cores: tf32 high and low parts of the GEMM operands
+    size_t x3_a_hi, x3_a_lo, x3_wu_hi, x3_wu_lo, x3_wd_hi, x3_wd_lo, x3_h_hi, x3_h_lo;
     size_t total;
 };
+
+// fp32 experts whose contraction lengths (d for the up projection, d_ff for
+// the down projection) are multiples of 32 run on the tensor cores as three
+// tf32 products (ffn_tf32.cu); other fp32 shapes run on FFMA (ffn_simt.cu).
+inline bool ffn_uses_x3(const moe_config* c) {
+    return c->act_dtype == MOE_DTYPE_F32 && c->act != MOE_ACT_IDENTITY && c->d % 32 == 0 &&
+           c->d_ff % 32 == 0;
+}
 
 Layout layout_of(const moe_config* c) {
     Layout L;
@@ -87,6 +97,24 @@ Layout layout_of(const moe_config* c) {
     o = align_up(o + (size_t)c->R * c->R * 4);
     L.n_dropped = o;
     o = align_up(o + 4);
+    L.x3_a_hi = L.x3_a_lo = L.x3_wu_hi = L.x3_wu_lo = L.x3_wd_hi = L.x3_wd_lo = L.x3_h_hi =
+        L.x3_h_lo = o;
+    if (ffn_uses_x3(c)) {
+        // rows of A: the routed rows, or the shared expert's T rows (the passes
+        // run one after the other and reuse these sections)
+        const int64_t mr = max_rows_of(c);
+        const size_t arows = (size_t)(c->n_shared == 1 && c->T > mr ? c->T : mr);
+        const size_t up_rows = (size_t)(c->act == MOE_ACT_SWIGLU ? 2 : 1) * c->d_ff;
+        const size_t a = arows * c->d * 4, wu = (size_t)c->E * up_rows * c->d * 4;
+        const size_t wd = (size_t)c->E * c->d * c->d_ff * 4, h = arows * c->d_ff * 4;
+        size_t* sec[8] = {&L.x3_a_hi, &L.x3_a_lo, &L.x3_wu_hi, &L.x3_wu_lo,
+                          &L.x3_wd_hi, &L.x3_wd_lo, &L.x3_h_hi, &L.x3_h_lo};
+        const size_t len[8] = {a, a, wu, wu, wd, wd, h, h};
+        for (int i = 0; i < 8; ++i) {
+            *sec[i] = o;
+            o = align_up(o + len[i]);
+        }
+    }
     L.total = o;
     return L;
 }
@@ -208,6 +236,7 @@ moe_status ffn_impl(const moe_config* c, const void* xp, const int32_t* offsets,
     const Layout L = layout_of(c);
     uint32_t* status = at<uint32_t>(ws, L.status);
     const bool tc = c->act_dtype == MOE_DTYPE_BF16;
+    const bool x3 = ffn_uses_x3(c);
     if (kChecked && !check_only) {
         // checked build: the kernels read a copy made non-decreasing within the rows
         int32_t* safe = at<int32_t>(ws, L.safe_offsets);
@@ -243,15 +272,53 @@ moe_status ffn_impl(const moe_config* c, const void* xp, const int32_t* offsets,
         dn.N = c->d;
         dn.K = c->d_ff;
         dn.epi = EPI_NONE;
+        if (x3) {
+            // both GEMMs read the tf32 split of their operands; the up projection
+            // stores h and its split, which the down projection reads
+            u.A = at<float>(ws, L.x3_a_hi);
+            u.A_lo = at<float>(ws, L.x3_a_lo);
+            u.B = at<float>(ws, L.x3_wu_hi);
+            u.B_lo = at<float>(ws, L.x3_wu_lo);
+            u.out_hi = at<float>(ws, L.x3_h_hi);
+            u.out_lo = at<float>(ws, L.x3_h_lo);
+            dn.A = u.out_hi;
+            dn.A_lo = u.out_lo;
+            dn.B = at<float>(ws, L.x3_wd_hi);
+            dn.B_lo = at<float>(ws, L.x3_wd_lo);
+        }
         if (u.rows_cap > 0 && tc && (gemm_tc_supported(u) != 0 || gemm_tc_supported(dn) != 0))
+            return MOE_ERR_UNSUPPORTED;
+        if (u.rows_cap > 0 && x3 && (gemm_x3_supported(u) != 0 || gemm_x3_supported(dn) != 0))
             return MOE_ERR_UNSUPPORTED;
     }
     if (check_only) return MOE_OK;
     for (int pass = 0; pass < npass; ++pass) {
         if (up[pass].rows_cap == 0) continue;
-        cudaError_t e = tc ? launch_gemm_tc(up[pass], s) : launch_gemm_simt(up[pass], s);
-        if (e != cudaSuccess) return MOE_ERR_CUDA;
-        e = tc ? launch_gemm_tc(down[pass], s) : launch_gemm_simt(down[pass], s);
+        cudaError_t e;
+        if (x3) {
+            // this expert set's input rows and weights, split into the workspace
+            const bool shared = pass == 1;
+            const int64_t up_rows = (int64_t)(c->act == MOE_ACT_SWIGLU ? 2 : 1) * c->d_ff;
+            Tf32SplitJob j[3];
+            j[0].src = static_cast<const float*>(shared ? shared_x : xp);
+            j[0].n = up[pass].rows_cap * c->d;
+            j[1].src = static_cast<const float*>(shared ? shared_up : w_up);
+            j[1].n = (int64_t)up[pass].G * up_rows * c->d;
+            j[2].src = static_cast<const float*>(shared ? shared_down : w_down);
+            j[2].n = (int64_t)up[pass].G * c->d * c->d_ff;
+            const size_t hi[3] = {L.x3_a_hi, L.x3_wu_hi, L.x3_wd_hi};
+            const size_t lo[3] = {L.x3_a_lo, L.x3_wu_lo, L.x3_wd_lo};
+            for (int i = 0; i < 3; ++i) {
+                j[i].hi = at<float>(ws, hi[i]);
+                j[i].lo = at<float>(ws, lo[i]);
+            }
+            e = launch_tf32_split(j, 3, s);
+            if (e == cudaSuccess) e = launch_gemm_x3(up[pass], s);
+            if (e == cudaSuccess) e = launch_gemm_x3(down[pass], s);
+        } else {
+            e = tc ? launch_gemm_tc(up[pass], s) : launch_gemm_simt(up[pass], s);
+            if (e == cudaSuccess) e = tc ? launch_gemm_tc(down[pass], s) : launch_gemm_simt(down[pass], s);
+        }
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     return MOE_OK;

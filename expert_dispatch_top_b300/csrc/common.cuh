@@ -134,6 +134,13 @@ __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
 // kernels of small batches kept the launch-latency gain of the pre-staging.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// The fp32 expert activations: GELU in its erf form, 0.5 v (1 + erf(v / sqrt 2)),
+// and SiLU, v / (1 + e^-v).
+__device__ __forceinline__ float gelu_erf_f(float v) {
+    return 0.5f * v * (1.f + erff(v * 0.70710678118654752440f));
+}
+__device__ __forceinline__ float silu_exact_f(float v) { return v / (1.f + expf(-v)); }
+
 // Counts one kernel launch enqueued by this library (moe_launch_count).
 void note_launch();
 // Counts the launch just made with <<<...>>> if it was accepted; returns its error.

@@ -23,10 +23,6 @@ namespace {
 
 constexpr int SBM = 128, SBN = 128, SBK = 8;
 
-__device__ __forceinline__ float gelu_f(float v) {
-    return 0.5f * v * (1.f + erff(v * 0.70710678118654752440f));
-}
-__device__ __forceinline__ float silu_f(float v) { return v / (1.f + expf(-v)); }
 
 // Packed fp32 pairs (a .b64 register holding two floats) and the paired FMA
 // of sm_100+: two IEEE single-precision FMAs per instruction, each rounded as
@@ -165,10 +161,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a) {
             const int n = n0 + tx * 4;
             if (n < N) {
                 float4 o;
-                o.x = silu_f(acc[i][0]) * acc[i][4];
-                o.y = silu_f(acc[i][1]) * acc[i][5];
-                o.z = silu_f(acc[i][2]) * acc[i][6];
-                o.w = silu_f(acc[i][3]) * acc[i][7];
+                o.x = silu_exact_f(acc[i][0]) * acc[i][4];
+                o.y = silu_exact_f(acc[i][1]) * acc[i][5];
+                o.z = silu_exact_f(acc[i][2]) * acc[i][6];
+                o.w = silu_exact_f(acc[i][3]) * acc[i][7];
                 *reinterpret_cast<float4*>(orow + n) = o;
             }
         } else {
@@ -182,10 +178,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a) {
                 o.z = acc[i][4 * h + 2];
                 o.w = acc[i][4 * h + 3];
                 if (a.epi == EPI_GELU) {
-                    o.x = gelu_f(o.x);
-                    o.y = gelu_f(o.y);
-                    o.z = gelu_f(o.z);
-                    o.w = gelu_f(o.w);
+                    o.x = gelu_erf_f(o.x);
+                    o.y = gelu_erf_f(o.y);
+                    o.z = gelu_erf_f(o.z);
+                    o.w = gelu_erf_f(o.w);
                 }
                 *reinterpret_cast<float4*>(orow + n) = o;
             }

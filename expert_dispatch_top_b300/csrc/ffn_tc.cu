@@ -52,6 +52,7 @@
 // Every mbarrier wait is bounded by %globaltimer: on timeout the kernel sets
 // MOE_DEV_GEMM_TIMEOUT, raises an abort flag seen by the other roles, drains
 // its own MMAs (bounded) and frees TMEM before returning.
+#include "gemm_tiles.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
 
@@ -59,6 +60,7 @@ namespace moe {
 namespace {
 
 using namespace tc;
+using tiles::TileInfo;
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
@@ -68,7 +70,7 @@ constexpr int EPI_WARPS = 4;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int STG_PITCH = 144;  // staged row: 128 data bytes + 16 pad (conflict-free)
 constexpr int STG_BYTES = EPI_WARPS * 32 * STG_PITCH;
-constexpr int MAX_GROUPS = 256;
+constexpr int MAX_GROUPS = tiles::kMaxGroups;
 constexpr int TABLE_BYTES = 128 + 4 * MAX_GROUPS * 4;  // barriers + flags, then 4 int tables
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_BYTES + TABLE_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
@@ -113,64 +115,6 @@ __device__ __forceinline__ float gelu_f(float v) {
     return fmaf(hv, t, hv);
 }
 __device__ __forceinline__ float silu_f(float v) { return v / (1.f + __expf(-v)); }
-
-// Tile -> (group, n-tile, m-tile) from the per-group tile table.
-struct TileInfo {
-    int g, m_tile, n_tile, row0, rows;
-    int kb0, nkb;  // K blocks of the tile
-};
-
-// Row-offset mode: rowoff/grows hold each group's first row and row count.
-// K-grouped mode: they hold each group's first K block and K-block count.
-template <bool KG>
-__device__ __forceinline__ TileInfo decode_tile(int tile, int G, const int* tstart, const int* mt,
-                                                const int* rowoff, const int* grows,
-                                                const TcParams& p) {
-    int lo = 0, hi = G - 1;  // last g with tstart[g] <= tile
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (tstart[mid] <= tile) lo = mid;
-        else hi = mid - 1;
-    }
-    TileInfo ti;
-    ti.g = lo;
-    const int local = tile - tstart[lo];
-    ti.n_tile = local / mt[lo];
-    ti.m_tile = local - ti.n_tile * mt[lo];
-    if (KG) {
-        ti.row0 = ti.m_tile * BM;
-        ti.rows = p.kg_M - ti.row0;
-        ti.kb0 = rowoff[lo];
-        ti.nkb = grows[lo];
-    } else {
-        if (p.band > 0) {
-            // band b holds n-tiles [b*band, b*band + wb); its tiles run m-fastest
-            const int b = local / (mt[lo] * p.band);
-            const int wb = min(p.band, p.n_tiles - b * p.band);
-            const int lb = local - b * mt[lo] * p.band;
-            ti.m_tile = lb / wb;
-            ti.n_tile = b * p.band + (lb - ti.m_tile * wb);
-        }
-        ti.row0 = rowoff[lo] + ti.m_tile * BM;
-        ti.rows = grows[lo] - ti.m_tile * BM;
-        ti.kb0 = 0;
-        ti.nkb = p.num_kb;
-    }
-    if (ti.rows > BM) ti.rows = BM;
-    return ti;
-}
-
-// Exclusive prefix sum over a warp.
-__device__ __forceinline__ int warp_excl_scan(int v, int lane, int* total) {
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-    }
-    *total = __shfl_sync(0xffffffffu, incl, 31);
-    return incl - v;
-}
 
 template <bool KG, bool BMN>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -217,50 +161,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     // programmatic dependent launch: everything above touched no global data
     pdl_wait();
-    if (warp == 2) {
-        // Per-group tile table: lane l covers groups [8l, 8l+8).
-        int cnt[8], kbs[8];
-        int sum = 0, ksum = 0;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int g = lane * 8 + q;
-            cnt[q] = 0;
-            kbs[q] = 0;
-            if (g < p.G) {
-                const int lo = p.offsets ? p.offsets[g] : 0;
-                const int hi = p.offsets ? p.offsets[g + 1] : (int)p.m_rows;
-                if (KG) {
-                    const int m = (p.kg_M + BM - 1) / BM;
-                    kbs[q] = (hi - lo + BK - 1) / BK;
-                    mt[g] = m;
-                    grows[g] = kbs[q];
-                    cnt[q] = m * p.n_tiles;  // a group without rows gets zero tiles written
-                } else {
-                    const int m = (hi - lo + BM - 1) / BM;
-                    mt[g] = m > 0 ? m : 1;
-                    rowoff[g] = lo;
-                    grows[g] = hi - lo;
-                    cnt[q] = m * p.n_tiles;
-                }
-                sum += cnt[q];
-                ksum += kbs[q];
-            }
-        }
-        int total_tiles, total_kb;
-        int run = warp_excl_scan(sum, lane, &total_tiles);
-        int krun = warp_excl_scan(ksum, lane, &total_kb);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int g = lane * 8 + q;
-            if (g < p.G) {
-                tstart[g] = run;
-                if (KG) rowoff[g] = krun;
-            }
-            run += cnt[q];
-            krun += kbs[q];
-        }
-        if (lane == 31) *total_s = total_tiles;
-    }
+    if (warp == 2)
+        tiles::build_tile_table<KG, BM, BK>(p.offsets, p.m_rows, p.G, p.n_tiles, p.kg_M, lane, tstart,
+                                            mt, rowoff, grows, total_s);
     fence_before();
     __syncthreads();
     fence_after();
@@ -273,7 +176,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-                const TileInfo ti = decode_tile<KG>(tile, p.G, tstart, mt, rowoff, grows, p);
+                const TileInfo ti = tiles::decode_tile<KG, BM>(tile, p.G, tstart, mt, rowoff, grows, p);
                 for (int kb = 0; kb < ti.nkb; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, MOE_DEV_GEMM_TIMEOUT, p.wait_ns)) break;
                     const uint32_t fb = full0 + 8 * stage;
@@ -328,7 +231,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                const TileInfo ti = decode_tile<KG>(tile, p.G, tstart, mt, rowoff, grows, p);
+                const TileInfo ti = tiles::decode_tile<KG, BM>(tile, p.G, tstart, mt, rowoff, grows, p);
                 const int nkb = KG ? ti.nkb : p.num_kb;
                 const bool half = !KG && ti.rows <= HALF_M;
                 for (int kb = 0; kb < nkb; ++kb) {
@@ -379,7 +282,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const TileInfo ti = decode_tile<KG>(tile, p.G, tstart, mt, rowoff, grows, p);
+            const TileInfo ti = tiles::decode_tile<KG, BM>(tile, p.G, tstart, mt, rowoff, grows, p);
             __nv_bfloat16* obase = KG ? p.out + (int64_t)ti.g * p.kg_M * p.N : p.out;
             // every lane waits, then the warp agrees, so the .sync.aligned TMEM loads
             // below always run converged

@@ -119,11 +119,32 @@ struct GemmArgs {
     // tile (-1: off); wait_ns bounds every pipeline wait (0: the 4 s default).
     int stall_kb = -1;
     uint64_t wait_ns = 0;
+    // fp32 on the tensor cores (3xTF32 kernel): A and B are the tf32 high parts of
+    // the fp32 operands and A_lo / B_lo their low parts (same shapes, see
+    // launch_tf32_split); out_hi / out_lo, if non-null, receive the split of out.
+    const void* A_lo = nullptr;
+    const void* B_lo = nullptr;
+    void* out_hi = nullptr;
+    void* out_lo = nullptr;
 };
 cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s);
 // Returns 0 if the tensor-core grouped GEMM supports the shape, else non-zero.
 int gemm_tc_supported(const GemmArgs& a);
+// fp32 grouped GEMM on the tensor cores as three tf32 products (ffn_tf32.cu):
+// row-offset mode, K-major B, any epilogue.  0 if supported.
+int gemm_x3_supported(const GemmArgs& a);
+cudaError_t launch_gemm_x3(const GemmArgs& a, cudaStream_t s);
+// Splits up to three fp32 arrays x (n elements each, n % 4 == 0, 16-byte
+// aligned) into tf32 high and low parts: hi = rn_tf32(x), lo = rn_tf32(x - hi)
+// (non-finite x: hi = x, lo = 0).  One launch; null src skips a job.
+struct Tf32SplitJob {
+    const float* src = nullptr;
+    float* hi = nullptr;
+    float* lo = nullptr;
+    int64_t n = 0;
+};
+cudaError_t launch_tf32_split(const Tf32SplitJob* jobs, int njobs, cudaStream_t s);
 
 // Backward through the expert FFNs (input gradient, optional weight gradients).
 struct FfnBwdArgs {

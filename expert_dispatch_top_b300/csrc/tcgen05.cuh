@@ -148,6 +148,24 @@ __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t chunk
     return d;
 }
 
+// Instruction descriptor, kind::tf32: D fp32, A and B tf32 (format code 2),
+// both K-major; the field layout is that of kind::f16.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// D (+)= A . B^T with tf32 operands: 8 K elements (32 bytes of a 128-byte row) per MMA.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accum) {
     asm volatile(
@@ -193,24 +211,39 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Row-major bf16 matrix [rows, cols] as a TMA tensor map of rank 2, or a
-// stack of `depth` such matrices as rank 3 (the rank must match the loads the
-// kernel issues: tma_load_2d or tma_load_3d), with a box of box_rows x 64
-// columns and the 128-byte swizzle.  Returns false if the driver rejects it.
-inline bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows,
-                           uint64_t depth, uint32_t box_rows, int rank) {
+// Row-major matrix [rows, cols] of `dtype` (element size esize bytes) as a TMA
+// tensor map of rank 2, or a stack of `depth` such matrices as rank 3 (the
+// rank must match the loads the kernel issues: tma_load_2d or tma_load_3d),
+// with a box of box_rows x (128 / esize) columns -- one 128-byte row -- and the
+// 128-byte swizzle.  Returns false if the driver rejects it.
+inline bool make_tmap_sw128(CUtensorMap* tm, CUtensorMapDataType dtype, uint32_t esize,
+                            const void* base, uint64_t cols, uint64_t rows, uint64_t depth,
+                            uint32_t box_rows, int rank) {
     auto encode = encode_fn();
     if (!encode) return false;
     if (rank != 2 && rank != 3) return false;
     cuuint64_t dims[3] = {cols, rows, depth};
-    cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
-    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint64_t strides[2] = {cols * esize, rows * cols * esize};
+    cuuint32_t box[3] = {128 / esize, box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    return encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
-                  dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    return encode(tm, dtype, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
+}
+
+// bf16: boxes of box_rows x 64 columns.
+inline bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows,
+                           uint64_t depth, uint32_t box_rows, int rank) {
+    return make_tmap_sw128(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, depth,
+                           box_rows, rank);
+}
+
+// fp32 (read by the tensor cores as tf32): boxes of box_rows x 32 columns.
+inline bool make_tmap_f32(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows,
+                          uint64_t depth, uint32_t box_rows, int rank) {
+    return make_tmap_sw128(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, cols, rows, depth,
+                           box_rows, rank);
 }
 
 }  // namespace tc

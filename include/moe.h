@@ -122,7 +122,10 @@ moe_status moe_check_config(const moe_config* cfg);
 
 /* Workspace bytes for cfg (0 if cfg is invalid).  The workspace holds the
    device status word, the dispatch scan state and the default metadata
-   arrays of moe_layer_forward.  Caller-allocated, 256-byte aligned; it need
+   arrays of moe_layer_forward, and for fp32 experts on the tensor cores the
+   tf32 split of the expert GEMMs' operands (2 x 4 bytes per element of the
+   input rows, both weight stacks and h: about 168 MB for T = 4096, d = 512,
+   E = 8, k = 2, d_ff = 1024).  Caller-allocated, 256-byte aligned; it need
    not be initialised, except that the status word should be zeroed once
    (moe_read_device_status does this). */
 size_t moe_workspace_size(const moe_config* cfg);
@@ -244,7 +247,13 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x, const int3
  *   [T, d_ff] scratch and shared_out [T,d] output; all NULL when
  *   n_shared == 0.
  * bf16 runs on the tensor cores (tcgen05, fp32 accumulation in tensor
- * memory, h rounded to bf16 once); fp32 runs as an fp32 FFMA grouped GEMM.
+ * memory, h rounded to bf16 once).  fp32 with d and d_ff multiples of 32 also
+ * runs on the tensor cores: each operand x is split into tf32 numbers
+ * hi = rn(x), lo = rn(x - hi) in the workspace (one elementwise pass over the
+ * input rows and weights, and h's split written beside h), and each product
+ * is a_lo*b_hi + a_hi*b_lo + a_hi*b_hi (kind::tf32, fp32 accumulation),
+ * within a few 2^-22 relative of the exact product; other fp32 shapes run as
+ * an fp32 FFMA grouped GEMM.
  * IDENTITY copies xp to yp (nothing if they are the same buffer).
  */
 moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* expert_offsets,
@@ -437,8 +446,8 @@ int moe_build_checked(void);
  * readings around a region counts the library's kernels enqueued in it, e.g.
  * the launches one moe_layer_forward makes for a configuration (route 1, or 2
  * when a batch's expert slices take more than one wave; dispatch 3; FFN 2 per
- * expert set; combine 1).  Host-side; no
- * synchronisation.
+ * expert set, 3 for fp32 experts on the tensor cores; combine 1).  Host-side;
+ * no synchronisation.
  */
 uint64_t moe_launch_count(void);
 

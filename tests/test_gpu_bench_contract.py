@@ -32,12 +32,14 @@ def test_bench_json_line():
     e2e = line["e2e"]
     assert e2e["value"] > 0 and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 4096 * 512 * 4 == e2e["d2h_bytes_per_step"]
-    # counted by the library: route, count, scan, place, up, down, combine
-    assert line["gpu_launches"] == 7 * 3 and line["launches_per_step"] == 7
+    # counted by the library: route, count, scan, place, tf32 split, up, down, combine
+    assert line["gpu_launches"] == 8 * 3 and line["launches_per_step"] == 8
     rf = line["roofline"]
     for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
         assert key in rf, key
-    assert rf["bound"] == "alu" and rf["achieved"] > 0 and rf["peak"] > 0
+    # the toy's fp32 experts run on the tensor cores (three tf32 products per product)
+    assert rf["bound"] == "tensor" and rf["achieved"] > 0 and rf["peak"] > 0
+    assert abs(rf["achieved"] - 3 * rf["fp32_TFLOP/s"]) < 1e-6 * rf["achieved"]
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
     assert set(line["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
     # per-kernel times come from the timed pass and add up to at most the step
