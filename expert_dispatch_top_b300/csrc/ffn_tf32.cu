@@ -26,9 +26,10 @@
 // one CTA per SM, warp 0 TMA producer, warp 1 TMEM allocator and single-lane
 // MMA issuer, warps 2-5 epilogue, two 256-column fp32 accumulators so the
 // epilogue of one tile overlaps the MMAs of the next, the ragged tile schedule
-// of gemm_tiles.cuh -- with a stage of A_hi, A_lo (128 x 32 fp32 each) and
-// B_hi, B_lo (256 x 32 fp32 each, 128-byte swizzle): 96 KB, two stages.  Per
-// K step of 8 the issuer runs the three tcgen05.mma kind::tf32 above, the
+// of gemm_tiles.cuh -- with a stage of A_hi, A_lo (128 x 16 fp32 each) and
+// B_hi, B_lo (256 x 16 fp32 each), rows of 64 bytes with the 64-byte swizzle:
+// 48 KB, four stages in 192 KB.  Per K step of 8 the issuer runs the three
+// tcgen05.mma kind::tf32 above, the
 // small terms first (M = 128, or 64 for a group's last tile of at most 64
 // rows; N = 256).  The epilogue applies the activation in fp32 (GELU in its erf
 // form, SwiGLU = silu(gate) * up) and stores fp32 rows through a padded
@@ -45,23 +46,39 @@ namespace {
 using namespace tc;
 using tiles::TileInfo;
 
-constexpr int BM = 128, BN = 256, BK = 32, STAGES = 2;  // BK fp32 = one 128-byte row
-constexpr int A_TILE = BM * BK * 4;                      // 16 KB
-constexpr int B_TILE = BN * BK * 4;                      // 32 KB
-constexpr int STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;     // A_hi, A_lo, B_hi, B_lo: 96 KB
+constexpr int BM = 128, BN = 256;
 constexpr int EPI_WARPS = 4;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int STG_PITCH = 144;  // staged row: 32 fp32 (128 bytes) + 16 pad (conflict-free)
 constexpr int STG_BYTES = EPI_WARPS * 32 * STG_PITCH;
 constexpr int MAX_GROUPS = tiles::kMaxGroups;
 constexpr int TABLE_BYTES = 128 + 4 * MAX_GROUPS * 4;  // barriers + flags, then 4 int tables
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_BYTES + TABLE_BYTES;
+constexpr int RING_BYTES = 192 * 1024;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int HALF_M = 64;  // tail tiles: accumulator rows in TMEM lanes 32*(r/16) + r%16
 constexpr uint32_t kIdesc = idesc_tf32(BM, BN);
 constexpr uint32_t kIdesc64 = idesc_tf32(HALF_M, BN);
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
-static_assert(2 * STAGES + 5 <= 14, "barriers fit below the abort flag");
+// K elements per stage: 16 fp32 (64-byte rows, 64-byte swizzle, 48 KB stages,
+// four in the ring) keep more loads in flight than 32 (128-byte rows, 96 KB
+// stages, two).
+constexpr int kStageK = 16;
+
+// Ring geometry for BK fp32 of K per stage (one swizzled shared-memory row).
+template <int BK>
+struct X3Ring {
+    static constexpr int SPAN = BK * 4;                              // bytes per row
+    static constexpr int A_TILE = BM * SPAN;                         // 8 or 16 KB
+    static constexpr int B_TILE = BN * SPAN;                         // 16 or 32 KB
+    static constexpr int STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;      // A_hi A_lo B_hi B_lo
+    static constexpr int STAGES = RING_BYTES / STAGE_BYTES;          // 4 or 2
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_BYTES + TABLE_BYTES;
+    static_assert(BK == 16 || BK == 32, "64- or 128-byte rows");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
+    static_assert(2 * STAGES + 5 <= 14, "barriers fit below the abort flag");
+    __device__ static uint64_t desc(uint32_t saddr) {
+        return BK == 32 ? sw128_desc(saddr) : sw64_desc(saddr);
+    }
+};
 
 struct X3Params {
     const int32_t* offsets;
@@ -121,17 +138,21 @@ __global__ void __launch_bounds__(256) tf32_split_kernel(Tf32SplitJob j0, Tf32Sp
     }
 }
 
+template <int BK>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_x3_kernel(const __grid_constant__ CUtensorMap tmAh,
                       const __grid_constant__ CUtensorMap tmAl,
                       const __grid_constant__ CUtensorMap tmBh,
                       const __grid_constant__ CUtensorMap tmBl, const X3Params p) {
+    using R = X3Ring<BK>;
+    constexpr int STAGES = R::STAGES, STAGE_BYTES = R::STAGE_BYTES;
+    constexpr int A_TILE = R::A_TILE, B_TILE = R::B_TILE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint8_t* stg = smem + STAGES * STAGE_BYTES;
     uint8_t* tbl = stg + STG_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(tbl);  // full[2] empty[2] accf[2] acce[2] drain
+    uint64_t* bars = reinterpret_cast<uint64_t*>(tbl);  // full[] empty[] accf[2] acce[2] drain
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tbl + 112);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tbl + 116);
     int* total_s = reinterpret_cast<int*>(tbl + 120);
@@ -243,11 +264,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t al = ah + A_TILE, bh = ah + 2 * A_TILE, bl = bh + B_TILE;
 #pragma unroll
                     for (int kk = 0; kk < BK / 8; ++kk) {
-                        const uint32_t o = (uint32_t)kk * 32;  // 8 fp32 of each 128-byte row
-                        mma_tf32(d_tmem, sw128_desc(al + o), sw128_desc(bh + o), idesc,
+                        const uint32_t o = (uint32_t)kk * 32;  // 8 fp32 of each row
+                        mma_tf32(d_tmem, R::desc(al + o), R::desc(bh + o), idesc,
                                  (kb | kk) != 0 ? 1u : 0u);
-                        mma_tf32(d_tmem, sw128_desc(ah + o), sw128_desc(bl + o), idesc, 1u);
-                        mma_tf32(d_tmem, sw128_desc(ah + o), sw128_desc(bh + o), idesc, 1u);
+                        mma_tf32(d_tmem, R::desc(ah + o), R::desc(bl + o), idesc, 1u);
+                        mma_tf32(d_tmem, R::desc(ah + o), R::desc(bh + o), idesc, 1u);
                     }
                     commit(empty0 + 8 * stage);
                     if (++stage == STAGES) {
@@ -353,7 +374,7 @@ inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) =
 
 int gemm_x3_supported(const GemmArgs& a) {
     if (a.dtype != MOE_DTYPE_F32) return 1;
-    if (a.K < BK || a.K % BK != 0 || a.N < 4 || a.N % 4 != 0) return 2;
+    if (a.K < kStageK || a.K % kStageK != 0 || a.N < 4 || a.N % 4 != 0) return 2;
     if (a.G < 1 || a.G > MAX_GROUPS) return 3;
     if (a.rows_cap >= (1ll << 31) || a.m_rows >= (1ll << 31) || a.K > (1 << 20) || a.N > (1 << 20))
         return 4;
@@ -367,6 +388,7 @@ int gemm_x3_supported(const GemmArgs& a) {
 }
 
 cudaError_t launch_gemm_x3(const GemmArgs& a, cudaStream_t s) {
+    using R = X3Ring<kStageK>;
     if (gemm_x3_supported(a) != 0) return cudaErrorInvalidValue;
     const int64_t rows_cap = a.offsets ? a.rows_cap : a.m_rows;
     if (rows_cap <= 0) return cudaSuccess;
@@ -375,10 +397,10 @@ cudaError_t launch_gemm_x3(const GemmArgs& a, cudaStream_t s) {
     const int G = a.offsets ? a.G : 1;
     const uint32_t b_box = gated ? 128 : BN;
     CUtensorMap tmAh, tmAl, tmBh, tmBl;
-    if (!make_tmap_f32(&tmAh, a.A, (uint64_t)a.K, (uint64_t)rows_cap, 1, BM, 2) ||
-        !make_tmap_f32(&tmAl, a.A_lo, (uint64_t)a.K, (uint64_t)rows_cap, 1, BM, 2) ||
-        !make_tmap_f32(&tmBh, a.B, (uint64_t)a.K, b_rows, (uint64_t)G, b_box, 3) ||
-        !make_tmap_f32(&tmBl, a.B_lo, (uint64_t)a.K, b_rows, (uint64_t)G, b_box, 3))
+    if (!make_tmap_f32(&tmAh, R::SPAN, a.A, (uint64_t)a.K, (uint64_t)rows_cap, 1, BM, 2) ||
+        !make_tmap_f32(&tmAl, R::SPAN, a.A_lo, (uint64_t)a.K, (uint64_t)rows_cap, 1, BM, 2) ||
+        !make_tmap_f32(&tmBh, R::SPAN, a.B, (uint64_t)a.K, b_rows, (uint64_t)G, b_box, 3) ||
+        !make_tmap_f32(&tmBl, R::SPAN, a.B_lo, (uint64_t)a.K, b_rows, (uint64_t)G, b_box, 3))
         return cudaErrorInvalidValue;
     X3Params p;
     p.offsets = a.offsets;
@@ -387,7 +409,7 @@ cudaError_t launch_gemm_x3(const GemmArgs& a, cudaStream_t s) {
     p.N = a.N;
     p.K = a.K;
     p.epi = a.epi;
-    p.num_kb = a.K / BK;
+    p.num_kb = a.K / kStageK;
     p.out_cols = gated ? 128 : BN;
     p.n_tiles = (a.N + p.out_cols - 1) / p.out_cols;
     p.kg_M = 0;
@@ -404,17 +426,17 @@ cudaError_t launch_gemm_x3(const GemmArgs& a, cudaStream_t s) {
     const int64_t tiles_bound = ((rows_cap + BM - 1) / BM + G) * p.n_tiles;
     int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
     if (grid < 1) grid = 1;
+    auto kern = tc_gemm_x3_kernel<kStageK>;
     // the shared-memory limit is a per-device function attribute: set it once per device
     constexpr int kDevs = 64;
     static bool attr_set[kDevs] = {};
     if (dev < 0 || dev >= kDevs || !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_x3_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, R::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kDevs) attr_set[dev] = true;
     }
-    return launch_pdl(tc_gemm_x3_kernel, dim3(grid), THREADS, (size_t)SMEM_BYTES, s, tmAh, tmAl, tmBh,
-                      tmBl, p);
+    return launch_pdl(kern, dim3(grid), THREADS, (size_t)R::SMEM_BYTES, s, tmAh, tmAl, tmBh, tmBl, p);
 }
 
 cudaError_t launch_tf32_split(const Tf32SplitJob* jobs, int njobs, cudaStream_t s) {

@@ -123,6 +123,17 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return d;
 }
 
+// The same for rows of 64 bytes with the 64-byte swizzle (8-row groups 512
+// bytes apart).
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;           // leading byte offset (unused with this swizzle)
+    d |= (uint64_t)(512 >> 4) << 32;  // stride byte offset: 8 rows x 64 B
+    d |= (uint64_t)1 << 46;           // descriptor version
+    d |= (uint64_t)4 << 61;           // SWIZZLE_64B
+    return d;
+}
+
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
 // N in bits 17-22 (N>>3), M in bits 24-28 (M>>4).
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
@@ -214,20 +225,22 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // Row-major matrix [rows, cols] of `dtype` (element size esize bytes) as a TMA
 // tensor map of rank 2, or a stack of `depth` such matrices as rank 3 (the
 // rank must match the loads the kernel issues: tma_load_2d or tma_load_3d),
-// with a box of box_rows x (128 / esize) columns -- one 128-byte row -- and the
-// 128-byte swizzle.  Returns false if the driver rejects it.
-inline bool make_tmap_sw128(CUtensorMap* tm, CUtensorMapDataType dtype, uint32_t esize,
-                            const void* base, uint64_t cols, uint64_t rows, uint64_t depth,
-                            uint32_t box_rows, int rank) {
+// with a box of box_rows x (span / esize) columns -- one shared-memory row of
+// span bytes -- and the span-byte swizzle (span 128 or 64).  Returns false if
+// the driver rejects it.
+inline bool make_tmap_swizzled(CUtensorMap* tm, CUtensorMapDataType dtype, uint32_t esize,
+                               uint32_t span, const void* base, uint64_t cols, uint64_t rows,
+                               uint64_t depth, uint32_t box_rows, int rank) {
     auto encode = encode_fn();
     if (!encode) return false;
-    if (rank != 2 && rank != 3) return false;
+    if ((rank != 2 && rank != 3) || (span != 128 && span != 64)) return false;
     cuuint64_t dims[3] = {cols, rows, depth};
     cuuint64_t strides[2] = {cols * esize, rows * cols * esize};
-    cuuint32_t box[3] = {128 / esize, box_rows, 1};
+    cuuint32_t box[3] = {span / esize, box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return encode(tm, dtype, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
@@ -235,15 +248,15 @@ inline bool make_tmap_sw128(CUtensorMap* tm, CUtensorMapDataType dtype, uint32_t
 // bf16: boxes of box_rows x 64 columns.
 inline bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows,
                            uint64_t depth, uint32_t box_rows, int rank) {
-    return make_tmap_sw128(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, depth,
-                           box_rows, rank);
+    return make_tmap_swizzled(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128, base, cols, rows, depth,
+                              box_rows, rank);
 }
 
-// fp32 (read by the tensor cores as tf32): boxes of box_rows x 32 columns.
-inline bool make_tmap_f32(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows,
-                          uint64_t depth, uint32_t box_rows, int rank) {
-    return make_tmap_sw128(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, cols, rows, depth,
-                           box_rows, rank);
+// fp32 (read by the tensor cores as tf32): boxes of box_rows x (span / 4) columns.
+inline bool make_tmap_f32(CUtensorMap* tm, uint32_t span, const void* base, uint64_t cols,
+                          uint64_t rows, uint64_t depth, uint32_t box_rows, int rank) {
+    return make_tmap_swizzled(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, span, base, cols, rows, depth,
+                              box_rows, rank);
 }
 
 }  // namespace tc
