@@ -49,7 +49,7 @@ struct Layout {
     size_t topk_idx, topk_gate, slot_row, row_token, expert_counts, offsets, rank_counts,
         rank_splits, n_dropped;
     // fp32 experts on the tensor cores: tf32 high and low parts of the GEMM operands
-    size_t x3_a_hi, x3_a_lo, x3_wu_hi, x3_wu_lo, x3_wd_hi, x3_wd_lo, x3_h_hi, x3_h_lo;
+    size_t x3_a_hi, x3_a_lo, x3_wu_hi, x3_wu_lo, x3_wd_hi, x3_wd_lo, x3_h_lo;
     size_t total;
 };
 
@@ -97,8 +97,7 @@ Layout layout_of(const moe_config* c) {
     o = align_up(o + (size_t)c->R * c->R * 4);
     L.n_dropped = o;
     o = align_up(o + 4);
-    L.x3_a_hi = L.x3_a_lo = L.x3_wu_hi = L.x3_wu_lo = L.x3_wd_hi = L.x3_wd_lo = L.x3_h_hi =
-        L.x3_h_lo = o;
+    L.x3_a_hi = L.x3_a_lo = L.x3_wu_hi = L.x3_wu_lo = L.x3_wd_hi = L.x3_wd_lo = L.x3_h_lo = o;
     if (ffn_uses_x3(c)) {
         // rows of A: the routed rows, or the shared expert's T rows (the passes
         // run one after the other and reuse these sections)
@@ -107,10 +106,10 @@ Layout layout_of(const moe_config* c) {
         const size_t up_rows = (size_t)(c->act == MOE_ACT_SWIGLU ? 2 : 1) * c->d_ff;
         const size_t a = arows * c->d * 4, wu = (size_t)c->E * up_rows * c->d * 4;
         const size_t wd = (size_t)c->E * c->d * c->d_ff * 4, h = arows * c->d_ff * 4;
-        size_t* sec[8] = {&L.x3_a_hi, &L.x3_a_lo, &L.x3_wu_hi, &L.x3_wu_lo,
-                          &L.x3_wd_hi, &L.x3_wd_lo, &L.x3_h_hi, &L.x3_h_lo};
-        const size_t len[8] = {a, a, wu, wu, wd, wd, h, h};
-        for (int i = 0; i < 8; ++i) {
+        size_t* sec[7] = {&L.x3_a_hi, &L.x3_a_lo, &L.x3_wu_hi, &L.x3_wu_lo,
+                          &L.x3_wd_hi, &L.x3_wd_lo, &L.x3_h_lo};
+        const size_t len[7] = {a, a, wu, wu, wd, wd, h};
+        for (int i = 0; i < 7; ++i) {
             *sec[i] = o;
             o = align_up(o + len[i]);
         }
@@ -274,14 +273,13 @@ moe_status ffn_impl(const moe_config* c, const void* xp, const int32_t* offsets,
         dn.epi = EPI_NONE;
         if (x3) {
             // both GEMMs read the tf32 split of their operands; the up projection
-            // stores h and its split, which the down projection reads
+            // stores h split (high part in h, low part in the workspace), which the
+            // down projection reads
             u.A = at<float>(ws, L.x3_a_hi);
             u.A_lo = at<float>(ws, L.x3_a_lo);
             u.B = at<float>(ws, L.x3_wu_hi);
             u.B_lo = at<float>(ws, L.x3_wu_lo);
-            u.out_hi = at<float>(ws, L.x3_h_hi);
             u.out_lo = at<float>(ws, L.x3_h_lo);
-            dn.A = u.out_hi;
             dn.A_lo = u.out_lo;
             dn.B = at<float>(ws, L.x3_wd_hi);
             dn.B_lo = at<float>(ws, L.x3_wd_lo);

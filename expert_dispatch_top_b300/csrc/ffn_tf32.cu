@@ -17,15 +17,17 @@
 //
 // The split: launch_tf32_split writes hi and lo of the expert inputs and of
 // both weight stacks into the workspace in one elementwise pass, and the up
-// projection's epilogue writes h together with its split, which the down
+// projection's epilogue writes h already split -- its tf32 high part into the
+// caller's h (scratch), its low part into the workspace -- which the down
 // projection reads.  Since the tensor cores only ever see numbers exact in
 // tf32, the result does not depend on how the hardware treats the low 13 bits
 // of an fp32 operand.
 //
 // Kernel: the structure of the bf16 grouped GEMM (ffn_tc.cu) -- persistent,
 // one CTA per SM, warp 0 TMA producer, warp 1 TMEM allocator and single-lane
-// MMA issuer, warps 2-5 epilogue, two 256-column fp32 accumulators so the
-// epilogue of one tile overlaps the MMAs of the next, the ragged tile schedule
+// MMA issuer, warps 2-9 epilogue (two per TMEM lane quarter, each on half of
+// the tile's columns), two 256-column fp32 accumulators so the epilogue of one
+// tile overlaps the MMAs of the next, the ragged tile schedule
 // of gemm_tiles.cuh -- with a stage of A_hi, A_lo (128 x 16 fp32 each) and
 // B_hi, B_lo (256 x 16 fp32 each), rows of 64 bytes with the 64-byte swizzle:
 // 48 KB, four stages in 192 KB.  Per K step of 8 the issuer runs the three
@@ -47,9 +49,12 @@ using namespace tc;
 using tiles::TileInfo;
 
 constexpr int BM = 128, BN = 256;
-constexpr int EPI_WARPS = 4;
+// Eight epilogue warps: two per TMEM lane quarter, each taking half of a tile's
+// output columns (the up projection's epilogue -- activation and three fp32
+// outputs per element -- outlasts the tile's MMAs with four).
+constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
-constexpr int STG_PITCH = 144;  // staged row: 32 fp32 (128 bytes) + 16 pad (conflict-free)
+constexpr int STG_PITCH = 80;  // staged row: 16 fp32 (64 bytes) + 16 pad (conflict-free writes)
 constexpr int STG_BYTES = EPI_WARPS * 32 * STG_PITCH;
 constexpr int MAX_GROUPS = tiles::kMaxGroups;
 constexpr int TABLE_BYTES = 128 + 4 * MAX_GROUPS * 4;  // barriers + flags, then 4 int tables
@@ -89,9 +94,8 @@ struct X3Params {
     int out_cols;   // output columns per tile (128 SwiGLU, 256 otherwise)
     int kg_M, band;  // tile decoder: row-offset mode without bands (both 0)
     uint64_t wait_ns;
-    float* out;
-    float* out_hi;  // non-null: out's split is stored as well (the up projection's h)
-    float* out_lo;
+    float* out;     // the output, or with out_lo its tf32 high part
+    float* out_lo;  // non-null: the output's tf32 low part (the up projection's h)
     uint32_t* status;
 };
 
@@ -291,9 +295,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ---------------- epilogue ----------------
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int q = warp & 3;               // TMEM lane quarter this warp may access
+        const int ch = p.out_cols / 64;       // 32-column chunks per warp
+        const int c0 = ((warp - 2) >> 2) * ch;  // first chunk: warps 2-5 the left half, 6-9 the right
         uint8_t* my_stg = stg + (warp - 2) * (32 * STG_PITCH);
-        const int nout = p.out_hi ? 3 : 1;
+        const bool split = p.out_lo != nullptr;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -307,8 +313,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             const bool half = ti.rows <= HALF_M;  // M = 64: rows 16q + lane, lane < 16
-            const int gc0 = ti.n_tile * p.out_cols + (lane & 7) * 4;
-            for (int c = 0; c < p.out_cols / 32; ++c) {
+            const int gc0 = ti.n_tile * p.out_cols + (lane & 3) * 4;
+            for (int c = c0; c < c0 + ch; ++c) {
                 float v[32];
                 tmem_ld32(tbase + (uint32_t)(c * 32), v);
                 if (p.epi == EPI_SWIGLU) {
@@ -320,36 +326,39 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = gelu_erf_f(v[i]);
                 }
-                const int gc = gc0 + c * 32;
-                for (int o = 0; o < nout; ++o) {
-                    // o = 0: the value; 1: its tf32 high part; 2: its low part
-                    float* dst = o == 0 ? p.out : o == 1 ? p.out_hi : p.out_lo;
-                    uint8_t* srow = my_stg + lane * STG_PITCH;
+                for (int o = 0; o < (split ? 2 : 1); ++o) {
+                    // o = 0: the value, or its tf32 high part; 1: its low part
+                    float* dst = o == 0 ? p.out : p.out_lo;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        uint32_t w[4];
+                    for (int part = 0; part < 2; ++part) {  // 16 columns at a time
+                        uint8_t* srow = my_stg + lane * STG_PITCH;
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float x = v[4 * i + j];
-                            const float hi = rn_tf32(x);
-                            w[j] = __float_as_uint(o == 0 ? x : o == 1 ? hi : tf32_lo(x, hi));
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float x = v[16 * part + 4 * i + j];
+                                const float hi = rn_tf32(x);
+                                w[j] = __float_as_uint(!split ? x : o == 0 ? hi : tf32_lo(x, hi));
+                            }
+                            *reinterpret_cast<uint4*>(srow + 16 * i) = make_uint4(w[0], w[1], w[2], w[3]);
                         }
-                        *reinterpret_cast<uint4*>(srow + 16 * i) = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                    __syncwarp();
-                    // 32 rows x 128 bytes: 8 lanes per row, 4 rows per pass
+                        __syncwarp();
+                        // 32 rows x 64 bytes: 4 lanes per row, 8 rows per pass
+                        const int gc = gc0 + c * 32 + part * 16;
 #pragma unroll
-                    for (int it = 0; it < 8; ++it) {
-                        const int r = it * 4 + (lane >> 3);
-                        // row inside the tile of staged row r (TMEM lane q*32 + r)
-                        const int lr = half ? (r < 16 ? q * 16 + r : BM) : q * 32 + r;
-                        if (lr < ti.rows && gc < p.N) {
-                            const uint4 w = *reinterpret_cast<const uint4*>(my_stg + r * STG_PITCH +
-                                                                            (lane & 7) * 16);
-                            st_v4(dst + (int64_t)(ti.row0 + lr) * p.N + gc, w);
+                        for (int it = 0; it < 4; ++it) {
+                            const int r = it * 8 + (lane >> 2);
+                            // row inside the tile of staged row r (TMEM lane q*32 + r)
+                            const int lr = half ? (r < 16 ? q * 16 + r : BM) : q * 32 + r;
+                            if (lr < ti.rows && gc < p.N) {
+                                const uint4 w = *reinterpret_cast<const uint4*>(
+                                    my_stg + r * STG_PITCH + (lane & 3) * 16);
+                                st_v4(dst + (int64_t)(ti.row0 + lr) * p.N + gc, w);
+                            }
                         }
+                        __syncwarp();
                     }
-                    __syncwarp();
                 }
             }
             fence_before();
@@ -379,10 +388,10 @@ int gemm_x3_supported(const GemmArgs& a) {
     if (a.rows_cap >= (1ll << 31) || a.m_rows >= (1ll << 31) || a.K > (1 << 20) || a.N > (1 << 20))
         return 4;
     if (!al16(a.A) || !al16(a.A_lo) || !al16(a.B) || !al16(a.B_lo) || !al16(a.out) ||
-        !al16(a.out_hi) || !al16(a.out_lo))
+        !al16(a.out_lo))
         return 5;
     if (a.b_mn || a.kgrouped || a.stall_kb >= 0) return 6;
-    if (!a.A || !a.A_lo || !a.B || !a.B_lo || !a.out || (a.out_hi == nullptr) != (a.out_lo == nullptr))
+    if (!a.A || !a.A_lo || !a.B || !a.B_lo || !a.out)
         return 7;
     return 0;
 }
@@ -416,7 +425,6 @@ cudaError_t launch_gemm_x3(const GemmArgs& a, cudaStream_t s) {
     p.band = 0;
     p.wait_ns = a.wait_ns ? a.wait_ns : kWaitTimeoutNs;
     p.out = static_cast<float*>(a.out);
-    p.out_hi = static_cast<float*>(a.out_hi);
     p.out_lo = static_cast<float*>(a.out_lo);
     p.status = a.status;
 

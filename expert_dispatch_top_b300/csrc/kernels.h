@@ -121,10 +121,11 @@ struct GemmArgs {
     uint64_t wait_ns = 0;
     // fp32 on the tensor cores (3xTF32 kernel): A and B are the tf32 high parts of
     // the fp32 operands and A_lo / B_lo their low parts (same shapes, see
-    // launch_tf32_split); out_hi / out_lo, if non-null, receive the split of out.
+    // launch_tf32_split).  out_lo non-null: the output is stored split, its tf32
+    // high part in out and its low part in out_lo (the up projection's h, which
+    // the down projection reads as its A and A_lo).
     const void* A_lo = nullptr;
     const void* B_lo = nullptr;
-    void* out_hi = nullptr;
     void* out_lo = nullptr;
 };
 cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t s);

@@ -124,8 +124,8 @@ moe_status moe_check_config(const moe_config* cfg);
    device status word, the dispatch scan state and the default metadata
    arrays of moe_layer_forward, and for fp32 experts on the tensor cores the
    tf32 split of the expert GEMMs' operands (2 x 4 bytes per element of the
-   input rows, both weight stacks and h: about 168 MB for T = 4096, d = 512,
-   E = 8, k = 2, d_ff = 1024).  Caller-allocated, 256-byte aligned; it need
+   input rows and both weight stacks, 4 bytes per element of h: about 134 MB
+   for T = 4096, d = 512, E = 8, k = 2, d_ff = 1024).  Caller-allocated, 256-byte aligned; it need
    not be initialised, except that the status word should be zeroed once
    (moe_read_device_status does this). */
 size_t moe_workspace_size(const moe_config* cfg);
@@ -239,7 +239,8 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x, const int3
  *   host synchronisation).  w_up [E, d_ff, d] (GELU) or [E, 2*d_ff, d]
  *   (SwiGLU: the d_ff gate rows first, then the d_ff up rows); w_down
  *   [E, d, d_ff].  All weights are [out, in] row-major.
- *   h [max_rows, d_ff]: scratch for the hidden activations (act dtype).
+ *   h [max_rows, d_ff]: scratch for the hidden activations (act dtype; for
+ *   fp32 experts on the tensor cores, the activations' tf32 high parts).
  *   yp [max_rows, d]: expert outputs, same row layout as xp.  Rows past
  *   offsets[E] are left untouched.
  *   Shared expert (cfg->n_shared == 1): shared_x [T,d] (normally x),
@@ -250,7 +251,8 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x, const int3
  * memory, h rounded to bf16 once).  fp32 with d and d_ff multiples of 32 also
  * runs on the tensor cores: each operand x is split into tf32 numbers
  * hi = rn(x), lo = rn(x - hi) in the workspace (one elementwise pass over the
- * input rows and weights, and h's split written beside h), and each product
+ * input rows and weights; h is stored split, hi in h and lo in the
+ * workspace), and each product
  * is a_lo*b_hi + a_hi*b_lo + a_hi*b_hi (kind::tf32, fp32 accumulation),
  * within a few 2^-22 relative of the exact product; other fp32 shapes run as
  * an fp32 FFMA grouped GEMM.
