@@ -150,6 +150,14 @@ def test_ffn_fp32_tensor_cores_keep_both_cross_terms(act):
     assert worst < 2e-5, worst
 
 
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_ffn_fp32_tensor_cores_smallest_shape_and_no_rows(act):
+    """d = d_ff = 32 (two 16-column K stages, 32 of a tile's 256 columns stored)
+    and a call whose experts received no rows."""
+    _run_ffn([3, 0, 130], 32, 32, act, torch.float32, seed=21, values="normal")
+    _run_ffn([0, 0], 64, 64, act, torch.float32, seed=22, rows_cap=40)
+
+
 def test_ffn_fp32_tensor_cores_shared_expert_and_many_groups():
     counts = [int(c) for c in torch.randint(0, 40, (256,), generator=torch.Generator().manual_seed(9))]
     _run_ffn(counts, 64, 64, "swiglu", torch.float32, seed=12, rows_cap=sum(counts) + 70)
