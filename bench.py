@@ -95,9 +95,9 @@ TF32_PER_BF16 = 1.1 / 2.25
 
 
 def ffn_on_tf32(w):
-    """fp32 experts whose d and d_ff are multiples of 32 run on the tensor cores
+    """fp32 experts whose d and d_ff are multiples of 16 run on the tensor cores
     as three tf32 products per fp32 product (split pass + up + down)."""
-    return w.dtype == "f32" and w.act != "identity" and w.d % 32 == 0 and w.d_ff % 32 == 0
+    return w.dtype == "f32" and w.act != "identity" and w.d % 16 == 0 and w.d_ff % 16 == 0
 
 
 class ClockSampler:

@@ -54,11 +54,12 @@ struct Layout {
 };
 
 // fp32 experts whose contraction lengths (d for the up projection, d_ff for
-// the down projection) are multiples of 32 run on the tensor cores as three
-// tf32 products (ffn_tf32.cu); other fp32 shapes run on FFMA (ffn_simt.cu).
+// the down projection) are multiples of 16 -- the 3xTF32 kernel's K per stage
+// -- run on the tensor cores as three tf32 products (ffn_tf32.cu); other fp32
+// shapes run on FFMA (ffn_simt.cu).
 inline bool ffn_uses_x3(const moe_config* c) {
-    return c->act_dtype == MOE_DTYPE_F32 && c->act != MOE_ACT_IDENTITY && c->d % 32 == 0 &&
-           c->d_ff % 32 == 0;
+    return c->act_dtype == MOE_DTYPE_F32 && c->act != MOE_ACT_IDENTITY && c->d % 16 == 0 &&
+           c->d_ff % 16 == 0;
 }
 
 Layout layout_of(const moe_config* c) {

@@ -248,7 +248,7 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* x, const int3
  *   [T, d_ff] scratch and shared_out [T,d] output; all NULL when
  *   n_shared == 0.
  * bf16 runs on the tensor cores (tcgen05, fp32 accumulation in tensor
- * memory, h rounded to bf16 once).  fp32 with d and d_ff multiples of 32 also
+ * memory, h rounded to bf16 once).  fp32 with d and d_ff multiples of 16 also
  * runs on the tensor cores: each operand x is split into tf32 numbers
  * hi = rn(x), lo = rn(x - hi) in the workspace (one elementwise pass over the
  * input rows and weights; h is stored split, hi in h and lo in the

@@ -1,7 +1,7 @@
 """GPU parity of Step 3 (expert FFN, grouped GEMM) against the oracle:
 ragged groups (empty, 1 row, tile edges, several tiles), GELU and SwiGLU,
 the bf16 tensor-core path, the fp32 tensor-core path (three tf32 products per
-fp32 product; d and d_ff multiples of 32) and the fp32 FFMA path (other fp32
+fp32 product; d and d_ff multiples of 16) and the fp32 FFMA path (other fp32
 shapes), plus the shared expert."""
 import pytest
 import torch
@@ -119,10 +119,13 @@ def test_ffn_bf16_shared_expert():
     _run_ffn([100, 60, 0, 96], 256, 128, "swiglu", torch.bfloat16, seed=4, shared=True)
 
 
-# d = 68, f = 36: FFMA path; the others: tensor cores (three tf32 products)
+# d = 68, f = 36 and d = 64, f = 36: FFMA path; the others: tensor cores (three
+# tf32 products), d = 48, f = 80 with contraction lengths of 3 and 5 K stages
 @pytest.mark.parametrize("act", ["gelu", "swiglu"])
 @pytest.mark.parametrize("counts,d,f", [
     ([0, 1, 63, 64, 65, 200], 68, 36),
+    ([5, 130], 64, 36),
+    ([0, 1, 63, 64, 65, 200], 48, 80),
     ([1024, 1000], 512, 1024),
     ([0, 1, 63, 64, 65, 127, 128, 129, 300], 128, 96),
     ([40, 0, 0, 250], 256, 416),
@@ -152,9 +155,9 @@ def test_ffn_fp32_tensor_cores_keep_both_cross_terms(act):
 
 @pytest.mark.parametrize("act", ["gelu", "swiglu"])
 def test_ffn_fp32_tensor_cores_smallest_shape_and_no_rows(act):
-    """d = d_ff = 32 (two 16-column K stages, 32 of a tile's 256 columns stored)
+    """d = d_ff = 16 (one 16-column K stage, 16 of a tile's 256 columns stored)
     and a call whose experts received no rows."""
-    _run_ffn([3, 0, 130], 32, 32, act, torch.float32, seed=21, values="normal")
+    _run_ffn([3, 0, 130], 16, 16, act, torch.float32, seed=21, values="normal")
     _run_ffn([0, 0], 64, 64, act, torch.float32, seed=22, rows_cap=40)
 
 
