@@ -27,15 +27,15 @@
 // one CTA per SM, warp 0 TMA producer, warp 1 TMEM allocator and single-lane
 // MMA issuer, warps 2-9 epilogue (two per TMEM lane quarter, each on half of
 // the tile's columns), two 256-column fp32 accumulators so the epilogue of one
-// tile overlaps the MMAs of the next, the ragged tile schedule
-// of gemm_tiles.cuh -- with a stage of A_hi, A_lo (128 x 16 fp32 each) and
-// B_hi, B_lo (256 x 16 fp32 each), rows of 64 bytes with the 64-byte swizzle:
-// 48 KB, four stages in 192 KB.  Per K step of 8 the issuer runs the three
-// tcgen05.mma kind::tf32 above, the
-// small terms first (M = 128, or 64 for a group's last tile of at most 64
-// rows; N = 256).  The epilogue applies the activation in fp32 (GELU in its erf
-// form, SwiGLU = silu(gate) * up) and stores fp32 rows through a padded
-// shared-memory transpose as coalesced 128-byte segments.  Every mbarrier
+// tile overlaps the MMAs of the next, the ragged tile schedule of
+// gemm_tiles.cuh -- with a stage of A_hi, A_lo (128 x 16 fp32 each) and B_hi,
+// B_lo (256 x 16 fp32 each), rows of 64 bytes with the 64-byte swizzle: 48 KB,
+// four stages in 192 KB.  Per K step of 8 the issuer runs the three
+// tcgen05.mma kind::tf32 above, the small terms first (M = 128, or 64 for a
+// group's last tile of at most 64 rows; N = 256).  The epilogue applies the
+// activation in fp32 (GELU in its erf form, SwiGLU = silu(gate) * up) and
+// stores fp32 rows through a padded shared-memory transpose as coalesced
+// 64-byte segments.  Every mbarrier
 // wait is bounded (MOE_DEV_GEMM_TIMEOUT, abort flag, bounded MMA drain, TMEM
 // freed before returning).
 #include "gemm_tiles.cuh"
@@ -50,8 +50,8 @@ using tiles::TileInfo;
 
 constexpr int BM = 128, BN = 256;
 // Eight epilogue warps: two per TMEM lane quarter, each taking half of a tile's
-// output columns (the up projection's epilogue -- activation and three fp32
-// outputs per element -- outlasts the tile's MMAs with four).
+// output columns (with four, the up projection's epilogue -- the activation and
+// two fp32 output streams per element -- outlasted the tile's MMAs).
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int STG_PITCH = 80;  // staged row: 16 fp32 (64 bytes) + 16 pad (conflict-free writes)
