@@ -11,9 +11,10 @@
 //     hi = rn_tf32(x),   lo = rn_tf32(x - hi)          (x - hi is exact),
 // with |x - hi| <= 2^-11 |x| and |x - hi - lo| <= 2^-22 |x|, and
 //     a . b  ~=  a_lo . b_hi  +  a_hi . b_lo  +  a_hi . b_hi
-// drops only a_lo . b_lo (<= 2^-22 |a b|) and the two lo roundings: a few
-// 2^-22 relative per product, against fp32's own 2^-24 per rounding.  Products
-// of tf32 numbers (11-bit significands) are exact in the fp32 accumulator.
+// drops only a_lo . b_lo and the two lo roundings, each at most 2^-22 |a b|:
+// under 3 * 2^-22 relative per product, against fp32's own 2^-24 per rounding.
+// The product of two tf32 numbers (11-bit significands) is exact in fp32; the
+// accumulation rounds as an fp32 sum does.
 //
 // The split: launch_tf32_split writes hi and lo of the expert inputs and of
 // both weight stacks into the workspace in one elementwise pass, and the up
