@@ -7,10 +7,13 @@
 //   3. d_pre, h from pre and dh            (elementwise activation backward)
 //   4. d_xp = d_pre . W_up                 (grouped GEMM on W_up^T)
 //   5. dW_down[e] = sum over rows d_yp^T h, dW_up[e] = sum over rows d_pre^T xp
-// The GEMMs of steps 1, 2 and 4 run on the forward's grouped GEMM.  bf16: on
+// The GEMMs of steps 1, 2 and 4 run on the forward's grouped GEMMs.  bf16: on
 // the tensor cores, steps 2 and 4 reading the weights as stored through the
-// GEMM's MN-major B mode; fp32: FFMA, with the weights transposed once per
-// call by a batched tiled transpose.  Step 5 sums over each expert's ragged
+// GEMM's MN-major B mode; fp32: with the weights transposed once per call by a
+// batched tiled transpose, on the tensor cores as three tf32 products per
+// product when d and d_ff are multiples of 16 (the operands split into tf32
+// high and low parts in the scratch: xp, d_yp and both weights before step 1,
+// d_pre after step 3), else on FFMA.  Step 5 sums over each expert's ragged
 // rows: bf16 runs it on the tensor cores in the grouped GEMM's K-grouped mode
 // over transposed, 64-row-padded copies of the activations (that mode also
 // writes the zero gradients of experts without rows); fp32 runs a tiled FFMA
@@ -264,6 +267,12 @@ size_t ffn_backward_scratch_bytes(int64_t rows_cap, int E, int d, int f, int gat
         n += al((size_t)E * up * d * eb);  // W_up^T
         n += al((size_t)E * d * f * eb);   // W_down^T
         if (weight_grads) n += al((size_t)rows_cap * f * eb);  // h
+        if (d % 16 == 0 && f % 16 == 0) {
+            // tf32 high and low parts: xp, W_up, d_yp, W_down^T, d_pre, W_up^T
+            const size_t part[6] = {(size_t)rows_cap * d, (size_t)E * up * d, (size_t)rows_cap * d,
+                                    (size_t)E * f * d, (size_t)rows_cap * up, (size_t)E * d * up};
+            for (int i = 0; i < 6; ++i) n += 2 * al(part[i] * 4);
+        }
     } else if (weight_grads) {
         n += al(P * f * 2);     // h, padded rows
         n += al(P * up * 2);    // d_pre, padded rows
@@ -279,6 +288,7 @@ cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
     const int eb = a.dtype == MOE_DTYPE_F32 ? 4 : 2;
     const bool tc = eb == 2;
     const bool wg = a.d_w_up || a.d_w_down;
+    const bool x3 = !tc && a.d % 16 == 0 && a.f % 16 == 0;  // fp32 on the tensor cores
     if (tc && a.E > 256) return cudaErrorInvalidValue;
     auto al = [](size_t v) { return (v + 255) / 256 * 256; };
     const size_t P = (size_t)((a.rows_cap + 64 * (int64_t)a.E + 63) / 64 * 64);
@@ -303,12 +313,42 @@ cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
         xp_pad = take(P * a.d * 2);
         dyp_pad = take(P * a.d * 2);
     }
+    // fp32 on the tensor cores: high / low tf32 parts of each GEMM operand
+    enum { XP, WU, DYP, WDT, DPRE, WUT };
+    void *hi[6] = {}, *lo[6] = {};
+    if (x3) {
+        const size_t part[6] = {(size_t)a.rows_cap * a.d, (size_t)a.E * up * a.d,
+                                (size_t)a.rows_cap * a.d, (size_t)a.E * a.f * a.d,
+                                (size_t)a.rows_cap * up, (size_t)a.E * a.d * up};
+        for (int i = 0; i < 6; ++i) {
+            hi[i] = take(part[i] * 4);
+            lo[i] = take(part[i] * 4);
+        }
+    }
     cudaError_t e;
     if (!tc) {
         // transposed weights: W_up [E, up, d] -> [E, d, up]; W_down [E, d, f] -> [E, f, d]
         if ((e = transpose_batched<float>(a.w_up, w_upT, a.E, up, a.d, s)) != cudaSuccess) return e;
         if ((e = transpose_batched<float>(a.w_down, w_downT, a.E, a.d, a.f, s)) != cudaSuccess)
             return e;
+    }
+    // the split of n fp32 values at src into operand op's high / low parts
+    auto job = [&](int op, const void* src, int64_t n) {
+        Tf32SplitJob j;
+        j.src = static_cast<const float*>(src);
+        j.hi = static_cast<float*>(hi[op]);
+        j.lo = static_cast<float*>(lo[op]);
+        j.n = n;
+        return j;
+    };
+    if (x3) {
+        const Tf32SplitJob inputs[3] = {job(XP, a.xp, a.rows_cap * a.d),
+                                        job(WU, a.w_up, (int64_t)a.E * up * a.d),
+                                        job(DYP, a.d_yp, a.rows_cap * a.d)};
+        if ((e = launch_tf32_split(inputs, 3, s)) != cudaSuccess) return e;
+        const Tf32SplitJob transposed[2] = {job(WDT, w_downT, (int64_t)a.E * a.f * a.d),
+                                            job(WUT, w_upT, (int64_t)a.E * a.d * up)};
+        if ((e = launch_tf32_split(transposed, 2, s)) != cudaSuccess) return e;
     }
     // out = A . B^T with B [E, N, K] (b_mn = 0), or out = A . B with B [E, K, N] (b_mn = 1)
     auto gemm = [&](const void* A, const void* B, void* out, int N, int K, int b_mn) {
@@ -328,8 +368,30 @@ cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
         g.b_mn = b_mn;
         return tc ? launch_gemm_tc(g, s) : launch_gemm_simt(g, s);
     };
-    if ((e = gemm(a.xp, a.w_up, pre, up, a.d, 0)) != cudaSuccess) return e;  // 1
-    if ((e = gemm(a.d_yp, tc ? a.w_down : w_downT, dh, a.f, a.d, tc)) != cudaSuccess) return e;  // 2
+    // the same on the tensor cores from split fp32 operands (K-major B)
+    auto gemm3 = [&](int ia, int ib, void* out, int N, int K) {
+        GemmArgs g;
+        g.A = hi[ia];
+        g.A_lo = lo[ia];
+        g.B = hi[ib];
+        g.B_lo = lo[ib];
+        g.out = out;
+        g.offsets = a.offsets;
+        g.rows_cap = a.rows_cap;
+        g.m_rows = 0;
+        g.G = a.E;
+        g.N = N;
+        g.K = K;
+        g.epi = EPI_NONE;
+        g.dtype = a.dtype;
+        g.status = a.status;
+        return launch_gemm_x3(g, s);
+    };
+    e = x3 ? gemm3(XP, WU, pre, up, a.d) : gemm(a.xp, a.w_up, pre, up, a.d, 0);  // 1
+    if (e != cudaSuccess) return e;
+    e = x3 ? gemm3(DYP, WDT, dh, a.f, a.d)
+           : gemm(a.d_yp, tc ? a.w_down : w_downT, dh, a.f, a.d, tc);  // 2
+    if (e != cudaSuccess) return e;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -355,7 +417,13 @@ cudaError_t launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
             static_cast<__nv_bfloat16*>(d_pre), nullptr, a.offsets, a.E, a.f, gated, a.rows_cap);
     }
     if ((e = noted_launch()) != cudaSuccess) return e;
-    if ((e = gemm(d_pre, tc ? a.w_up : w_upT, a.d_xp, a.d, up, tc)) != cudaSuccess) return e;  // 4
+    if (x3) {
+        const Tf32SplitJob dp = job(DPRE, d_pre, a.rows_cap * up);
+        if ((e = launch_tf32_split(&dp, 1, s)) != cudaSuccess) return e;
+    }
+    e = x3 ? gemm3(DPRE, WUT, a.d_xp, a.d, up)
+           : gemm(d_pre, tc ? a.w_up : w_upT, a.d_xp, a.d, up, tc);  // 4
+    if (e != cudaSuccess) return e;
     if (!wg) return cudaSuccess;
     // 5: weight gradients
     if (!tc) {

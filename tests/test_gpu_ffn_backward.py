@@ -1,7 +1,9 @@
 """GPU parity of the expert-FFN backward (moe_expert_ffn_backward) against the
 oracle: input gradient d_xp and both weight gradients, GELU and SwiGLU, the
 bf16 tensor-core path (including the K-grouped weight-gradient GEMM) and the
-fp32 FFMA path, over ragged groups (empty, one row, tile edges, several tiles).
+fp32 paths (input-gradient GEMMs on the tensor cores as three tf32 products
+per product when d and d_ff are multiples of 16, else FFMA), over ragged
+groups (empty, one row, tile edges, several tiles).
 
 Tolerances.  d_xp: per row, relative to the row's max |ref| (as the forward
 FFN test): bf16 2e-2 -- pre, dh and d_pre are each rounded to bf16 once
@@ -43,16 +45,22 @@ def _offsets(counts):
     return offs
 
 
-def _inputs(counts, d, f, act, dtype, seed, sparse_rows=None):
+def _inputs(counts, d, f, act, dtype, seed, sparse_rows=None, normal=False):
     E = len(counts)
     offs = _offsets(counts)
     N = int(offs[-1])
     rows_up = 2 * f if act == "swiglu" else f
     g = W._gen(seed, "cpu")
-    w_up = W._grid_normal((E, rows_up, d), 0.08, 2.0 ** -9, 0.125, g, "cpu").to(dtype)
-    w_dn = W._grid_normal((E, d, f), 0.08, 2.0 ** -9, 0.125, g, "cpu").to(dtype)
-    xp = W._grid_int((max(N, 1), d), -8, 8, 8.0, g, "cpu").to(dtype)
-    d_yp = W._grid_normal((max(N, 1), d), 0.5, 2.0 ** -9, 4.0, g, "cpu").to(dtype)
+    if normal:  # arbitrary fp32 values: every operand has a non-zero tf32 low part
+        w_up = torch.randn((E, rows_up, d), generator=g) * 0.08
+        w_dn = torch.randn((E, d, f), generator=g) * 0.08
+        xp = torch.randn((max(N, 1), d), generator=g)
+        d_yp = torch.randn((max(N, 1), d), generator=g) * 0.5
+    else:
+        w_up = W._grid_normal((E, rows_up, d), 0.08, 2.0 ** -9, 0.125, g, "cpu").to(dtype)
+        w_dn = W._grid_normal((E, d, f), 0.08, 2.0 ** -9, 0.125, g, "cpu").to(dtype)
+        xp = W._grid_int((max(N, 1), d), -8, 8, 8.0, g, "cpu").to(dtype)
+        d_yp = W._grid_normal((max(N, 1), d), 0.5, 2.0 ** -9, 4.0, g, "cpu").to(dtype)
     if sparse_rows is not None:
         keep = torch.zeros(max(N, 1), dtype=torch.bool)
         keep[sparse_rows] = True
@@ -108,6 +116,26 @@ def test_ffn_backward(dtype, act, counts, d, f):
     n = int(offs[-1])
     if d_xp.shape[0] > n:
         assert torch.all(d_xp[n:].float().cpu() == 5.0)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("counts,d,f,normal", [
+    ([0, 1, 63, 64, 65, 200], 68, 36, False),   # FFMA (d, d_ff not multiples of 16)
+    ([1, 64, 65, 300, 0, 129], 128, 96, True),  # tensor cores, non-dyadic operands
+    ([40, 0, 250], 48, 80, True),
+])
+def test_ffn_backward_fp32_paths(act, counts, d, f, normal):
+    cfg, offs, w_up, w_dn, xp, d_yp = _inputs(counts, d, f, act, torch.float32, seed=d + f,
+                                              normal=normal)
+    d_xp, d_wu, d_wd = _run(cfg, offs, w_up, w_dn, xp, d_yp)
+    for e in range(len(counts)):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        ref_in, ref_wu, ref_wd = oracle.expert_ffn_backward(xp[lo:hi], w_up[e], w_dn[e],
+                                                            d_yp[lo:hi], act, f)
+        if hi > lo:
+            assert_rows_close(d_xp[lo:hi], ref_in, 1e-4)
+        assert_matrix_close(d_wu[e], ref_wu, 1e-4)
+        assert_matrix_close(d_wd[e], ref_wd, 1e-4)
 
 
 @pytest.mark.parametrize("act", ["gelu", "swiglu"])
