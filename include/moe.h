@@ -348,7 +348,10 @@ moe_status moe_dispatch_backward(const moe_config* cfg, const void* d_xp, const 
  * gradient is asked for).  ws supplies the device status word.
  * bf16: pre, dh and d_pre are rounded to bf16 once each; the three
  * contractions and the weight gradients run on the tensor cores with fp32
- * accumulation (each weight gradient rounded to bf16 once).  fp32: FFMA.
+ * accumulation (each weight gradient rounded to bf16 once).  fp32: the three
+ * contractions on the tensor cores as three tf32 products per product when d
+ * and d_ff are multiples of 16 (their operands split into tf32 parts in the
+ * scratch), else FFMA; the weight gradients on FFMA.
  * IDENTITY: d_xp = d_yp (weight gradients must be NULL, scratch unused).
  */
 size_t moe_expert_ffn_backward_scratch_size(const moe_config* cfg, int weight_grads);
