@@ -113,6 +113,23 @@ def test_workspace_size():
     assert moe.moe_workspace_size(big) > 131072 // 32 * 256 * 8
 
 
+def test_workspace_holds_the_tf32_split_of_fp32_experts():
+    """fp32 experts whose d and d_ff are multiples of 16 run on the tensor cores
+    from tf32 high / low parts kept in the workspace: 2 x 4 bytes per element of
+    the expert rows and of both weight stacks, 4 bytes per element of h (the
+    high part of h lives in the caller's h); other shapes, bf16 and identity
+    experts keep none."""
+    T, d, E, k, f = 4096, 512, 8, 2, 1024
+    split = 2 * 4 * (T * k * d + E * f * d + E * d * f) + 4 * T * k * f
+    base = moe.moe_workspace_size(_cfg(d_ff=1028))  # FFMA shape: no split sections
+    n = moe.moe_workspace_size(_cfg())
+    assert n - base >= split and n - base < split + 8 * 256
+    swiglu = moe.moe_workspace_size(_cfg(act="swiglu")) - moe.moe_workspace_size(_cfg(act="swiglu", d_ff=1028))
+    assert swiglu >= split + 2 * 4 * E * f * d  # the gate rows double W_up
+    for kw in (dict(dtype="bf16"), dict(act="identity", d_ff=0)):
+        assert moe.moe_workspace_size(_cfg(**kw)) < split
+
+
 def test_invalid_calls_fail_before_any_launch():
     """Argument errors come back synchronously, with no GPU touched."""
     c = _cfg()
