@@ -14,9 +14,10 @@ Tokens Move Between GPUs": route, dispatch, compute, combine.
 Pins: every function here is checked in ``tests/test_oracle_pins.py`` against
 something other than itself (the routing snippet's printed loads, the
 capacity example of the ai360xpert page, brute force, closed forms and
-library special cases).  The whole-layer composition has no printed values on
-the pages; beyond the per-step pins its end-to-end values are parity
-unpinned.
+library special cases).  The pages print no whole-layer output: the layer's
+composition is pinned against the dense-mixture definition computed with
+library matmuls (with and without a shared expert, where the activations are
+exactly the identity) and through the per-step pins.
 """
 from __future__ import annotations
 

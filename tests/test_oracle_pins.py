@@ -388,9 +388,10 @@ def test_layer_token_subset_equals_full():
 
 
 def test_layer_matches_dense_mixture_definition():
-    """Without drops, the layer equals the dense mixture sum_j g_j FFN_{e_j}(x)
-    + shared(x), computed token by token with library matmuls (the special case
-    where every pre-activation saturates GELU to the identity)."""
+    """Without drops or a shared expert, the layer equals the dense mixture
+    sum_j g_j FFN_{e_j}(x), computed token by token with library matmuls (the
+    special case where every pre-activation saturates GELU to the identity);
+    the shared-expert term is pinned by the two tests below."""
     T, d, E, k, f = 12, 24, 4, 2, 20
     g = torch.Generator().manual_seed(8)
     x = 1 + torch.randint(0, 9, (T, d), generator=g).float() / 8
